@@ -1,0 +1,370 @@
+"""CPU oracle of the MTP draft-layer forward (test infrastructure only).
+
+Plain, slow float64 numpy restatement of what the draft layer computes.  It
+exists to check the CUDA path: only the tests, the smoke check and the
+benchmark's CPU-baseline leg use it, and it shares no code with the CUDA
+path.  Every step follows the passage it cites; steps the pages leave open
+take the reading stated in the function's docstring.
+
+Pages cited (by title and item):
+  [mtp.rs]        hf2q 0.1.13 src/inference/models/qwen35/mtp.rs
+  [mimo_mtp.rs]   cortiq-engine 0.8.49 src/mimo_mtp.rs
+  [shared.rs]     hf2q 0.1.1 src/serve/forward_mlx_shared.rs
+
+Weights are mlx-affine 4-bit, group 32: ``q`` uint32 ``[N, K/8]``, ``s`` and
+``b`` float32 ``[N, K/32]``, element ``w[n, k] = s[n, k//32] * code + b[n,
+k//32]`` with the code of column ``k`` in bits ``4*(k%8) .. 4*(k%8)+3`` of
+word ``k//8``.
+"""
+
+from __future__ import annotations
+
+import numpy as np
+
+GROUP = 32
+PACK = 8
+_ROW_CHUNK = 8192
+
+
+# ---------------------------------------------------------------------------
+# Quantised weights
+# ---------------------------------------------------------------------------
+
+def unpack_codes(q: np.ndarray) -> np.ndarray:
+    """Integer codes ``[N, K]`` of a packed weight.
+
+    [shared.rs] ``MlxQWeight::from_mlx_affine_linear``: the code for column
+    ``8*kp + j`` sits at bits ``4*j .. 4*j+3`` of word ``kp`` (low nibble at
+    slot 0).
+    """
+    q = np.asarray(q, dtype=np.uint32)
+    n, kw = q.shape
+    shifts = (4 * np.arange(PACK, dtype=np.uint32))[None, None, :]
+    codes = (q[:, :, None] >> shifts) & np.uint32(0xF)
+    return codes.reshape(n, kw * PACK).astype(np.int64)
+
+
+def dequant(w) -> np.ndarray:
+    """Dense float64 ``[N, K]`` matrix ``s * code + b`` of an affine weight ``(q, s, b)``.
+
+    [shared.rs] ``MlxAffineExtra`` (per-group scales and biases ``[N,
+    K/group_size]``, bits 4, group 32) and the CPU reference in test
+    ``from_mlx_affine_linear_roundtrips_through_packed_kernel``
+    (``q * s + b`` per element).
+    """
+    q, s, b = w
+    codes = unpack_codes(q).astype(np.float64)
+    n, k = codes.shape
+    if k % GROUP:
+        raise ValueError("K must be a multiple of the group size 32")
+    s64 = np.repeat(np.asarray(s, dtype=np.float64), GROUP, axis=1)
+    b64 = np.repeat(np.asarray(b, dtype=np.float64), GROUP, axis=1)
+    if s64.shape != (n, k) or b64.shape != (n, k):
+        raise ValueError("scale/bias shape does not match [N, K/32]")
+    return codes * s64 + b64
+
+
+def weight_shape(w):
+    q, _, _ = w
+    return q.shape[0], q.shape[1] * PACK
+
+
+def qmatmul(x: np.ndarray, w, rows=None) -> np.ndarray:
+    """``y[r, n] = sum_k x[r, k] * w[n, k]`` for an affine weight, in float64.
+
+    [shared.rs] ``dispatch_qmatmul`` affine branch: ``y[m, N] = x[m, K] *
+    W^T`` with ``W`` dequantised per element.  Output rows are independent
+    dot products, so the matrix is dequantised a slab of rows at a time (or
+    only ``rows``) to bound memory; no sum is split or reordered.
+    """
+    q, s, b = w
+    x = np.atleast_2d(np.asarray(x, dtype=np.float64))
+    n, k = weight_shape(w)
+    if x.shape[1] != k:
+        raise ValueError(f"x has {x.shape[1]} columns, weight has K={k}")
+    sel = np.arange(n) if rows is None else np.asarray(rows, dtype=np.int64)
+    out = np.empty((x.shape[0], len(sel)), dtype=np.float64)
+    for lo in range(0, len(sel), _ROW_CHUNK):
+        r = sel[lo: lo + _ROW_CHUNK]
+        wd = dequant((q[r], s[r], b[r]))
+        out[:, lo: lo + len(r)] = x @ wd.T
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Normalisation, activations, rotary embedding
+# ---------------------------------------------------------------------------
+
+def rmsnorm(x: np.ndarray, w: np.ndarray, eps: float) -> np.ndarray:
+    """``x / sqrt(mean(x^2) + eps) * w`` over the last axis.
+
+    [mtp.rs] ``rms_norm_with_weight`` / ``dispatch_rms_norm`` (params
+    ``[eps, dim]``); [mimo_mtp.rs] ``inference::rms_norm_into``.  Reading:
+    the weight multiplies directly (no ``1 + w``).
+    """
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1, keepdims=True)
+    return x / np.sqrt(ms + eps) * np.asarray(w, dtype=np.float64)
+
+
+def sigmoid(z):
+    z = np.asarray(z, dtype=np.float64)
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def silu(z):
+    """``z * sigmoid(z)`` ([mimo_mtp.rs] ``Act::Silu`` of the dense MLP)."""
+    return np.asarray(z, dtype=np.float64) * sigmoid(z)
+
+
+def rope(x: np.ndarray, pos: int, theta: float, rot_dim: int) -> np.ndarray:
+    """Rotary embedding of one position over the last axis (half-split pairs).
+
+    [mtp.rs] ``apply_imrope`` with four equal text position ids; reading:
+    for text tokens this is 1-D RoPE at position ``pos``, rotating the pair
+    ``(x[i], x[i + R/2])`` by ``pos * theta^(-2i/R)`` for ``i < R/2`` with
+    ``R = rot_dim``; dimensions past ``R`` pass through.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    half = rot_dim // 2
+    i = np.arange(half, dtype=np.float64)
+    ang = pos * theta ** (-2.0 * i / rot_dim)
+    c, s = np.cos(ang), np.sin(ang)
+    out = x.copy()
+    a = x[..., :half]
+    bb = x[..., half:rot_dim]
+    out[..., :half] = a * c - bb * s
+    out[..., half:rot_dim] = a * s + bb * c
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Attention over the layer's own cache
+# ---------------------------------------------------------------------------
+
+def attention(q, k_all, v_all, q_pos, window=0, sinks=None, scale=None):
+    """Causal decode attention with an optional sliding window and sink logits.
+
+    ``q``: ``[m, nh, dqk]`` (already normed and rotated); ``k_all``/``v_all``:
+    ``[nkv, T, d]`` key/value rows at positions ``0 .. T-1``; ``q_pos[r]``
+    is the position of query row ``r``.
+
+    [mtp.rs] ``apply_sdpa_with_kv_cache`` (append then causal SDPA, grouped
+    KV heads) and [mimo_mtp.rs] module doc / ``qwen_attention_batch`` (window
+    128, per-head sinks).  Readings: query head ``h`` uses KV head
+    ``h // (nh/nkv)``; ``scale = 1/sqrt(dqk)``; the row at position ``p``
+    sees keys ``j`` with ``p - W < j <= p`` (all ``j <= p`` when ``W <=
+    0``); a sink is one extra logit per head, not scaled, that enters the
+    softmax denominator only.
+    """
+    q = np.asarray(q, dtype=np.float64)
+    k_all = np.asarray(k_all, dtype=np.float64)
+    v_all = np.asarray(v_all, dtype=np.float64)
+    m, nh, dqk = q.shape
+    nkv = k_all.shape[0]
+    group = nh // nkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(dqk)
+    out = np.zeros((m, nh, v_all.shape[2]), dtype=np.float64)
+    for r in range(m):
+        p = int(q_pos[r])
+        lo = 0 if window <= 0 else max(0, p - window + 1)
+        for h in range(nh):
+            kv = h // group
+            keys = k_all[kv, lo: p + 1]
+            vals = v_all[kv, lo: p + 1]
+            logits = scale * (keys @ q[r, h])
+            big = logits.max()
+            if sinks is not None:
+                big = max(big, float(sinks[h]))
+            e = np.exp(logits - big)
+            denom = e.sum()
+            if sinks is not None:
+                denom += np.exp(float(sinks[h]) - big)
+            out[r, h] = (e @ vals) / denom
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Feed-forward blocks
+# ---------------------------------------------------------------------------
+
+def swiglu(f, gate_w, up_w, down_w):
+    """``W_down (silu(W_gate f) * (W_up f))`` ([mtp.rs] ``build_dense_ffn_layer_gpu_q``)."""
+    g = qmatmul(f, gate_w)
+    u = qmatmul(f, up_w)
+    return qmatmul(silu(g) * u, down_w)
+
+
+def topk_lowest_index(p: np.ndarray, k: int) -> np.ndarray:
+    """Indices of the ``k`` largest entries; ties go to the lower index."""
+    order = sorted(range(len(p)), key=lambda i: (-p[i], i))
+    return np.array(order[:k], dtype=np.int64)
+
+
+def moe_route(f_row, router, top_k):
+    """Router of the MoE FFN for one row: ``(experts, weights)``.
+
+    [mtp.rs] ``MtpFfnWeightsGpu::Moe`` (router ``ffn_gate_inp``).  Reading:
+    softmax over all experts' logits ``router @ f``, keep the ``top_k``
+    largest (ties to the lower index), renormalise the kept weights to sum 1.
+    """
+    logits = np.asarray(router, dtype=np.float64) @ np.asarray(f_row, dtype=np.float64)
+    p = np.exp(logits - logits.max())
+    p /= p.sum()
+    sel = topk_lowest_index(p, top_k)
+    wsel = p[sel] / p[sel].sum()
+    return sel, wsel
+
+
+def moe_ffn(f, w, cfg):
+    """Routed experts plus a gated shared expert, per row ``f[r]``.
+
+    [mtp.rs] ``MtpFfnWeightsGpu::Moe`` (8 tensors: router, stacked expert
+    gate/up/down, and four shared-expert tensors) and
+    ``build_moe_ffn_layer_gpu_q_into``; [shared.rs] ``MlxAffineMoeStack``
+    (expert ``e`` of a stack is slab ``[e]`` of ``[E, N, K/8]``).  Reading:
+    ``sum_e p_e * SwiGLU_e(f) + sigmoid(w_sg . f) * SwiGLU_shared(f)``.
+    """
+    f = np.atleast_2d(np.asarray(f, dtype=np.float64))
+    out = np.zeros((f.shape[0], cfg.hidden), dtype=np.float64)
+    eg, eu, ed = w["exp_gate"], w["exp_up"], w["exp_down"]
+    for r in range(f.shape[0]):
+        sel, wsel = moe_route(f[r], w["router"], cfg.top_k)
+        acc = np.zeros(cfg.hidden, dtype=np.float64)
+        for e, pe in zip(sel, wsel):
+            ex = lambda t: (t[0][e], t[1][e], t[2][e])  # noqa: E731
+            acc += pe * swiglu(f[r], ex(eg), ex(eu), ex(ed))[0]
+        gate = sigmoid(np.asarray(w["sh_gate_inp"], dtype=np.float64) @ f[r])
+        acc += gate * swiglu(f[r], w["sh_gate"], w["sh_up"], w["sh_down"])[0]
+        out[r] = acc
+    return out
+
+
+# ---------------------------------------------------------------------------
+# Greedy head
+# ---------------------------------------------------------------------------
+
+def argmax_lowest(v: np.ndarray):
+    """``(index, value, top-2 margin)``; ties go to the lowest index.
+
+    [mtp.rs] ``forward_shared_head_greedy`` (argmax over the vocabulary
+    logits, returning index and value).
+    """
+    v = np.asarray(v, dtype=np.float64)
+    idx = int(np.argmax(v))  # numpy returns the first maximal index
+    val = float(v[idx])
+    rest = np.delete(v, idx)
+    margin = float(val - rest.max()) if rest.size else float("inf")
+    return idx, val, margin
+
+
+# ---------------------------------------------------------------------------
+# One draft layer
+# ---------------------------------------------------------------------------
+
+def draft_layer(cfg, w, lm_head, k_cache, v_cache, hidden, embed_rows, pos0=None,
+                want_logits=True):
+    """One MTP draft-layer step over ``m`` rows.
+
+    Follows [mimo_mtp.rs] module doc (the four-line layer statement) with
+    the step order of [mtp.rs] ``forward_draft_body``:
+
+    1. ``project_embedding_and_hidden``: ``e_n = RMSNorm(e) * enorm``,
+       ``h_n = RMSNorm(h) * hnorm`` (eps 1e-6), ``u = eh_proj [e_n ; h_n]``
+       (embedding first).
+    2. ``forward_full_attention``: ``x = RMSNorm(u) * attn_norm``; ``q``
+       (and, when gated, ``gate``), ``k``, ``v`` projections; per-head q/k
+       RMSNorm with a ``[dqk]`` weight when present; RoPE at position
+       ``pos0 + r``; append ``k``, ``v`` to the cache; attention; ``o *=
+       sigmoid(gate)`` when gated; ``u1 = u + W_o o``.  Reading for the gated
+       projection: ``W_q`` has ``2*nh*dqk`` rows, head ``h`` owning rows
+       ``[2*h*dqk, 2*h*dqk + dqk)`` for the query and the next ``dqk`` rows
+       for its gate.
+    3. ``forward_ffn_residual``: ``f = RMSNorm(u1) * post_norm``; ``u2 = u1
+       + FFN(f)``.
+    4. ``forward_shared_head_greedy`` on the last row ([mimo_mtp.rs]
+       ``mimo_mtp_draft``: only row ``n-1`` reaches the head): ``y =
+       RMSNorm(u2[-1]) * final_norm``, logits ``= lm_head y``, token =
+       argmax.  ``y`` is also the hidden a chained step consumes ([mtp.rs]
+       ``forward_draft_with_hidden``).
+
+    ``k_cache``/``v_cache`` are ``[nkv, cap, d]`` with rows ``< pos0``
+    filled; they are not modified (the appended rows are returned).
+    """
+    eps = cfg.eps
+    H, nh, nkv, dqk, dv = cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim_qk, cfg.head_dim_v
+    hidden = np.atleast_2d(np.asarray(hidden, dtype=np.float64))
+    embed_rows = np.atleast_2d(np.asarray(embed_rows, dtype=np.float64))
+    m = hidden.shape[0]
+    L = cfg.cache_len if pos0 is None else pos0
+
+    # 1. embedding / hidden projection
+    e_n = rmsnorm(embed_rows, w["enorm"], 1e-6)
+    h_n = rmsnorm(hidden, w["hnorm"], 1e-6)
+    u = qmatmul(np.concatenate([e_n, h_n], axis=1), w["eh_proj"])
+
+    # 2. attention
+    x = rmsnorm(u, w["attn_norm"], eps)
+    qf = qmatmul(x, w["wq"])
+    if cfg.gated_q:
+        qg = qf.reshape(m, nh, 2, dqk)
+        q, gate = qg[:, :, 0, :], qg[:, :, 1, :]
+    else:
+        q, gate = qf.reshape(m, nh, dqk), None
+    k = qmatmul(x, w["wk"]).reshape(m, nkv, dqk)
+    v = qmatmul(x, w["wv"]).reshape(m, nkv, dv)
+    if cfg.qk_norm:
+        q = rmsnorm(q, w["q_norm"], eps)
+        k = rmsnorm(k, w["k_norm"], eps)
+    q = np.stack([rope(q[r], L + r, cfg.rope_theta, cfg.rot_dim) for r in range(m)])
+    k = np.stack([rope(k[r], L + r, cfg.rope_theta, cfg.rot_dim) for r in range(m)])
+    k_all = np.concatenate([np.asarray(k_cache, np.float64)[:, :L], k.transpose(1, 0, 2)], axis=1)
+    v_all = np.concatenate([np.asarray(v_cache, np.float64)[:, :L], v.transpose(1, 0, 2)], axis=1)
+    o = attention(q, k_all, v_all, [L + r for r in range(m)], cfg.window,
+                  w.get("sinks") if cfg.sinks else None)
+    if gate is not None:
+        o = o * sigmoid(gate)
+    u1 = u + qmatmul(o.reshape(m, nh * dv), w["wo"])
+
+    # 3. FFN
+    f = rmsnorm(u1, w["post_norm"], eps)
+    if cfg.moe:
+        u2 = u1 + moe_ffn(f, w, cfg)
+    else:
+        u2 = u1 + swiglu(f, w["ffn_gate"], w["ffn_up"], w["ffn_down"])
+
+    # 4. greedy shared head on the last row
+    y = rmsnorm(u2[-1], w["final_norm"], eps)
+    out = {"u": u, "u1": u1, "u2": u2, "hidden_out": y, "k_new": k, "v_new": v,
+           "q_roped": q, "attn": o}
+    if want_logits:
+        logits = qmatmul(y[None, :], lm_head)[0]
+        tok, val, margin = argmax_lowest(logits)
+        out.update(logits=logits, token=tok, value=val, margin=margin)
+    return out
+
+
+def draft_chain(cfg, layers, lm_head, embed, caches, hidden, tokens, forced=None):
+    """The three-layer chained draft of one speculative round.
+
+    [mimo_mtp.rs] module doc ("How the three layers chain") and
+    ``mimo_mtp_draft``: layer ``k`` takes the same target hiddens ``h_j``
+    for every layer; its row ``i`` embeds token ``seq[i + k]`` where ``seq``
+    is the known tokens followed by this round's drafts; the draft of layer
+    ``k`` is the argmax of its last row.  ``embed(tok)`` returns one
+    embedding row.  ``forced[k]``, when given, replaces draft ``k`` for the
+    later layers (used when a near-tie allows either token).
+    """
+    m = cfg.m
+    seq = [int(t) for t in tokens]
+    results = []
+    for k, (w, (kc, vc)) in enumerate(zip(layers, caches)):
+        toks = seq[k: k + m]
+        e = np.stack([embed(t) for t in toks])
+        res = draft_layer(cfg, w, lm_head, kc, vc, hidden, e)
+        res["tokens_in"] = toks
+        results.append(res)
+        nxt = res["token"] if forced is None or forced[k] is None else int(forced[k])
+        seq.append(nxt)
+    return results

@@ -1,0 +1,442 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each test ties one oracle function to what the pages or the mathematics fix:
+the pages' printed fixtures checked by brute force, closed forms, invariants
+and special cases.  A plausible slip in the oracle (a dropped term, a wrong
+sign or index, a transposed operand, the wrong nibble order) fails one of
+them.
+"""
+
+import math
+
+import numpy as np
+import pytest
+
+import mtp_synth
+from golden.fixtures import affine_fixture, affine_fixture_shapes
+from oracle import mtp_oracle as O
+from mtp_synth.configs import CONFIGS, make_layer_weights, make_shared, make_state, make_step
+
+
+# ---------------------------------------------------------------------------
+# generator
+# ---------------------------------------------------------------------------
+
+def test_splitmix64_published_first_output():
+    # SplitMix64 seeded with 0: the first output of Vigna's reference code.
+    z = np.array([mtp_synth.GOLDEN], dtype=np.uint64)
+    assert int(mtp_synth._mix(z)[0]) == 0xE220A8397B1DCDAF
+
+
+def test_generator_slices_match_whole():
+    whole = mtp_synth.normal(7, "t", 101)
+    for start in (0, 1, 2, 33, 64):
+        part = mtp_synth.normal(7, "t", 101 - start, start=start)
+        assert np.array_equal(part, whole[start:])
+    rows = mtp_synth.embedding_rows(7, "e", 50, 12, rows=[3, 0, 49])
+    table = mtp_synth.embedding_rows(7, "e", 50, 12)
+    assert np.array_equal(rows, table[[3, 0, 49]])
+
+
+def test_generator_distributions():
+    z = mtp_synth.normal(1, "n", 200000)
+    assert abs(z.mean()) < 0.01 and abs(z.std() - 1.0) < 0.01
+    q, s, b = mtp_synth.affine4_weight(1, "w", 64, 256)
+    codes = O.unpack_codes(q)
+    assert codes.min() == 0 and codes.max() == 15
+    assert abs(codes.mean() - 7.5) < 0.1
+    assert np.all(s >= 0)
+    assert abs(float(np.mean(b + 8 * s))) < 1e-3
+
+
+# ---------------------------------------------------------------------------
+# packed codes and affine matmul
+# ---------------------------------------------------------------------------
+
+def test_unpack_low_nibble_first():
+    # [shared.rs] from_mlx_affine_linear: column 8*kp+j at bits 4j..4j+3.
+    q = np.array([[0x76543210, 0xFEDCBA98]], dtype=np.uint32)
+    assert O.unpack_codes(q).tolist() == [list(range(16))]
+
+
+def test_pack_unpack_roundtrip_page_fixture():
+    for m, n, k, _ in affine_fixture_shapes():
+        codes, _, _, _ = affine_fixture(m, n, k)
+        assert np.array_equal(O.unpack_codes(mtp_synth.pack_codes(codes)), codes)
+
+
+def test_dequant_single_word():
+    q = np.zeros((1, 4), dtype=np.uint32)
+    q[0, 0] = 0xF0000000          # column 7 has code 15, all others 0
+    s = np.array([[2.0]], dtype=np.float32)
+    b = np.array([[1.0]], dtype=np.float32)
+    w = O.dequant((q, s, b))
+    expect = np.ones(32)
+    expect[7] = 31.0
+    assert np.array_equal(w[0], expect)
+
+
+def _brute_qmatmul(codes, scales, biases, x, group=32):
+    # Element-by-element loop of the page's CPU reference, from unpacked codes.
+    m, k = x.shape
+    n = codes.shape[0]
+    y = [[0.0] * n for _ in range(m)]
+    for r in range(m):
+        for col in range(n):
+            acc = 0.0
+            for kk in range(k):
+                g = kk // group
+                wv = float(codes[col, kk]) * float(scales[col, g]) + float(biases[col, g])
+                acc += float(x[r, kk]) * wv
+            y[r][col] = acc
+    return np.array(y)
+
+
+@pytest.mark.parametrize("shape", affine_fixture_shapes())
+def test_qmatmul_page_fixtures_brute_force(shape):
+    m, n, k, tol = shape
+    codes, s, b, x = affine_fixture(m, n, k)
+    w = (mtp_synth.pack_codes(codes), s, b)
+    got = O.qmatmul(x, w)
+    ref = _brute_qmatmul(codes, s, b, x)
+    assert got.shape == (m, n)
+    assert np.max(np.abs(got - ref)) < 1e-9          # same math, f64 both sides
+    assert np.max(np.abs(got - ref)) < tol
+
+
+def test_qmatmul_special_cases():
+    rng = np.random.default_rng(0)
+    n, k = 5, 64
+    codes = rng.integers(0, 16, size=(n, k))
+    x = rng.standard_normal((3, k))
+    q = mtp_synth.pack_codes(codes)
+    # s = 0: y = b * sum(x) per group
+    b = rng.standard_normal((n, k // 32)).astype(np.float32)
+    y = O.qmatmul(x, (q, np.zeros_like(b), b))
+    xs = x.reshape(3, k // 32, 32).sum(axis=2)
+    assert np.allclose(y, xs @ b.astype(np.float64).T, rtol=0, atol=1e-12)
+    # code 8 everywhere and b = -8 s: the weight is exactly zero
+    q8 = mtp_synth.pack_codes(np.full((n, k), 8))
+    s = np.abs(rng.standard_normal((n, k // 32))).astype(np.float32)
+    assert np.all(O.qmatmul(x, (q8, s, (-8.0 * s).astype(np.float32))) == 0.0)
+    # rows selection equals the full product's columns
+    w = (q, s, b)
+    assert np.allclose(O.qmatmul(x, w, rows=[4, 1]), O.qmatmul(x, w)[:, [4, 1]], rtol=1e-14, atol=0)
+
+
+def test_qmatmul_orientation():
+    # y = x W^T: one nonzero weight row picks out one output column.
+    n, k = 3, 32
+    codes = np.zeros((n, k), dtype=np.int64)
+    codes[2, 5] = 1
+    s = np.zeros((n, 1), np.float32)
+    s[2, 0] = 1.0
+    x = np.arange(k, dtype=np.float64)[None, :]
+    y = O.qmatmul(x, (mtp_synth.pack_codes(codes), s, np.zeros((n, 1), np.float32)))
+    assert y.tolist() == [[0.0, 0.0, 5.0]]
+
+
+# ---------------------------------------------------------------------------
+# RMSNorm, activations, RoPE
+# ---------------------------------------------------------------------------
+
+def test_rmsnorm_closed_forms():
+    w = np.array([2.0, -1.0])
+    y = O.rmsnorm(np.array([3.0, 4.0]), w, 0.0)
+    assert np.allclose(y, np.array([3.0, 4.0]) / math.sqrt(12.5) * w, rtol=1e-15)
+    c, eps = 0.3, 1e-6
+    y = O.rmsnorm(np.full(8, c), np.ones(8), eps)
+    assert np.allclose(y, c / math.sqrt(c * c + eps), rtol=1e-15)
+    x = np.random.default_rng(1).standard_normal(64)
+    assert np.allclose(O.rmsnorm(5.0 * x, np.ones(64), 0.0), O.rmsnorm(x, np.ones(64), 0.0))
+    # rows are normalised independently
+    xx = np.stack([x, 3 * x + 1])
+    assert np.allclose(O.rmsnorm(xx, np.ones(64), eps)[1], O.rmsnorm(3 * x + 1, np.ones(64), eps))
+
+
+def test_sigmoid_silu_values():
+    assert O.sigmoid(0.0) == 0.5
+    assert abs(O.silu(1.0) - 1.0 / (1.0 + math.exp(-1.0))) < 1e-15
+    assert abs(O.silu(-2.0) - (-2.0 / (1.0 + math.exp(2.0)))) < 1e-15
+
+
+def test_rope_pairing_and_sign():
+    p, theta = 3, 1e4
+    y = O.rope(np.array([1.0, 0.0, 0.0, 0.0]), p, theta, 4)
+    assert np.allclose(y, [math.cos(p), 0.0, math.sin(p), 0.0], atol=1e-15)
+    t1 = theta ** -0.5
+    y = O.rope(np.array([0.0, 1.0, 0.0, 0.0]), p, theta, 4)
+    assert np.allclose(y, [0.0, math.cos(p * t1), 0.0, math.sin(p * t1)], atol=1e-15)
+    # dimensions past rot_dim pass through
+    y = O.rope(np.array([1.0, 2.0, 3.0, 4.0, 5.0, 6.0]), p, theta, 4)
+    assert y[4] == 5.0 and y[5] == 6.0
+
+
+def test_rope_invariants():
+    rng = np.random.default_rng(2)
+    q = rng.standard_normal(64)
+    k = rng.standard_normal(64)
+    assert np.allclose(O.rope(q, 0, 1e6, 64), q, rtol=0, atol=0)
+    r = O.rope(q, 17, 1e6, 64)
+    assert np.allclose(r[:32] ** 2 + r[32:] ** 2, q[:32] ** 2 + q[32:] ** 2)
+    d1 = O.rope(q, 40, 1e6, 64) @ O.rope(k, 33, 1e6, 64)
+    d2 = O.rope(q, 1007, 1e6, 64) @ O.rope(k, 1000, 1e6, 64)
+    assert abs(d1 - d2) < 1e-9
+
+
+# ---------------------------------------------------------------------------
+# attention
+# ---------------------------------------------------------------------------
+
+def _brute_attention(q, k_all, v_all, q_pos, window, sinks):
+    m, nh, d = q.shape
+    nkv, _, dv = v_all.shape
+    out = np.zeros((m, nh, dv))
+    for r in range(m):
+        p = q_pos[r]
+        for h in range(nh):
+            kv = h * nkv // nh
+            keys = [j for j in range(p + 1) if window <= 0 or j > p - window]
+            ls = [sum(q[r, h, i] * k_all[kv, j, i] for i in range(d)) / math.sqrt(d) for j in keys]
+            cands = ls + ([float(sinks[h])] if sinks is not None else [])
+            mx = max(cands)
+            ws = [math.exp(v - mx) for v in ls]
+            den = sum(ws) + (math.exp(float(sinks[h]) - mx) if sinks is not None else 0.0)
+            for c in range(dv):
+                out[r, h, c] = sum(wj * v_all[kv, j, c] for wj, j in zip(ws, keys)) / den
+    return out
+
+
+@pytest.mark.parametrize("window,use_sinks", [(0, False), (3, True), (5, False), (2, True)])
+def test_attention_brute_force(window, use_sinks):
+    rng = np.random.default_rng(3)
+    nh, nkv, d, dv, T, m = 4, 2, 6, 5, 9, 3
+    q = rng.standard_normal((m, nh, d))
+    k_all = rng.standard_normal((nkv, T, d))
+    v_all = rng.standard_normal((nkv, T, dv))
+    pos = [T - m + r for r in range(m)]
+    sinks = rng.standard_normal(nh) if use_sinks else None
+    got = O.attention(q, k_all, v_all, pos, window, sinks)
+    ref = _brute_attention(q, k_all, v_all, pos, window, sinks)
+    assert np.max(np.abs(got - ref)) < 1e-12
+
+
+def test_attention_invariants():
+    rng = np.random.default_rng(4)
+    nh, nkv, d, T, m = 4, 2, 8, 12, 2
+    q = rng.standard_normal((m, nh, d))
+    k_all = rng.standard_normal((nkv, T, d))
+    v_all = rng.standard_normal((nkv, T, d))
+    pos = [T - 2, T - 1]
+    full = O.attention(q, k_all, v_all, pos, 0, None)
+    assert np.allclose(O.attention(q, k_all, v_all, pos, T + 5, None), full, rtol=0, atol=1e-15)
+    assert np.allclose(O.attention(q, k_all, v_all, pos, 0, np.full(nh, -1e30)), full, atol=1e-15)
+    # a window of one: each row sees only its own key
+    one = O.attention(q, k_all, v_all, pos, 1, None)
+    for r, p in enumerate(pos):
+        for h in range(nh):
+            assert np.allclose(one[r, h], v_all[h // 2, p])
+    # one key with a sink: o = v * sigmoid(l - sink)
+    k1, v1 = k_all[:, :1], v_all[:, :1]
+    sinks = rng.standard_normal(nh)
+    o = O.attention(q[:1], k1, v1, [0], 0, sinks)
+    for h in range(nh):
+        logit = (q[0, h] @ k1[h // 2, 0]) / math.sqrt(d)
+        assert np.allclose(o[0, h], v1[h // 2, 0] / (1.0 + math.exp(sinks[h] - logit)))
+    # identical keys: o = mean of the visible values
+    ke = np.repeat(k_all[:, :1], T, axis=1)
+    o = O.attention(q, ke, v_all, pos, 0, None)
+    assert np.allclose(o[1, 0], v_all[0, :T].mean(axis=0))
+    # grouped KV heads: heads 0,1 read KV head 0, heads 2,3 read KV head 1
+    v2 = v_all.copy()
+    v2[1] += 1.0
+    o2 = O.attention(q, k_all, v2, pos, 0, None)
+    assert np.allclose(o2[:, :2], full[:, :2]) and np.allclose(o2[:, 2:], full[:, 2:] + 1.0)
+
+
+# ---------------------------------------------------------------------------
+# feed-forward and routing
+# ---------------------------------------------------------------------------
+
+def _tiny_affine(rng, n, k):
+    codes = rng.integers(0, 16, size=(n, k))
+    s = (np.abs(rng.standard_normal((n, k // 32))) * 0.01).astype(np.float32)
+    b = (-8 * s + 1e-3 * rng.standard_normal((n, k // 32))).astype(np.float32)
+    return mtp_synth.pack_codes(codes), s, b
+
+
+def test_swiglu_composition():
+    rng = np.random.default_rng(5)
+    H, I = 64, 32
+    g, u, d = _tiny_affine(rng, I, H), _tiny_affine(rng, I, H), _tiny_affine(rng, H, I)
+    f = rng.standard_normal((2, H))
+    G, U, D = O.dequant(g), O.dequant(u), O.dequant(d)
+    a = f @ G.T
+    ref = ((a / (1 + np.exp(-a))) * (f @ U.T)) @ D.T
+    assert np.allclose(O.swiglu(f, g, u, d), ref, rtol=1e-12, atol=1e-14)
+
+
+def _tiny_moe(rng, E=6, H=64, Ie=32, Is=32, top_k=2):
+    cfg = CONFIGS["moe"].with_(hidden=H, n_experts=E, top_k=top_k, expert_intermediate=Ie,
+                               shared_intermediate=Is)
+    w = {"router": rng.standard_normal((E, H)) * 0.3}
+    for name, (n, k) in (("exp_gate", (Ie, H)), ("exp_up", (Ie, H)), ("exp_down", (H, Ie))):
+        parts = [_tiny_affine(rng, n, k) for _ in range(E)]
+        w[name] = tuple(np.stack([p[i] for p in parts]) for i in range(3))
+    w["sh_gate"], w["sh_up"], w["sh_down"] = (_tiny_affine(rng, Is, H), _tiny_affine(rng, Is, H),
+                                              _tiny_affine(rng, H, Is))
+    w["sh_gate_inp"] = rng.standard_normal(H) * 0.1
+    return cfg, w
+
+
+def _expert(w, e):
+    return {k: (w[k][0][e], w[k][1][e], w[k][2][e]) for k in ("exp_gate", "exp_up", "exp_down")}
+
+
+def test_moe_all_experts_is_dense_mixture():
+    rng = np.random.default_rng(6)
+    cfg, w = _tiny_moe(rng, top_k=6)
+    f = rng.standard_normal(cfg.hidden)
+    logits = w["router"] @ f
+    p = np.exp(logits - logits.max())
+    p /= p.sum()
+    ref = np.zeros(cfg.hidden)
+    for e in range(cfg.n_experts):
+        ex = _expert(w, e)
+        ref += p[e] * O.swiglu(f, ex["exp_gate"], ex["exp_up"], ex["exp_down"])[0]
+    ref += O.sigmoid(w["sh_gate_inp"] @ f) * O.swiglu(f, w["sh_gate"], w["sh_up"], w["sh_down"])[0]
+    assert np.allclose(O.moe_ffn(f, w, cfg)[0], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_moe_one_hot_router_and_shared_gate():
+    rng = np.random.default_rng(7)
+    cfg, w = _tiny_moe(rng, top_k=1)
+    f = rng.standard_normal(cfg.hidden)
+    w["router"] = np.zeros((cfg.n_experts, cfg.hidden))
+    w["router"][4] = f * 50.0          # expert 4 dominates
+    w["sh_gate_inp"] = np.zeros(cfg.hidden)   # shared gate = sigmoid(0) = 1/2
+    ex = _expert(w, 4)
+    ref = O.swiglu(f, ex["exp_gate"], ex["exp_up"], ex["exp_down"])[0] \
+        + 0.5 * O.swiglu(f, w["sh_gate"], w["sh_up"], w["sh_down"])[0]
+    assert np.allclose(O.moe_ffn(f, w, cfg)[0], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_moe_route_topk_renormalised_and_ties():
+    sel = O.topk_lowest_index(np.array([0.1, 0.3, 0.3, 0.05, 0.3]), 2)
+    assert sel.tolist() == [1, 2]
+    router = np.eye(5)
+    f = np.array([0.0, 1.0, 3.0, 2.0, 0.5])
+    sel, wsel = O.moe_route(f, router, 2)
+    assert sel.tolist() == [2, 3]
+    assert np.allclose(wsel, [math.e / (math.e + 1), 1 / (math.e + 1)])
+
+
+# ---------------------------------------------------------------------------
+# argmax
+# ---------------------------------------------------------------------------
+
+def test_argmax_lowest_index():
+    v = np.zeros(1000)
+    v[737] = 2.0
+    assert O.argmax_lowest(v)[:2] == (737, 2.0)
+    v[12] = 2.0
+    idx, val, margin = O.argmax_lowest(v)
+    assert idx == 12 and margin == 0.0
+    idx, val, margin = O.argmax_lowest(np.array([1.0, 3.0, 2.5]))
+    assert (idx, val, margin) == (1, 3.0, 0.5)
+
+
+# ---------------------------------------------------------------------------
+# whole layer and chain
+# ---------------------------------------------------------------------------
+
+def _tiny_cfg(**kw):
+    base = CONFIGS["tiny_dense"].with_(hidden=64, n_heads=4, n_kv_heads=2, head_dim_qk=32,
+                                       head_dim_v=32, intermediate=64, vocab=96, cache_len=5)
+    return base.with_(**kw)
+
+
+def _zero(w):
+    q, s, b = w
+    return q, np.zeros_like(s), np.zeros_like(b)
+
+
+def test_layer_reduces_to_projection_and_head():
+    cfg = _tiny_cfg()
+    w = make_layer_weights(cfg)
+    sh = make_shared(cfg)
+    st = make_state(cfg)
+    step = make_step(cfg)
+    w["wo"] = _zero(w["wo"])
+    w["ffn_down"] = _zero(w["ffn_down"])
+    e = sh["embed"][step["tokens"]]
+    res = O.draft_layer(cfg, w, sh["lm_head"], st["k_cache"], st["v_cache"], step["hidden"], e)
+    cat = np.concatenate([O.rmsnorm(e, w["enorm"], 1e-6), O.rmsnorm(step["hidden"], w["hnorm"], 1e-6)], 1)
+    u = cat @ O.dequant(w["eh_proj"]).T
+    y = O.rmsnorm(u[-1], w["final_norm"], cfg.eps)
+    logits = O.dequant(sh["lm_head"]) @ y
+    assert np.allclose(res["u2"], u, rtol=1e-12, atol=1e-12)
+    assert np.allclose(res["hidden_out"], y, rtol=1e-12, atol=1e-12)
+    assert np.allclose(res["logits"], logits, rtol=1e-12, atol=1e-12)
+    assert res["token"] == int(np.argmax(logits))
+
+
+def test_layer_embedding_comes_first():
+    cfg = _tiny_cfg()
+    w = make_layer_weights(cfg)
+    sh = make_shared(cfg)
+    st = make_state(cfg)
+    step = make_step(cfg)
+    q, s, b = w["eh_proj"]
+    s, b = s.copy(), b.copy()
+    H = cfg.hidden
+    s[:, H // 32:] = 0.0          # columns H..2H (the hidden half) contribute nothing
+    b[:, H // 32:] = 0.0
+    w["eh_proj"] = (q, s, b)
+    e = sh["embed"][step["tokens"]]
+    r1 = O.draft_layer(cfg, w, sh["lm_head"], st["k_cache"], st["v_cache"], step["hidden"], e)
+    r2 = O.draft_layer(cfg, w, sh["lm_head"], st["k_cache"], st["v_cache"], -3 * step["hidden"], e)
+    assert np.allclose(r1["u"], r2["u"], rtol=0, atol=1e-14)
+    e_n = O.rmsnorm(e, w["enorm"], 1e-6)
+    assert np.allclose(r1["u"], e_n @ O.dequant((q[:, :H // 8], s[:, :H // 32], b[:, :H // 32])).T)
+
+
+def test_layer_attention_single_key_and_gate():
+    # Empty cache: the only key is the row itself, so o = v (then gated).
+    cfg = _tiny_cfg(cache_len=0, gated_q=True)
+    w = make_layer_weights(cfg)
+    sh = make_shared(cfg)
+    st = make_state(cfg)
+    step = make_step(cfg)
+    e = sh["embed"][step["tokens"]]
+    res = O.draft_layer(cfg, w, sh["lm_head"], st["k_cache"], st["v_cache"], step["hidden"], e)
+    x = O.rmsnorm(res["u"], w["attn_norm"], cfg.eps)
+    qf = (x @ O.dequant(w["wq"]).T).reshape(cfg.n_heads, 2, cfg.head_dim_qk)
+    v = (x @ O.dequant(w["wv"]).T).reshape(cfg.n_kv_heads, cfg.head_dim_v)
+    o = np.stack([v[h // 2] for h in range(cfg.n_heads)]) * O.sigmoid(qf[:, 1, :])
+    u1 = res["u"] + o.reshape(1, -1) @ O.dequant(w["wo"]).T
+    assert np.allclose(res["u1"], u1, rtol=1e-12, atol=1e-12)
+    # the appended key is normed then rotated at position 0 (identity)
+    k = (x @ O.dequant(w["wk"]).T).reshape(cfg.n_kv_heads, cfg.head_dim_qk)
+    assert np.allclose(res["k_new"][0], O.rmsnorm(k, w["k_norm"], cfg.eps))
+
+
+def test_chain_rows_take_earlier_drafts():
+    cfg = _tiny_cfg(m=4, n_layers=3, window=3, sinks=True, qk_norm=False, head_dim_qk=48,
+                    cache_len=6, name="tiny_chain")
+    layers = [make_layer_weights(cfg, k) for k in range(3)]
+    sh = make_shared(cfg)
+    caches = [(make_state(cfg, k)["k_cache"], make_state(cfg, k)["v_cache"]) for k in range(3)]
+    step = make_step(cfg)
+    embed = lambda t: sh["embed"][t]  # noqa: E731
+    res = O.draft_chain(cfg, layers, sh["lm_head"], embed, caches, step["hidden"], step["tokens"])
+    seq = list(step["tokens"]) + [r["token"] for r in res]
+    for k in range(3):
+        assert res[k]["tokens_in"] == seq[k: k + 4]
+        e = sh["embed"][seq[k: k + 4]]
+        alone = O.draft_layer(cfg, layers[k], sh["lm_head"], *caches[k], step["hidden"], e)
+        assert alone["token"] == res[k]["token"]
+    forced = [5, 7, None]
+    res2 = O.draft_chain(cfg, layers, sh["lm_head"], embed, caches, step["hidden"], step["tokens"],
+                         forced)
+    assert res2[1]["tokens_in"][-1] == 5 and res2[2]["tokens_in"][-2:] == [5, 7]
