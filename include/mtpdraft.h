@@ -1,0 +1,277 @@
+/*
+ * mtpdraft.h -- C ABI of the MTP draft-layer forward on one sm_103a GPU.
+ *
+ * The draft layer (multi-token-prediction "NextN" block) drafts the next
+ * token for speculative greedy decoding:
+ *
+ *   u   = eh_proj . [RMSNorm(embed(tok)) * enorm ; RMSNorm(hid) * hnorm]
+ *   u1  = u  + o_proj(attn(RMSNorm(u) * attn_norm))     (own KV cache)
+ *   u2  = u1 + FFN(RMSNorm(u1) * post_norm)            (SwiGLU or MoE)
+ *   tok = argmax(lm_head(RMSNorm(u2) * final_norm))
+ *
+ * as stated in the module documentation of "cortiq-engine 0.8.49
+ * src/mimo_mtp.rs" and implemented step by step in "hf2q 0.1.13
+ * src/inference/models/qwen35/mtp.rs" (forward_draft_body,
+ * project_embedding_and_hidden, forward_full_attention,
+ * forward_ffn_residual, forward_shared_head_greedy).
+ *
+ * Every projection uses mlx-affine 4-bit group-32 weights ("hf2q 0.1.1
+ * src/serve/forward_mlx_shared.rs", MlxAffineExtra / MlxQWeight): codes
+ * uint32 [N][K/8] with the code of column 8*j+i in bits 4i..4i+3 of word j,
+ * float32 scales and biases [N][K/32], w[n][k] = s*code + b.
+ *
+ * Conventions for every entry point:
+ *  - Pointers named d_* or documented as device are device pointers owned by
+ *    the caller; host pointers are named h_* or are descriptor structs.  The
+ *    library never allocates device memory and keeps no state between calls.
+ *  - All work is enqueued on `stream` (a cudaStream_t, NULL = legacy
+ *    default stream); no call synchronises the device, so calls can be
+ *    captured into a CUDA graph (tensor maps are encoded on the host at
+ *    enqueue time and baked into the launch).
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns a non-zero mtp_status and launches nothing.
+ *    mtp_last_error() then returns a thread-local message.
+ *  - Device activations are float32, row-major.
+ *  - Device pointers must be 16-byte aligned.  Reduction lengths K must be
+ *    multiples of 32; entry points that take a workspace state their extra
+ *    shape rules.
+ *  - Workspaces are caller-owned device buffers of at least the size the
+ *    matching *_workspace_bytes() function returns.  Before its first use a
+ *    workspace must be cleared once with mtp_workspace_init(); kernels leave
+ *    it in that state again when they finish.  Calls that share a workspace
+ *    must not overlap on the GPU.
+ */
+#ifndef MTPDRAFT_H
+#define MTPDRAFT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MTPDRAFT_VERSION 1
+
+typedef enum {
+    MTP_OK = 0,
+    MTP_ERR_INVALID_ARG = 1,   /* null pointer, bad shape, misaligned pointer */
+    MTP_ERR_UNSUPPORTED = 2,   /* a shape the kernels do not implement */
+    MTP_ERR_CAPACITY = 3,      /* cache_len + m exceeds the cache capacity */
+    MTP_ERR_WORKSPACE = 4,     /* workspace missing or too small */
+    MTP_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+    MTP_ERR_DEVICE_TIMEOUT = 6 /* a bounded device-side wait gave up (see mtp_workspace_status) */
+} mtp_status;
+
+/* One affine 4-bit group-32 weight [n][k] (device pointers). */
+typedef struct {
+    const uint32_t *q;   /* [n][k/8] packed codes, low nibble first */
+    const float *s;      /* [n][k/32] scales */
+    const float *b;      /* [n][k/32] biases */
+    int32_t n;
+    int32_t k;
+} mtp_affine4;
+
+/* Thread-local description of the last failure on this thread ("" if none). */
+const char *mtp_last_error(void);
+int mtp_version(void);
+
+/* Clears a workspace (device memset of `bytes`, enqueued on `stream`). */
+mtp_status mtp_workspace_init(void *d_ws, size_t bytes, void *stream);
+
+/* Reads the device error word of a workspace (synchronous device-to-host
+ * copy).  0 = no device-side wait has timed out since mtp_workspace_init. */
+mtp_status mtp_workspace_status(const void *d_ws, int32_t *h_code, void *stream);
+
+/* ------------------------------------------------------------------------
+ * qmatmul_affine4: y[r][n] = sum_k x[r][k] * (s[n][k/32]*code[n][k] + b[n][k/32])
+ *
+ * "hf2q 0.1.1 src/serve/forward_mlx_shared.rs", dispatch_qmatmul (affine
+ * branch) and the CPU reference of its unit tests.
+ *   d_x  [m][K] float32; d_y [m][N] float32 (overwritten); 1 <= m <= 16.
+ *   W->k must equal K and be a multiple of 32.
+ *   d_ws: workspace of qmatmul_affine4_workspace_bytes(m, K) bytes; it holds
+ *         the activations in the tensor-core operand layout.
+ * ------------------------------------------------------------------------ */
+size_t qmatmul_affine4_workspace_bytes(int32_t m, int32_t k);
+mtp_status qmatmul_affine4(const float *d_x, const mtp_affine4 *W, float *d_y, int32_t m,
+                           void *d_ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * rmsnorm_residual: sum = a + delta (or a when delta is NULL);
+ *   out_norm = sum / sqrt(mean(sum^2) + eps) * w ; out_sum = sum (if not NULL)
+ *
+ * "hf2q 0.1.13 src/inference/models/qwen35/mtp.rs", forward_ffn_residual
+ * (dispatch_fused_residual_norm_f32: the residual sum and its RMSNorm, both
+ * written) and rms_norm_with_weight.
+ *   d_a, d_delta, d_out_norm, d_out_sum: [rows][dim] float32; d_w: [dim].
+ *   out_norm may alias neither input; out_sum may alias d_a.
+ * ------------------------------------------------------------------------ */
+mtp_status rmsnorm_residual(const float *d_a, const float *d_delta, const float *d_w,
+                            float *d_out_norm, float *d_out_sum, int32_t rows, int32_t dim,
+                            float eps, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Attention geometry of a draft layer.
+ *   q_rows = n_heads*head_dim_qk, or 2*n_heads*head_dim_qk when gated_q: head h
+ *   then owns projection rows [2h*dqk, 2h*dqk+dqk) for its query and the next
+ *   dqk rows for its sigmoid gate (requires head_dim_v == head_dim_qk).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int32_t n_heads;
+    int32_t n_kv_heads;    /* divides n_heads; query head h reads KV head h / (n_heads/n_kv_heads) */
+    int32_t head_dim_qk;   /* multiple of 32, <= 256 */
+    int32_t head_dim_v;    /* multiple of 32, <= 256 */
+    int32_t rot_dim;       /* rotated dims (even, <= head_dim_qk); pairs (i, i + rot_dim/2) */
+    int32_t window;        /* > 0: row at position p sees keys p-window < j <= p; <= 0: full causal */
+    int32_t gated_q;       /* 0/1 */
+    float eps;             /* epsilon of the per-head q/k RMSNorm */
+    float scale;           /* logit scale; 0 selects 1/sqrt(head_dim_qk) */
+} mtp_attn_geom;
+
+/* Fills d_rope[p][i] = (cos(p*theta^(-2i/rot_dim)), sin(...)) for 0 <= p < max_pos,
+ * 0 <= i < rot_dim/2, angles evaluated in double precision.  d_rope holds
+ * max_pos*rot_dim floats.  "hf2q 0.1.13 ... mtp.rs", apply_imrope with four
+ * equal text position ids (1-D rotary embedding at the token position). */
+mtp_status mtp_rope_table(float *d_rope, int32_t max_pos, int32_t rot_dim, double theta,
+                          void *stream);
+
+/* ------------------------------------------------------------------------
+ * attn_decode_sink: per-head q/k RMSNorm (when q_norm/k_norm are given),
+ * rotary embedding at positions cache_len + r, append of the m new K/V rows
+ * to the cache, causal (optionally windowed) attention with an optional sink
+ * logit per head, optional sigmoid output gate.
+ *
+ * "hf2q 0.1.13 ... mtp.rs" forward_full_attention (per-head norm, IMROPE,
+ * apply_sdpa_with_kv_cache, apply_sigmoid_gate_multiply) and
+ * "cortiq-engine 0.8.49 src/mimo_mtp.rs" module doc (window 128, sinks).
+ * The sink is one extra logit per head, not scaled, entering the softmax
+ * denominator only.
+ *   d_qp [m][q_rows], d_kp [m][n_kv*dqk], d_vp [m][n_kv*dv]: raw projections.
+ *   d_q_norm, d_k_norm: [dqk] or NULL.  d_sinks: [n_heads] or NULL.
+ *   d_rope: table of mtp_rope_table with max_pos >= cache_len + m.
+ *   d_k_cache [n_kv][cache_cap][dqk], d_v_cache [n_kv][cache_cap][dv]:
+ *     rows < cache_len are read; rows cache_len .. cache_len+m-1 are written.
+ *   d_out [m][n_heads*dv] float32.
+ *   1 <= m <= 16; (n_heads/n_kv_heads)*m <= 64.
+ *   Returns MTP_ERR_CAPACITY if cache_len + m > cache_cap.
+ * ------------------------------------------------------------------------ */
+size_t attn_decode_sink_workspace_bytes(const mtp_attn_geom *g, int32_t m, int32_t cache_len);
+mtp_status attn_decode_sink(const mtp_attn_geom *g, const float *d_qp, const float *d_kp,
+                            const float *d_vp, const float *d_q_norm, const float *d_k_norm,
+                            const float *d_rope, const float *d_sinks, float *d_k_cache,
+                            float *d_v_cache, int32_t cache_len, int32_t cache_cap, int32_t m,
+                            float *d_out, void *d_ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * lmhead_argmax: y_n = RMSNorm(y)*norm_w (or y when norm_w is NULL);
+ *   logits = W . y_n; token = argmax (lowest index among equal maxima).
+ *
+ * "hf2q 0.1.13 ... mtp.rs" forward_shared_head_greedy (norm, vocabulary
+ * projection and argmax in one submission); logits stay on chip unless
+ * d_logits is given.
+ *   d_y [H]; W [V][H]; d_token (int32) and d_value (float) receive the result;
+ *   d_logits [V] or NULL; d_y_normed [H] or NULL.  H % 128 == 0.
+ * ------------------------------------------------------------------------ */
+size_t lmhead_argmax_workspace_bytes(int32_t hidden, int32_t vocab);
+mtp_status lmhead_argmax(const float *d_y, const float *d_norm_w, float eps,
+                         const mtp_affine4 *W, int32_t *d_token, float *d_value, float *d_logits,
+                         float *d_y_normed, void *d_ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * MoE feed-forward (router softmax, top-k, renormalised expert SwiGLUs plus a
+ * sigmoid-gated shared expert).  "hf2q 0.1.13 ... mtp.rs" MtpFfnWeightsGpu::Moe
+ * (router, stacked expert gate/up/down, four shared-expert tensors) and
+ * "hf2q 0.1.1 ... forward_mlx_shared.rs" MlxAffineMoeStack (expert e of a
+ * stack is slab e of [E][N][K/8]; here with float32 scales and biases).
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int32_t n_experts;        /* <= 1024 */
+    int32_t top_k;            /* 1..16 */
+    int32_t expert_inter;     /* multiple of 128 */
+    int32_t shared_inter;     /* multiple of 128, 0 = no shared expert */
+    const float *router;      /* [n_experts][hidden] float32 */
+    mtp_affine4 exp_gate;     /* stacked: n = n_experts*expert_inter, k = hidden */
+    mtp_affine4 exp_up;       /* stacked: n = n_experts*expert_inter, k = hidden */
+    mtp_affine4 exp_down;     /* stacked: n = n_experts*hidden, k = expert_inter */
+    mtp_affine4 sh_gate, sh_up, sh_down;
+    const float *sh_gate_inp; /* [hidden]: shared expert gate = sigmoid(sh_gate_inp . f) */
+} mtp_moe_weights;
+
+/* u2 = u1 + MoE(RMSNorm(u1)*post_norm) for one row (m = 1).
+ * d_sel (int32 [top_k]) and d_weight (float [top_k+1]) receive the routing
+ * decision (chosen experts and their renormalised weights, then the shared
+ * gate) when not NULL. */
+size_t moe_ffn_workspace_bytes(const mtp_moe_weights *w, int32_t hidden);
+mtp_status moe_ffn(const mtp_moe_weights *w, const float *d_u1, const float *d_post_norm,
+                   float eps, int32_t hidden, float *d_u2, int32_t *d_sel, float *d_weight,
+                   void *d_ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * Whole draft layer.
+ * ------------------------------------------------------------------------ */
+typedef struct {
+    int32_t hidden;           /* multiple of 128 */
+    int32_t vocab;
+    int32_t intermediate;     /* dense SwiGLU width (multiple of 128); ignored when moe != NULL */
+    float eps;                /* RMSNorm eps of attn/post/final norms (enorm/hnorm use 1e-6) */
+    mtp_attn_geom attn;
+    const float *enorm, *hnorm;      /* [hidden] */
+    mtp_affine4 eh_proj;             /* [hidden][2*hidden], embedding half first */
+    const float *attn_norm;          /* [hidden] */
+    mtp_affine4 wq, wk, wv, wo;
+    const float *q_norm, *k_norm;    /* [head_dim_qk] or NULL */
+    const float *sinks;              /* [n_heads] or NULL */
+    const float *post_norm;          /* [hidden] */
+    mtp_affine4 ffn_gate, ffn_up, ffn_down;
+    const mtp_moe_weights *moe;      /* host struct, or NULL for the dense FFN */
+    const float *final_norm;         /* [hidden] */
+    mtp_affine4 lm_head;             /* [vocab][hidden] */
+    const float *embed;              /* [vocab][hidden] float32, or NULL (caller passes rows) */
+    const float *rope;               /* mtp_rope_table with max_pos >= cache_cap */
+    float *k_cache, *v_cache;        /* [n_kv][cache_cap][d] */
+    int32_t cache_cap;
+} mtp_layer_desc;
+
+typedef struct {
+    const int32_t *d_tokens;         /* [m] token ids (used when embed != NULL) */
+    const float *d_embed_rows;       /* [m][hidden] embedding rows (used when embed == NULL) */
+    const float *d_hidden;           /* [m][hidden] target hidden states */
+    int32_t cache_len;               /* rows already in the layer's cache */
+    int32_t m;                       /* new rows, 1..16 */
+} mtp_step_in;
+
+typedef struct {
+    int32_t *d_token;                /* argmax of the last row's logits */
+    float *d_value;                  /* its logit */
+    float *d_hidden_out;             /* [hidden] RMSNorm(u2[m-1])*final_norm, or NULL */
+    float *d_u2;                     /* [m][hidden] layer output before the final norm, or NULL */
+    float *d_logits;                 /* [vocab] or NULL */
+} mtp_step_out;
+
+/* One draft-layer step over m rows at positions cache_len .. cache_len+m-1.
+ * The m new K/V rows are written into the cache; the caller advances its
+ * cache length by m when the call returns MTP_OK. */
+size_t mtp_draft_workspace_bytes(const mtp_layer_desc *L, int32_t m);
+mtp_status mtp_draft_forward(const mtp_layer_desc *L, const mtp_step_in *in,
+                             const mtp_step_out *out, void *d_ws, size_t ws_bytes, void *stream);
+
+/* Chained draft of n_layers layers ("cortiq-engine 0.8.49 src/mimo_mtp.rs",
+ * "How the three layers chain" and mimo_mtp_draft): every layer reads the
+ * same target hiddens d_hidden [m][hidden]; layer k row i embeds
+ * d_seq[i + k], and layer k writes its draft to d_seq[m + k], so d_seq holds
+ * m + n_layers int32 (the first m given).  The draft of one layer feeds the
+ * next layer's embedding gather on the device, with no host round trip.
+ * All layers need an embedding table.  d_values [n_layers] receives the
+ * drafts' logits; d_hidden_out [n_layers][hidden] (or NULL) each layer's
+ * normed last row.  cache_lens[k] is layer k's cache length (host array). */
+mtp_status mtp_draft_chain(const mtp_layer_desc *layers, int32_t n_layers,
+                           const float *d_hidden, int32_t *d_seq, const int32_t *cache_lens,
+                           int32_t m, float *d_values, float *d_hidden_out, void *d_ws,
+                           size_t ws_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MTPDRAFT_H */

@@ -1,0 +1,12 @@
+"""GB300 (sm_103a) MTP draft-layer forward: Python binding of libmtpdraft.
+
+Every entry point here marshals torch tensors into the C ABI declared in
+``include/mtpdraft.h``; all arithmetic runs in the library's CUDA kernels.
+"""
+
+from .api import (  # noqa: F401
+    affine4, attn_decode_sink, attn_geom, lmhead_argmax, moe_ffn, moe_weights, mtp_draft_chain,
+    mtp_draft_forward, mtp_rope_table, mtp_workspace_init, mtp_workspace_status,
+    qmatmul_affine4, rmsnorm_residual, workspace,
+)
+from .layer import DraftLayer, DraftChain  # noqa: F401

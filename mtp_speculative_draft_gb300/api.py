@@ -1,0 +1,130 @@
+"""Thin torch-facing wrappers with the C ABI's names (argument marshalling only)."""
+
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib as L
+from ._lib import Affine4, AttnGeom, MoeWeights, check
+
+
+def _p(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("device tensors are required")
+    if not t.is_contiguous():
+        raise ValueError("contiguous tensors are required")
+    return t.data_ptr()
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return C.c_void_p(s.cuda_stream)
+
+
+def affine4(q: torch.Tensor, s: torch.Tensor, b: torch.Tensor, n: int | None = None,
+            k: int | None = None) -> Affine4:
+    """Descriptor of an affine 4-bit weight held in device tensors ``q [n, k/8]``, ``s``/``b [n, k/32]``."""
+    if q.dtype not in (torch.int32, torch.uint32) or s.dtype != torch.float32 or b.dtype != torch.float32:
+        raise TypeError("codes must be int32/uint32, scales and biases float32")
+    n = q.shape[0] if n is None else n
+    k = q.shape[-1] * 8 if k is None else k
+    return Affine4(_p(q), _p(s), _p(b), int(n), int(k))
+
+
+def attn_geom(n_heads, n_kv_heads, head_dim_qk, head_dim_v, rot_dim=None, window=0, gated_q=False,
+              eps=1e-6, scale=0.0) -> AttnGeom:
+    return AttnGeom(n_heads, n_kv_heads, head_dim_qk, head_dim_v,
+                    head_dim_qk if rot_dim is None else rot_dim, window, int(bool(gated_q)),
+                    eps, scale)
+
+
+def moe_weights(n_experts, top_k, expert_inter, shared_inter, router, exp_gate, exp_up, exp_down,
+                sh_gate, sh_up, sh_down, sh_gate_inp) -> MoeWeights:
+    return MoeWeights(n_experts, top_k, expert_inter, shared_inter, _p(router), exp_gate, exp_up,
+                      exp_down, sh_gate, sh_up, sh_down, _p(sh_gate_inp))
+
+
+def workspace(nbytes: int, device="cuda", stream=None) -> torch.Tensor:
+    """A cleared workspace of ``nbytes`` bytes (uint8 device tensor)."""
+    ws = torch.empty(max(int(nbytes), 1024), dtype=torch.uint8, device=device)
+    mtp_workspace_init(ws, stream)
+    return ws
+
+
+def mtp_workspace_init(ws: torch.Tensor, stream=None):
+    check(L.load().mtp_workspace_init(_p(ws), ws.numel(), _stream(stream)), "mtp_workspace_init")
+
+
+def mtp_workspace_status(ws: torch.Tensor, stream=None) -> int:
+    code = C.c_int32(0)
+    check(L.load().mtp_workspace_status(_p(ws), C.byref(code), _stream(stream)),
+          "mtp_workspace_status")
+    return code.value
+
+
+def mtp_rope_table(table: torch.Tensor, max_pos: int, rot_dim: int, theta: float, stream=None):
+    check(L.load().mtp_rope_table(_p(table), max_pos, rot_dim, float(theta), _stream(stream)),
+          "mtp_rope_table")
+
+
+def qmatmul_affine4(x, w: Affine4, y, m: int, ws=None, stream=None):
+    lib = L.load()
+    if ws is None:
+        ws = workspace(lib.qmatmul_affine4_workspace_bytes(m, w.k), stream=stream)
+    check(lib.qmatmul_affine4(_p(x), C.byref(w), _p(y), m, _p(ws), ws.numel(), _stream(stream)),
+          "qmatmul_affine4")
+    return ws
+
+
+def rmsnorm_residual(a, delta, w, out_norm, out_sum, rows, dim, eps, stream=None):
+    check(L.load().rmsnorm_residual(_p(a), _p(delta), _p(w), _p(out_norm), _p(out_sum), rows, dim,
+                                    eps, _stream(stream)), "rmsnorm_residual")
+
+
+def attn_decode_sink(g: AttnGeom, qp, kp, vp, q_norm, k_norm, rope, sinks, k_cache, v_cache,
+                     cache_len, cache_cap, m, out, ws=None, stream=None):
+    lib = L.load()
+    if ws is None:
+        ws = workspace(lib.attn_decode_sink_workspace_bytes(C.byref(g), m, cache_len), stream=stream)
+    check(lib.attn_decode_sink(C.byref(g), _p(qp), _p(kp), _p(vp), _p(q_norm), _p(k_norm),
+                               _p(rope), _p(sinks), _p(k_cache), _p(v_cache), cache_len, cache_cap,
+                               m, _p(out), _p(ws), ws.numel(), _stream(stream)),
+          "attn_decode_sink")
+    return ws
+
+
+def lmhead_argmax(y, norm_w, eps, w: Affine4, token, value, logits=None, y_normed=None, ws=None,
+                  stream=None):
+    lib = L.load()
+    if ws is None:
+        ws = workspace(lib.lmhead_argmax_workspace_bytes(w.k, w.n), stream=stream)
+    check(lib.lmhead_argmax(_p(y), _p(norm_w), eps, C.byref(w), _p(token), _p(value), _p(logits),
+                            _p(y_normed), _p(ws), ws.numel(), _stream(stream)), "lmhead_argmax")
+    return ws
+
+
+def moe_ffn(w: MoeWeights, u1, post_norm, eps, hidden, u2, sel=None, weight=None, ws=None,
+            stream=None):
+    lib = L.load()
+    if ws is None:
+        ws = workspace(lib.moe_ffn_workspace_bytes(C.byref(w), hidden), stream=stream)
+    check(lib.moe_ffn(C.byref(w), _p(u1), _p(post_norm), eps, hidden, _p(u2), _p(sel), _p(weight),
+                      _p(ws), ws.numel(), _stream(stream)), "moe_ffn")
+    return ws
+
+
+def mtp_draft_forward(desc, step_in, step_out, ws, stream=None):
+    check(L.load().mtp_draft_forward(C.byref(desc), C.byref(step_in), C.byref(step_out), _p(ws),
+                                     ws.numel(), _stream(stream)), "mtp_draft_forward")
+
+
+def mtp_draft_chain(descs, hidden, seq, cache_lens, m, values, hidden_out, ws, stream=None):
+    arr = (L.LayerDesc * len(descs))(*descs)
+    lens = (C.c_int32 * len(descs))(*cache_lens)
+    check(L.load().mtp_draft_chain(arr, len(descs), _p(hidden), _p(seq), lens, m, _p(values),
+                                   _p(hidden_out), _p(ws), ws.numel(), _stream(stream)),
+          "mtp_draft_chain")

@@ -1,0 +1,199 @@
+// Affine 4-bit GEMV/skinny-GEMM kernels and their host launchers.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "host.h"
+
+namespace mtp {
+
+// --------------------------------------------------------------- fallback
+__global__ void gemv_simple_kernel(const float* __restrict__ x, int m, int K,
+                                   const uint32_t* __restrict__ q, const float* __restrict__ s,
+                                   const float* __restrict__ b, int N, float* __restrict__ y) {
+  const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int lane = threadIdx.x & 31;
+  pdl_wait();
+  if (warp >= N) return;
+  const int n = warp;
+  const int KW = K / 8;
+  float acc[16];
+#pragma unroll
+  for (int c = 0; c < 16; ++c) acc[c] = 0.f;
+  for (int kw = lane; kw < KW; kw += 32) {
+    const uint32_t word = q[(size_t)n * KW + kw];
+    const int g = kw / 4;
+    const float sc = s[(size_t)n * (K / kGroup) + g];
+    const float bi = b[(size_t)n * (K / kGroup) + g];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const float w = fmaf(sc, (float)((word >> (4 * i)) & 0xFu), bi);
+      const int k = kw * 8 + i;
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        if (c < m) acc[c] = fmaf(x[(size_t)c * K + k], w, acc[c]);
+    }
+  }
+#pragma unroll
+  for (int c = 0; c < 16; ++c) {
+    if (c < m) {
+      const float v = warp_sum(acc[c]);
+      if (lane == 0) y[(size_t)c * N + n] = v;
+    }
+  }
+}
+
+// --------------------------------------------------------------- packing
+// One thread per (group, column, octet); the four octets of a group are
+// adjacent lanes and combine their sums with two shuffles.
+__global__ void pack_x_kernel(const float* __restrict__ x, int m, int K, uint4* __restrict__ xp,
+                              float* __restrict__ xs) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int G = K / kGroup;
+  const int total = G * m * 4;
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  float sum = 0.f;
+  if (i < total) {
+    const int t = i & 3;
+    const int gc = i >> 2;
+    const int c = gc % m;
+    const int g = gc / m;
+    const float4* src = reinterpret_cast<const float4*>(x + (size_t)c * K + g * kGroup + t * 8);
+    const float4 v0 = src[0], v1 = src[1];
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint4 hi, lo;
+    sum = pack8(v, hi, lo);
+    xp[xp_index(g, c, t, 0, m)] = hi;
+    xp[xp_index(g, c, t, 1, m)] = lo;
+  }
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  if (i < total && (i & 3) == 0) {
+    const int gc = i >> 2;
+    xs[(gc / m) * m + gc % m] = sum;
+  }
+}
+
+// --------------------------------------------------------------- launchers
+static cudaLaunchAttribute pdl_attr() {
+  cudaLaunchAttribute a;
+  a.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  a.val.programmaticStreamSerializationAllowed = 1;
+  return a;
+}
+
+template <int NMAT, int NT, int EPI>
+static cudaError_t launch_gemv_t(const GemvParams& p, int tiles, cudaStream_t st) {
+  constexpr int S = NMAT == 1 ? 4 : 2;
+  auto kern = gemv_tc_kernel<NMAT, NT, EPI, S>;
+  const int smem = gemv_smem_bytes<NMAT, S>();
+  static thread_local int configured_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    configured_dev = dev;
+  }
+  const int ctas_per_sm = 2;
+  int grid = (tiles + kGemvWarps - 1) / kGemvWarps;
+  const int cap = sm_count() * ctas_per_sm;
+  if (grid > cap) grid = cap;
+  if (grid < 1) grid = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemvWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr = pdl_attr();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+cudaError_t launch_gemv(int nmat, int nt, int epi, const GemvParams& p, int tiles,
+                        cudaStream_t st) {
+  if (epi == kEpiArgmax) return launch_gemv_t<1, 1, kEpiArgmax>(p, tiles, st);
+  if (nmat == 1) {
+    if (epi != kEpiStore) return cudaErrorInvalidValue;
+    return nt == 1 ? launch_gemv_t<1, 1, kEpiStore>(p, tiles, st)
+                   : launch_gemv_t<1, 2, kEpiStore>(p, tiles, st);
+  }
+  if (epi != kEpiSwiglu) return cudaErrorInvalidValue;
+  return nt == 1 ? launch_gemv_t<2, 1, kEpiSwiglu>(p, tiles, st)
+                 : launch_gemv_t<2, 2, kEpiSwiglu>(p, tiles, st);
+}
+
+cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float* xs, cudaStream_t st) {
+  const int total = (K / kGroup) * m * 4;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((total + 255) / 256);
+  cfg.blockDim = dim3(256);
+  cfg.stream = st;
+  cudaLaunchAttribute attr = pdl_attr();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, pack_x_kernel, x, m, K, xp, xs);
+}
+
+cudaError_t launch_gemv_simple(const float* x, int m, int K, const mtp_affine4& w, float* y,
+                               cudaStream_t st) {
+  const int threads = 256;
+  const int blocks = (w.n * 32 + threads - 1) / threads;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks);
+  cfg.blockDim = dim3(threads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr = pdl_attr();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, gemv_simple_kernel, x, m, K, w.q, w.s, w.b, (int)w.n, y);
+}
+
+// --------------------------------------------------------------- tensor maps
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &ptr, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  });
+  return fn;
+}
+
+static CUresult encode2d(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner,
+                         uint64_t rows, uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                         CUtensorMapSwizzle sw) {
+  auto fn = get_encode();
+  if (!fn) return CUDA_ERROR_NOT_FOUND;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+mtp_status encode_qmat(QMat* out, const mtp_affine4& w, const char* name) {
+  const uint64_t kw = (uint64_t)w.k / 8, kg = (uint64_t)w.k / kGroup;
+  CUresult r = encode2d(&out->q, CU_TENSOR_MAP_DATA_TYPE_UINT32, w.q, kw, (uint64_t)w.n, kw * 4,
+                        32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (r == CUDA_SUCCESS)
+    r = encode2d(&out->s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w.s, kg, (uint64_t)w.n, kg * 4, 8, 32,
+                 CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (r == CUDA_SUCCESS)
+    r = encode2d(&out->b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w.b, kg, (uint64_t)w.n, kg * 4, 8, 32,
+                 CU_TENSOR_MAP_SWIZZLE_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(MTP_ERR_CUDA, std::string("tensor map encoding failed for ") + name +
+                                  " (CUresult " + std::to_string((int)r) + ")");
+  return MTP_OK;
+}
+
+}  // namespace mtp

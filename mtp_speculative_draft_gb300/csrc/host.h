@@ -1,0 +1,94 @@
+// Host-side internals shared by the entry points (not part of the C ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <string>
+
+#include "../../include/mtpdraft.h"
+#include "gemv.cuh"
+
+namespace mtp {
+
+// Records a thread-local error message and returns `st`.
+mtp_status fail(mtp_status st, const std::string& msg);
+mtp_status cuda_fail(cudaError_t e, const char* what);
+
+bool aligned16(const void* p);
+
+// Number of SMs of the current device (cached per device).
+int sm_count();
+
+// Encodes the three tensor maps of an affine weight viewed as [rows][k].
+mtp_status encode_qmat(QMat* out, const mtp_affine4& w, const char* name);
+
+// Checks an affine weight descriptor: non-null, aligned, positive sizes,
+// k % 32 == 0, and (when `need_tma`) k % 128 == 0 so the scale rows are
+// 16-byte aligned for the tensor maps.
+mtp_status check_affine(const mtp_affine4* w, int n, int k, const char* name, bool need_tma);
+
+// Launch helpers (programmatic dependent launch on `stream`).
+cudaError_t launch_gemv(int nmat, int nt, int epi, const GemvParams& p, int tiles,
+                        cudaStream_t stream);
+cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float* xs, cudaStream_t st);
+cudaError_t launch_gemv_simple(const float* x, int m, int K, const mtp_affine4& w, float* y,
+                               cudaStream_t st);
+
+struct NormSeg {
+  const float* src;       // row 0 source (row stride = src_ld); null when gathered from `table`
+  const float* delta;     // residual added to src (same layout), or null
+  const float* table;     // embedding table [V][dim] gathered with tokens[c]
+  const int* tokens;
+  int vocab;
+  const float* w;         // norm weight, or null (no normalisation)
+  float eps;
+  int dim;
+  int src_ld;
+  float* out_sum;         // fp32 sum (ld = dim), or null
+  float* out_norm;        // fp32 normalised row (ld = dim), or null
+};
+
+// Normalises m rows (up to two segments concatenated along K) and writes
+// the packed activations of the concatenation (xp may be null).
+cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, float* xs,
+                             int* err, cudaStream_t st);
+
+struct AttnParams {
+  int nh, nkv, dqk, dv, rot, window, gated;
+  float eps, scale;
+  const float *qp, *kp, *vp, *qn, *kn, *rope, *sinks;
+  float *kc, *vc;
+  int L, cap, m;
+  float* out;          // [m][nh*dv] fp32 (may be null)
+  uint4* out_xp;       // packed output for the next projection (may be null)
+  float* out_xs;
+  float* part;         // partials
+  unsigned* counters;  // [nkv]
+  int nsplit;
+  int* err;
+};
+int attn_splits(int nkv, int keys);
+size_t attn_part_bytes(int nkv, int nsplit, int q_per_kv, int dv);
+cudaError_t launch_attn(const AttnParams& a, cudaStream_t st);
+
+struct RouterParams {
+  const float* u1;       // [H] residual stream row
+  const float* post_norm;
+  float eps;
+  int H;
+  const float* router;   // [E][H]
+  int E, top_k;
+  const float* sh_gate_inp;  // [H] or null
+  float* logits;         // [E] scratch
+  unsigned* counter;
+  int* sel;              // [top_k]
+  float* weight;         // [top_k + 1]
+  uint4* xp;             // packed normalised row for the expert projections
+  float* xs;
+};
+cudaError_t launch_router(const RouterParams& r, cudaStream_t st);
+
+cudaError_t launch_rope_table(float* d, int max_pos, int rot, double theta, cudaStream_t st);
+
+}  // namespace mtp

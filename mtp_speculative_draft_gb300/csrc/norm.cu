@@ -1,0 +1,163 @@
+// RMSNorm (+ residual, + embedding gather) with packing of the result into the
+// tensor-core activation layout, and the rotary-table initialiser.
+//
+// RMSNorm: x / sqrt(mean(x^2) + eps) * w ("hf2q 0.1.13
+// src/inference/models/qwen35/mtp.rs", rms_norm_with_weight and
+// dispatch_fused_residual_norm_f32).
+#include "host.h"
+
+namespace mtp {
+
+struct NormPackArgs {
+  NormSeg seg[2];
+  int nseg;
+  int m;
+  uint4* xp;
+  float* xs;
+  int* err;
+};
+
+constexpr int kNormThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = 0.f;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) t += red[w];
+  return t;
+}
+
+__device__ __forceinline__ const float* seg_row(const NormSeg& s, int c, int* err) {
+  if (s.table) {
+    int tok = s.tokens[c];
+    if (tok < 0 || tok >= s.vocab) {
+      set_dev_error(err, 2);
+      tok = 0;
+    }
+    return s.table + (size_t)tok * s.dim;
+  }
+  return s.src + (size_t)c * s.src_ld;
+}
+
+__global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackArgs a) {
+  __shared__ float red[kNormThreads / 32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int c = blockIdx.x;
+  float inv[2] = {1.f, 1.f};
+  for (int si = 0; si < a.nseg; ++si) {
+    const NormSeg& s = a.seg[si];
+    if (!s.w) continue;
+    const float* row = seg_row(s, c, a.err);
+    const float* dl = s.delta ? s.delta + (size_t)c * s.src_ld : nullptr;
+    float ss = 0.f;
+    for (int k = threadIdx.x * 4; k < s.dim; k += kNormThreads * 4) {
+      float4 v = *reinterpret_cast<const float4*>(row + k);
+      if (dl) {
+        const float4 d = *reinterpret_cast<const float4*>(dl + k);
+        v.x += d.x; v.y += d.y; v.z += d.z; v.w += d.w;
+      }
+      ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+    }
+    ss = block_sum(ss, red);
+    inv[si] = rsqrtf(ss / (float)s.dim + s.eps);
+  }
+  // pass 2: octets of the concatenation
+  const int K = a.seg[0].dim + (a.nseg > 1 ? a.seg[1].dim : 0);
+  const int octets = K / 8;
+  for (int o0 = 0; o0 < octets; o0 += kNormThreads) {
+    const int o = o0 + threadIdx.x;
+    float sum = 0.f;
+    if (o < octets) {
+      const int k = o * 8;
+      const int si = (a.nseg > 1 && k >= a.seg[0].dim) ? 1 : 0;
+      const NormSeg& s = a.seg[si];
+      const int kk = k - (si ? a.seg[0].dim : 0);
+      const float* row = seg_row(s, c, a.err);
+      const float* dl = s.delta ? s.delta + (size_t)c * s.src_ld : nullptr;
+      float v[8];
+      const float4 v0 = *reinterpret_cast<const float4*>(row + kk);
+      const float4 v1 = *reinterpret_cast<const float4*>(row + kk + 4);
+      v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+      v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+      if (dl) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] += dl[kk + i];
+      }
+      if (s.out_sum) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s.out_sum[(size_t)c * s.dim + kk + i] = v[i];
+      }
+      if (s.w) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) v[i] = v[i] * inv[si] * s.w[kk + i];
+      }
+      if (s.out_norm) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s.out_norm[(size_t)c * s.dim + kk + i] = v[i];
+      }
+      if (a.xp) {
+        uint4 hi, lo;
+        sum = pack8(v, hi, lo);
+        const int g = k / kGroup, t = (k % kGroup) / 8;
+        a.xp[xp_index(g, c, t, 0, a.m)] = hi;
+        a.xp[xp_index(g, c, t, 1, a.m)] = lo;
+      }
+    }
+    if (a.xp) {
+      // octets o..o+3 of one group sit in adjacent lanes (kNormThreads % 4 == 0)
+      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      if (o < octets && (o & 3) == 0) a.xs[(o / 4) * a.m + c] = sum;
+    }
+  }
+}
+
+cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, float* xs,
+                             int* err, cudaStream_t st) {
+  NormPackArgs a = {};
+  a.seg[0] = segs[0];
+  if (nseg > 1) a.seg[1] = segs[1];
+  a.nseg = nseg;
+  a.m = m;
+  a.xp = xp;
+  a.xs = xs;
+  a.err = err;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(m);
+  cfg.blockDim = dim3(kNormThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr;
+  attr.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr.val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, norm_pack_kernel, a);
+}
+
+// --------------------------------------------------------------- rotary table
+__global__ void rope_table_kernel(float* __restrict__ d, int max_pos, int rot, double theta) {
+  const int half = rot / 2;
+  const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (long long)max_pos * half) return;
+  const int p = (int)(i / half);
+  const int j = (int)(i % half);
+  const double ang = (double)p * pow(theta, -2.0 * (double)j / (double)rot);
+  double sn, cs;
+  sincos(ang, &sn, &cs);
+  d[2 * i] = (float)cs;
+  d[2 * i + 1] = (float)sn;
+}
+
+cudaError_t launch_rope_table(float* d, int max_pos, int rot, double theta, cudaStream_t st) {
+  const long long n = (long long)max_pos * (rot / 2);
+  const int threads = 256;
+  const int blocks = (int)((n + threads - 1) / threads);
+  rope_table_kernel<<<blocks, threads, 0, st>>>(d, max_pos, rot, theta);
+  return cudaGetLastError();
+}
+
+}  // namespace mtp

@@ -22,6 +22,9 @@ KV-cache rows ``N(0, 1)``, sink logits ``N(0, 1)``, router weights
 
 from __future__ import annotations
 
+import os
+from concurrent.futures import ThreadPoolExecutor
+
 import numpy as np
 
 from .configs import CONFIGS, LayerConfig, layer_config  # noqa: F401
@@ -76,7 +79,8 @@ def normal(seed: int, name: str, count: int, start: int = 0) -> np.ndarray:
     p0 = start // 2
     p1 = (start + count + 1) // 2
     out = np.empty(2 * (p1 - p0), dtype=np.float64)
-    for lo in range(p0, p1, _CHUNK):
+
+    def fill(lo: int) -> None:
         hi = min(p1, lo + _CHUNK)
         raw = stream_u64(seed, name, 2 * lo, 2 * (hi - lo)) >> np.uint64(11)
         u1 = (raw[0::2].astype(np.float64) + 1.0) * 2.0 ** -53  # (0, 1]
@@ -86,6 +90,15 @@ def normal(seed: int, name: str, count: int, start: int = 0) -> np.ndarray:
         seg = out[2 * (lo - p0): 2 * (hi - p0)]
         seg[0::2] = r * np.cos(t)
         seg[1::2] = r * np.sin(t)
+
+    starts = list(range(p0, p1, _CHUNK))
+    if len(starts) > 2:
+        # numpy releases the GIL inside these array operations: chunks run in parallel
+        with ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 1)) as ex:
+            list(ex.map(fill, starts))
+    else:
+        for lo in starts:
+            fill(lo)
     off = start - 2 * p0
     return out[off: off + count]
 
