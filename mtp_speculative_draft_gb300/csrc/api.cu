@@ -100,6 +100,16 @@ struct Carve {
 
 static WsHeader* header(void* ws) { return static_cast<WsHeader*>(ws); }
 
+// Split-K partials and per-tile counters used by the GEMV launches of a call.
+static GemvScratch carve_scratch(Carve& cv) {
+  GemvScratch sc;
+  sc.part_bytes = gemv_scratch_part_bytes();
+  sc.part = cv.take<float>(sc.part_bytes);
+  sc.cnt = cv.take<unsigned>(sizeof(unsigned) * kGemvCounters);
+  sc.cnt_len = kGemvCounters;
+  return sc;
+}
+
 // Counter slots inside WsHeader::counters.
 constexpr int kCntAttn = 0;      // [n_kv] (n_kv <= 64)
 constexpr int kCntArgmax = 64;
@@ -162,7 +172,10 @@ mtp_status mtp_rope_table(float* d_rope, int32_t max_pos, int32_t rot_dim, doubl
 // ------------------------------------------------------------------ qmatmul
 size_t qmatmul_affine4_workspace_bytes(int32_t m, int32_t k) {
   if (m <= 0 || k <= 0) return 0;
-  return sizeof(WsHeader) + align256(xpack_bytes(m, k)) + 256;
+  Carve cv(nullptr);
+  cv.take<uint8_t>(xpack_bytes(m, k));
+  carve_scratch(cv);
+  return cv.off + 256;
 }
 
 mtp_status qmatmul_affine4(const float* d_x, const mtp_affine4* W, float* d_y, int32_t m,
@@ -185,8 +198,9 @@ mtp_status qmatmul_affine4(const float* d_x, const mtp_affine4* W, float* d_y, i
     return fail(MTP_ERR_WORKSPACE, "qmatmul_affine4: workspace too small");
   Carve cv(d_ws);
   const size_t G = K / kGroup;
-  uint4* xp = cv.take<uint4>(G * m * 128 + G * m * 4);
-  float* xs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xp) + G * m * 128);
+  uint4* xp = cv.take<uint4>(xpack_bytes(m, K));
+  float2* xs = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(xp) + xpack_xs_offset(m, K));
+  const GemvScratch sc = carve_scratch(cv);
   GemvParams p = {};
   s = qmat_cached(&p.mat[0], *W, "qmatmul_affine4 weight");
   if (s != MTP_OK) return s;
@@ -198,7 +212,7 @@ mtp_status qmatmul_affine4(const float* d_x, const mtp_affine4* W, float* d_y, i
   p.seg[0] = plain_seg(tiles_of(N), N, 0, d_y, N, nullptr);
   p.err = &header(d_ws)->err;
   cudaError_t e = launch_pack(d_x, m, K, xp, xs, st);
-  if (e == cudaSuccess) e = launch_gemv(1, m > 8 ? 2 : 1, kEpiStore, p, tiles_of(N), st);
+  if (e == cudaSuccess) e = launch_gemv(1, m > 8 ? 2 : 1, kEpiStore, p, tiles_of(N), sc, st);
   if (e != cudaSuccess) return cuda_fail(e, "qmatmul_affine4 launch");
   return MTP_OK;
 }
@@ -247,6 +261,10 @@ static mtp_status check_geom(const mtp_attn_geom* g, int m) {
   if (m < 1 || m > 16) return fail(MTP_ERR_UNSUPPORTED, "attention: m must be in 1..16");
   if ((g->n_heads / g->n_kv_heads) * m > 16)
     return fail(MTP_ERR_UNSUPPORTED, "attention: (n_heads/n_kv_heads)*m must be <= 16");
+  // the P.V split gives each thread (512 / head_dim_v) query slices of at most 8 rows
+  if (g->head_dim_v > 512 ||
+      ((g->n_heads / g->n_kv_heads) * m + (512 / g->head_dim_v) - 1) / (512 / g->head_dim_v) > 8)
+    return fail(MTP_ERR_UNSUPPORTED, "attention: too many query rows for head_dim_v");
   if (!(g->eps >= 0.f) || !(g->scale >= 0.f))
     return fail(MTP_ERR_INVALID_ARG, "attention: eps and scale must be >= 0");
   return MTP_OK;
@@ -323,13 +341,17 @@ mtp_status attn_decode_sink(const mtp_attn_geom* g, const float* d_qp, const flo
 // ------------------------------------------------------------------ lm head
 size_t lmhead_argmax_workspace_bytes(int32_t hidden, int32_t vocab) {
   if (hidden <= 0 || vocab <= 0) return 0;
-  return sizeof(WsHeader) + align256(xpack_bytes(1, hidden)) + align256(8 * 4096) + 256;
+  Carve cv(nullptr);
+  cv.take<uint8_t>(xpack_bytes(1, hidden));
+  cv.take<uint8_t>(8 * 4096);
+  carve_scratch(cv);
+  return cv.off + 256;
 }
 
 static mtp_status enqueue_head(const float* y_src, const float* norm_w, float eps, int H,
                                const mtp_affine4& W, int32_t* tok, float* val, float* logits,
-                               float* y_normed, uint4* xp, float* xs, unsigned long long* partial,
-                               void* ws, cudaStream_t st) {
+                               float* y_normed, uint4* xp, float2* xs, unsigned long long* partial,
+                               const GemvScratch& sc, void* ws, cudaStream_t st) {
   NormSeg sg = {};
   sg.src = y_src;
   sg.w = norm_w;
@@ -354,7 +376,7 @@ static mtp_status enqueue_head(const float* y_src, const float* norm_w, float ep
   p.am_value = val;
   p.logits = logits;
   p.err = &header(ws)->err;
-  e = launch_gemv(1, 1, kEpiArgmax, p, tiles_of(W.n), st);
+  e = launch_gemv(1, 1, kEpiArgmax, p, tiles_of(W.n), sc, st);
   if (e != cudaSuccess) return cuda_fail(e, "lm head launch");
   return MTP_OK;
 }
@@ -374,10 +396,11 @@ mtp_status lmhead_argmax(const float* d_y, const float* d_norm_w, float eps,
   Carve cv(d_ws);
   const int H = W->k;
   uint4* xp = cv.take<uint4>(xpack_bytes(1, H));
-  float* xs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(xp) + (size_t)(H / kGroup) * 128);
+  float2* xs = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(xp) + xpack_xs_offset(1, H));
   auto* partial = cv.take<unsigned long long>(8 * 4096);
+  const GemvScratch sc = carve_scratch(cv);
   return enqueue_head(d_y, d_norm_w, eps, H, *W, d_token, d_value, d_logits, d_y_normed, xp, xs,
-                      partial, d_ws, static_cast<cudaStream_t>(stream));
+                      partial, sc, d_ws, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ MoE
@@ -406,13 +429,14 @@ static mtp_status check_moe(const mtp_moe_weights* w, int H) {
 }
 
 struct MoeScratch {
+  GemvScratch gemv;
   float* logits;
   int* sel;
   float* weight;
   uint4* xp_f;
-  float* xs_f;
+  float2* xs_f;
   uint4* xp_h;
-  float* xs_h;
+  float2* xs_h;
 };
 
 static void carve_moe(Carve& cv, const mtp_moe_weights* w, int H, MoeScratch* m) {
@@ -424,8 +448,9 @@ static void carve_moe(Carve& cv, const mtp_moe_weights* w, int H, MoeScratch* m)
   m->xs_h = nullptr;
   const int Kh = (w->top_k + 1) * w->expert_inter;
   m->xp_h = cv.take<uint4>(xpack_bytes(1, Kh));
-  if (m->xp_f) m->xs_f = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(m->xp_f) + (size_t)(H / kGroup) * 128);
-  if (m->xp_h) m->xs_h = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(m->xp_h) + (size_t)(Kh / kGroup) * 128);
+  if (m->xp_f) m->xs_f = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(m->xp_f) + xpack_xs_offset(1, H));
+  if (m->xp_h) m->xs_h = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(m->xp_h) + xpack_xs_offset(1, Kh));
+  m->gemv = carve_scratch(cv);
 }
 
 static mtp_status enqueue_moe(const mtp_moe_weights* w, const float* u1, const float* post_norm,
@@ -478,7 +503,7 @@ static mtp_status enqueue_moe(const mtp_moe_weights* w, const float* u1, const f
   p.out_xs = sc.xs_h;
   p.out_m = 1;
   p.err = &header(ws)->err;
-  e = launch_gemv(2, 1, kEpiSwiglu, p, (K + 1) * tpe, st);
+  e = launch_gemv(2, 1, kEpiSwiglu, p, (K + 1) * tpe, sc.gemv, st);
   if (e != cudaSuccess) return cuda_fail(e, "moe expert gate/up launch");
 
   // down projections over the concatenated expert activations, + residual
@@ -498,7 +523,7 @@ static mtp_status enqueue_moe(const mtp_moe_weights* w, const float* u1, const f
   d.kseg_row_mult = H;
   d.kseg_last_mat = 1;
   d.err = &header(ws)->err;
-  e = launch_gemv(1, 1, kEpiStore, d, tiles_of(H), st);
+  e = launch_gemv(1, 1, kEpiStore, d, tiles_of(H), sc.gemv, st);
   if (e != cudaSuccess) return cuda_fail(e, "moe expert down launch");
   return MTP_OK;
 }
@@ -541,12 +566,13 @@ mtp_status moe_ffn(const mtp_moe_weights* w, const float* d_u1, const float* d_p
 // ------------------------------------------------------------------ layer
 struct LayerWs {
   uint4* xa;
-  float* xsa;
+  float2* xsa;
   uint4* xb;
-  float* xsb;
+  float2* xsb;
   float *u, *u1, *u2, *qp, *kp, *vp;
   float* part;
   unsigned long long* am_partial;
+  GemvScratch gemv;
   MoeScratch moe;
 };
 
@@ -564,10 +590,9 @@ static void carve_layer(Carve& cv, const mtp_layer_desc* L, int m, LayerWs* w) {
   const int Kmax = layer_kmax(L);
   const mtp_attn_geom& g = L->attn;
   const int qrows = g.n_heads * g.head_dim_qk * (g.gated_q ? 2 : 1);
-  auto xp_pair = [&](uint4** xp, float** xs) {
+  auto xp_pair = [&](uint4** xp, float2** xs) {
     *xp = cv.take<uint4>(xpack_bytes(m, Kmax));
-    *xs = *xp ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(*xp) +
-                                         (size_t)(Kmax / kGroup) * m * 128)
+    *xs = *xp ? reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(*xp) + xpack_xs_offset(m, Kmax))
               : nullptr;
   };
   xp_pair(&w->xa, &w->xsa);
@@ -583,6 +608,7 @@ static void carve_layer(Carve& cv, const mtp_layer_desc* L, int m, LayerWs* w) {
   w->part = cv.take<float>(attn_part_bytes(g.n_kv_heads, ns, (g.n_heads / g.n_kv_heads) * m,
                                            g.head_dim_v));
   w->am_partial = cv.take<unsigned long long>(8 * 4096);
+  w->gemv = carve_scratch(cv);
   if (L->moe) carve_moe(cv, L->moe, H, &w->moe);
 }
 
@@ -676,7 +702,7 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   p.seg[0] = plain_seg(tiles_of(H), H, 0, w.u, H, nullptr);
   p.err = err;
   const int nt = m > 8 ? 2 : 1;
-  if ((e = launch_gemv(1, nt, kEpiStore, p, tiles_of(H), st)) != cudaSuccess)
+  if ((e = launch_gemv(1, nt, kEpiStore, p, tiles_of(H), w.gemv, st)) != cudaSuccess)
     return cuda_fail(e, "eh_proj launch");
 
   // 3. x = RMSNorm(u) * attn_norm
@@ -706,7 +732,7 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   q.seg[1] = plain_seg(tq + tk, krows, 1, w.kp, krows, nullptr);
   q.seg[2] = plain_seg(tq + tk + tv, vrows, 2, w.vp, vrows, nullptr);
   q.err = err;
-  if ((e = launch_gemv(1, nt, kEpiStore, q, tq + tk + tv, st)) != cudaSuccess)
+  if ((e = launch_gemv(1, nt, kEpiStore, q, tq + tk + tv, w.gemv, st)) != cudaSuccess)
     return cuda_fail(e, "qkv launch");
 
   // 5. attention (norm + rope + append + split-K + sink + gate), packed output
@@ -715,6 +741,7 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   a.part = w.part;
   a.counters = header(ws)->counters + kCntAttn;
   a.err = err;
+  a.prefetch_before_wait = 1;  // the q/k/v projection signals only after its own wait
   a.out = nullptr;
   a.out_xp = w.xa;
   a.out_xs = w.xsa;
@@ -731,7 +758,7 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   o.nseg = 1;
   o.seg[0] = plain_seg(tiles_of(H), H, 0, w.u1, H, w.u);
   o.err = err;
-  if ((e = launch_gemv(1, nt, kEpiStore, o, tiles_of(H), st)) != cudaSuccess)
+  if ((e = launch_gemv(1, nt, kEpiStore, o, tiles_of(H), w.gemv, st)) != cudaSuccess)
     return cuda_fail(e, "o_proj launch");
 
   float* u2 = out->d_u2 ? out->d_u2 : w.u2;
@@ -763,7 +790,7 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     gu.out_xs = w.xsb;
     gu.out_m = m;
     gu.err = err;
-    if ((e = launch_gemv(2, nt, kEpiSwiglu, gu, tiles_of(I), st)) != cudaSuccess)
+    if ((e = launch_gemv(2, nt, kEpiSwiglu, gu, tiles_of(I), w.gemv, st)) != cudaSuccess)
       return cuda_fail(e, "gate/up launch");
     // 9. u2 = u1 + W_down h
     GemvParams dn = {};
@@ -775,14 +802,14 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     dn.nseg = 1;
     dn.seg[0] = plain_seg(tiles_of(H), H, 0, u2, H, w.u1);
     dn.err = err;
-    if ((e = launch_gemv(1, nt, kEpiStore, dn, tiles_of(H), st)) != cudaSuccess)
+    if ((e = launch_gemv(1, nt, kEpiStore, dn, tiles_of(H), w.gemv, st)) != cudaSuccess)
       return cuda_fail(e, "down launch");
   }
 
   // 10-11. final norm of the last row, lm_head + argmax
   return enqueue_head(u2 + (size_t)(m - 1) * H, L->final_norm, L->eps, H, L->lm_head,
                       out->d_token, out->d_value, out->d_logits, out->d_hidden_out, w.xa, w.xsa,
-                      w.am_partial, ws, st);
+                      w.am_partial, w.gemv, ws, st);
 }
 
 mtp_status mtp_draft_forward(const mtp_layer_desc* L, const mtp_step_in* in,

@@ -7,31 +7,65 @@
 // apply_sigmoid_gate_multiply) and "cortiq-engine 0.8.49 src/mimo_mtp.rs"
 // (sliding window, per-head sinks).
 //
-// Split-K over the cache (one CTA per (split, KV head)): each CTA serves all
-// query heads of its KV head (grouped-query sharing of the K/V stream) for all
-// m new rows, keeps an online softmax in the log2 domain, and writes an
-// unnormalised partial.  The last CTA of a KV head (completion counter, no
-// spinning) merges the partials, adds the sink to the denominator, applies
-// the gate and writes the output both as fp32 and packed for the o_proj GEMV.
+// Split-K over the cache, one CTA per (split, KV head), about one CTA per
+// SM.  Each CTA serves all query heads of its KV head (grouped-query sharing
+// of the K/V stream) for all m new rows.  The cached keys and values stream
+// through a ring of shared-memory stages filled by bulk copies (one copy per
+// key row into a padded row, one copy per value tile) and completed on
+// mbarriers; the softmax is kept online in the log2 domain.  The m new keys
+// and values are normalised/rotated in shared memory, appended to the cache
+// with plain stores, and attended to by the last split from shared memory.
+// The last CTA of a KV head to finish (completion counter, no spinning)
+// merges the partials with precomputed split weights, adds the sink to the
+// denominator, applies the gate and writes the output both as fp32 and
+// packed for the o_proj GEMV.
 #include "host.h"
 
 namespace mtp {
 
-constexpr int kAttnThreads = 128;
+constexpr int kAttnThreads = 512;
 constexpr int kTileKeys = 32;
 constexpr int kMaxQ = 16;            // query rows per KV head (heads per group x m)
 constexpr float kNegBig = -1e30f;
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr int kAttnSmemMax = 200 * 1024;
+constexpr int kQpt = 8;              // largest per-thread query count of the P.V split
+// probability/statistics rows allocated for the padded query slices of P.V
+// (up to kQpt rows per slice, at most kAttnThreads / 32 slices)
+constexpr int kPadQ = kQpt * (kAttnThreads / 32);
 
-struct AttnSmem {
-  static size_t bytes(int dqk, int dv, int QG) {
-    return (size_t)kTileKeys * (dqk + 4) * 4 + (size_t)kTileKeys * dv * 4 +
-           (size_t)QG * dqk * 4 + (size_t)QG * kTileKeys * 4 + 4 * kMaxQ * 4 + 64;
-  }
+struct AttnLayout {
+  int stages;
+  int kstride;       // padded K row (floats)
+  size_t stage_bytes, q_off, p_off, stat_off, newk_off, newv_off, bar_off, total;
 };
 
+// Partials: (M, l) pairs [nkv][nsplit][QG][2], then outputs [nkv][nsplit][QG][dv]
+// starting on a 16-byte boundary.
+__host__ __device__ inline size_t attn_part_o_offset(int nkv, int nsplit, int QG) {
+  return ((size_t)nkv * nsplit * QG * 2 + 3) / 4 * 4;
+}
+
+__host__ __device__ inline AttnLayout attn_layout(int dqk, int dv, int QG, int m) {
+  AttnLayout L;
+  L.kstride = dqk + 4;
+  L.stage_bytes = (size_t)kTileKeys * L.kstride * 4 + (size_t)kTileKeys * dv * 4;
+  const size_t fixed = (size_t)QG * dqk * 4 + (size_t)kPadQ * kTileKeys * 4 + 3 * kPadQ * 4 +
+                       (size_t)m * (dqk + dv) * 4 + 8 * 8 + 256;
+  int s = (int)((kAttnSmemMax - fixed) / L.stage_bytes);
+  L.stages = s > 3 ? 3 : (s < 1 ? 1 : s);
+  L.q_off = L.stages * L.stage_bytes;
+  L.p_off = L.q_off + (size_t)QG * dqk * 4;
+  L.stat_off = L.p_off + (size_t)kPadQ * kTileKeys * 4;
+  L.newk_off = L.stat_off + 3 * kPadQ * 4;
+  L.newv_off = L.newk_off + (size_t)m * dqk * 4;
+  L.bar_off = (L.newv_off + (size_t)m * dv * 4 + 15) / 16 * 16;
+  L.total = L.bar_off + 8 * 8;
+  return L;
+}
+
 // Per-head RMSNorm (optional) then rotary embedding of one head vector held
-// in shared memory by one warp.
+// in shared memory by one warp; the result is multiplied by `post_scale`.
 __device__ __forceinline__ void warp_norm_rope(float* v, int d, const float* nw, float eps,
                                                const float* rope_row, int rot, float post_scale,
                                                int lane) {
@@ -57,8 +91,71 @@ __device__ __forceinline__ void warp_norm_rope(float* v, int d, const float* nw,
   __syncwarp();
 }
 
+// Work split of the P.V product: thread t owns output dim t % dv for the
+// query rows q = t / dv + k * (kAttnThreads / dv), k < QPT (a template
+// bound chosen on the host as the smallest power of two that covers QG).
+
+// One tile of keys [key0, key0 + nk) from shared memory: logits, online
+// softmax update and P.V accumulation.  Ends with the CTA synchronised.
+template <int QPT>
+__device__ __forceinline__ void attend_tile(const AttnParams& a, const float* Ks, int kstride,
+                                           const float* Vs, int nk, int key0, const float* qs,
+                                           float* ps, float* Ms, float* ls, float* als,
+                                           float (&oacc)[QPT], int QG, int G) {
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int dqk = a.dqk, dv = a.dv;
+  const int kq4 = dqk / 4;
+  for (int pi = tid; pi < QG * kTileKeys; pi += kAttnThreads) {
+    const int jj = pi & (kTileKeys - 1), qi = pi / kTileKeys;
+    const int j = key0 + jj, p = a.L + qi / G;
+    float l = kNegBig;
+    if (jj < nk && j <= p && (a.window <= 0 || j > p - a.window)) {
+      const float4* qv = reinterpret_cast<const float4*>(qs + qi * dqk);
+      const float4* kv = reinterpret_cast<const float4*>(Ks + jj * kstride);
+      float acc = 0.f;
+      for (int d4 = 0; d4 < kq4; ++d4) {
+        const float4 x = qv[d4], y = kv[d4];
+        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
+      }
+      l = acc;
+    }
+    ps[qi * kTileKeys + jj] = l;
+  }
+  __syncthreads();
+  for (int qi = warp; qi < QG; qi += kAttnThreads / 32) {
+    const float l = ps[qi * kTileKeys + lane];
+    const float mold = Ms[qi];
+    const float mnew = fmaxf(mold, warp_max(l));
+    const float pr = l <= 0.5f * kNegBig ? 0.f : exp2f(l - mnew);
+    const float s = warp_sum(pr);
+    ps[qi * kTileKeys + lane] = pr;
+    if (lane == 0) {
+      const float alpha = exp2f(mold - mnew);
+      als[qi] = alpha;
+      ls[qi] = ls[qi] * alpha + s;
+      Ms[qi] = mnew;
+    }
+  }
+  __syncthreads();
+  const int nsl = kAttnThreads / dv;  // query slices
+  const int d = tid % dv, q0 = tid / dv;
+  if (q0 < nsl) {
+    // rows past QG read zero probabilities and rescale factors (padded)
+#pragma unroll
+    for (int k = 0; k < QPT; ++k) oacc[k] *= als[q0 + k * nsl];
+    for (int jj = 0; jj < nk; ++jj) {
+      const float v = Vs[jj * dv + d];
+#pragma unroll
+      for (int k = 0; k < QPT; ++k)
+        oacc[k] = fmaf(ps[(q0 + k * nsl) * kTileKeys + jj], v, oacc[k]);
+    }
+  }
+  __syncthreads();
+}
+
+template <int QPT>
 __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnParams a) {
-  extern __shared__ __align__(16) float sm[];
+  extern __shared__ __align__(16) uint8_t smraw[];
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -66,25 +163,57 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
   const int QG = G * a.m;
   const int dqk = a.dqk, dv = a.dv;
   const int q_rows = a.nh * dqk * (a.gated ? 2 : 1);
-
-  float* Ks = sm;                                   // [TK][dqk+4]
-  float* Vs = Ks + kTileKeys * (dqk + 4);           // [TK][dv]
-  float* qs = Vs + kTileKeys * dv;                  // [QG][dqk]
-  float* ps = qs + QG * dqk;                        // [QG][TK]
-  float* Ms = ps + QG * kTileKeys;                  // [kMaxQ]
-  float* ls = Ms + kMaxQ;
-  float* als = ls + kMaxQ;
+  const AttnLayout Ly = attn_layout(dqk, dv, QG, a.m);
+  const int S = Ly.stages;
+  float* qs = reinterpret_cast<float*>(smraw + Ly.q_off);
+  float* ps = reinterpret_cast<float*>(smraw + Ly.p_off);
+  float* Ms = reinterpret_cast<float*>(smraw + Ly.stat_off);
+  float* ls = Ms + kPadQ;
+  float* als = ls + kPadQ;
+  float* newk = reinterpret_cast<float*>(smraw + Ly.newk_off);
+  float* newv = reinterpret_cast<float*>(smraw + Ly.newv_off);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smraw + Ly.bar_off);
   __shared__ bool last;
 
+  // cached keys [kbeg, L) in whole tiles per split; new keys go to the last split
   const int L = a.L;
-  const int kbeg = a.window > 0 ? max(0, L - a.window + 1) : 0;
-  const int kend = L + a.m;
-  const int chunk = (kend - kbeg + a.nsplit - 1) / a.nsplit;
-  const int c0 = min(kend, kbeg + split * chunk);
-  const int c1 = min(kend, c0 + chunk);
+  const int kbeg = a.window > 0 ? max(0, L + 1 - a.window) : 0;
+  const int ntiles = (L - kbeg + kTileKeys - 1) / kTileKeys;
+  const int tps = (ntiles + a.nsplit - 1) / a.nsplit;
+  const int t_begin = min(ntiles, split * tps);
+  const int t_end = min(ntiles, t_begin + tps);
+  const int my_tiles = t_end - t_begin;
+  const float* kbase = a.kc + (size_t)kvh * a.cap * dqk;
+  const float* vbase = a.vc + (size_t)kvh * a.cap * dv;
 
+  if (tid == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+    mbar_fence_init();
+  }
+  __syncthreads();
+
+  const uint64_t pol = l2_policy_evict_first();
+  // Warp 0 fills stage `slot` with tile `t` (relative to t_begin).
+  auto issue = [&](int t, int slot) {
+    const int key0 = kbeg + (t_begin + t) * kTileKeys;
+    const int nk = min(kTileKeys, L - key0);
+    uint8_t* st = smraw + (size_t)slot * Ly.stage_bytes;
+    float* Ks = reinterpret_cast<float*>(st);
+    float* Vs = Ks + kTileKeys * Ly.kstride;
+    if (lane == 0) mbar_arrive_expect_tx(&bars[slot], (uint32_t)nk * (dqk + dv) * 4);
+    __syncwarp();
+    if (lane < nk)
+      bulk_load(Ks + lane * Ly.kstride, kbase + (size_t)(key0 + lane) * dqk, dqk * 4, &bars[slot],
+                pol);
+    if (lane == 0)
+      bulk_load(Vs, vbase + (size_t)key0 * dv, (uint32_t)nk * dv * 4, &bars[slot], pol);
+  };
+  if (a.prefetch_before_wait && warp == 0)
+    for (int t = 0; t < S && t < my_tiles; ++t) issue(t, t);
   pdl_wait();
   pdl_launch_dependents();
+  if (!a.prefetch_before_wait && warp == 0)
+    for (int t = 0; t < S && t < my_tiles; ++t) issue(t, t);
 
   // ---- queries of this KV head: norm, rotate, pre-scale (log2 domain)
   const float qscale = a.scale * kLog2e;
@@ -95,123 +224,73 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
     for (int i = lane; i < dqk; i += 32) dst[i] = src[i];
     warp_norm_rope(dst, dqk, a.qn, a.eps, a.rope + (size_t)(L + r) * a.rot, a.rot, qscale, lane);
   }
-  // ---- new keys/values whose positions fall in this CTA's chunk: append
-  for (int r = warp; r < a.m; r += kAttnThreads / 32) {
-    const int pos = L + r;
-    if (pos < c0 || pos >= c1) continue;
-    float* kdst = a.kc + ((size_t)kvh * a.cap + pos) * dqk;
-    const float* ksrc = a.kp + (size_t)r * a.nkv * dqk + (size_t)kvh * dqk;
-    // normalise + rotate in the K tile area of shared memory, then store
-    float* tmp = Ks + warp * (dqk + 4);
-    for (int i = lane; i < dqk; i += 32) tmp[i] = ksrc[i];
-    warp_norm_rope(tmp, dqk, a.kn, a.eps, a.rope + (size_t)pos * a.rot, a.rot, 1.f, lane);
-    for (int i = lane; i < dqk; i += 32) kdst[i] = tmp[i];
-    float* vdst = a.vc + ((size_t)kvh * a.cap + pos) * dv;
-    const float* vsrc = a.vp + (size_t)r * a.nkv * dv + (size_t)kvh * dv;
-    for (int i = lane; i < dv; i += 32) vdst[i] = vsrc[i];
+  // ---- new keys/values (last split): normalise, rotate, append to the cache
+  const bool has_new = split == a.nsplit - 1;
+  if (has_new) {
+    for (int r = warp; r < a.m; r += kAttnThreads / 32) {
+      const int pos = L + r;
+      float* kn = newk + r * dqk;
+      const float* ksrc = a.kp + (size_t)r * a.nkv * dqk + (size_t)kvh * dqk;
+      for (int i = lane; i < dqk; i += 32) kn[i] = ksrc[i];
+      warp_norm_rope(kn, dqk, a.kn, a.eps, a.rope + (size_t)pos * a.rot, a.rot, 1.f, lane);
+      float* kdst = a.kc + ((size_t)kvh * a.cap + pos) * dqk;
+      for (int i = lane; i < dqk; i += 32) kdst[i] = kn[i];
+      float* vn = newv + r * dv;
+      const float* vsrc = a.vp + (size_t)r * a.nkv * dv + (size_t)kvh * dv;
+      float* vdst = a.vc + ((size_t)kvh * a.cap + pos) * dv;
+      for (int i = lane; i < dv; i += 32) {
+        const float v = vsrc[i];
+        vn[i] = v;
+        vdst[i] = v;
+      }
+    }
   }
-  if (tid < kMaxQ) {
-    Ms[tid] = kNegBig;
-    ls[tid] = 0.f;
+  for (int i = tid; i < kPadQ; i += kAttnThreads) {
+    Ms[i] = kNegBig;
+    ls[i] = 0.f;
+    als[i] = 0.f;
   }
+  for (int i = tid; i < kPadQ * kTileKeys; i += kAttnThreads) ps[i] = 0.f;
   __syncthreads();
 
-  float oacc[kMaxQ][2];
+  float oacc[QPT];
 #pragma unroll
-  for (int q = 0; q < kMaxQ; ++q) oacc[q][0] = oacc[q][1] = 0.f;
+  for (int k = 0; k < QPT; ++k) oacc[k] = 0.f;
 
-  const float* kbase = a.kc + (size_t)kvh * a.cap * dqk;
-  const float* vbase = a.vc + (size_t)kvh * a.cap * dv;
-  for (int t0 = c0; t0 < c1; t0 += kTileKeys) {
-    const int nk = min(kTileKeys, c1 - t0);
-    // load K and V tiles
-    const int kq4 = dqk / 4, vq4 = dv / 4;
-    for (int i = tid; i < kTileKeys * kq4; i += kAttnThreads) {
-      const int jj = i / kq4, d4 = i - jj * kq4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (jj < nk) v = *reinterpret_cast<const float4*>(kbase + (size_t)(t0 + jj) * dqk + d4 * 4);
-      *reinterpret_cast<float4*>(Ks + jj * (dqk + 4) + d4 * 4) = v;
+  for (int t = 0; t < my_tiles; ++t) {
+    const int slot = t % S;
+    const bool ok = mbar_wait_bounded(&bars[slot], (uint32_t)((t / S) & 1));
+    if (__syncthreads_or(!ok)) {  // the whole CTA gives up together
+      if (tid == 0) set_dev_error(a.err, kErrMbarTimeout);
+      return;
     }
-    for (int i = tid; i < kTileKeys * vq4; i += kAttnThreads) {
-      const int jj = i / vq4, d4 = i - jj * vq4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (jj < nk) v = *reinterpret_cast<const float4*>(vbase + (size_t)(t0 + jj) * dv + d4 * 4);
-      *reinterpret_cast<float4*>(Vs + jj * dv + d4 * 4) = v;
-    }
-    __syncthreads();
-    // logits
-    for (int pi = tid; pi < QG * kTileKeys; pi += kAttnThreads) {
-      const int jj = pi & (kTileKeys - 1), qi = pi / kTileKeys;
-      const int j = t0 + jj, r = qi / G, p = L + r;
-      float l = kNegBig;
-      const bool ok = jj < nk && j <= p && (a.window <= 0 || j > p - a.window);
-      if (ok) {
-        const float4* qv = reinterpret_cast<const float4*>(qs + qi * dqk);
-        const float4* kv = reinterpret_cast<const float4*>(Ks + jj * (dqk + 4));
-        float acc = 0.f;
-        for (int d4 = 0; d4 < kq4; ++d4) {
-          const float4 x = qv[d4], y = kv[d4];
-          acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
-        }
-        l = acc;
-      }
-      ps[qi * kTileKeys + jj] = l;
-    }
-    __syncthreads();
-    // online softmax update, one warp per query row
-    for (int qi = warp; qi < QG; qi += kAttnThreads / 32) {
-      const float l = ps[qi * kTileKeys + lane];
-      const float tmax = warp_max(l);
-      const float mold = Ms[qi];
-      const float mnew = fmaxf(mold, tmax);
-      const float pr = l <= 0.5f * kNegBig ? 0.f : exp2f(l - mnew);
-      const float s = warp_sum(pr);
-      ps[qi * kTileKeys + lane] = pr;
-      if (lane == 0) {
-        const float alpha = exp2f(mold - mnew);
-        als[qi] = alpha;
-        ls[qi] = ls[qi] * alpha + s;
-        Ms[qi] = mnew;
-      }
-    }
-    __syncthreads();
-    // o = alpha * o + P V
-#pragma unroll
-    for (int q = 0; q < kMaxQ; ++q) {
-      if (q < QG) {
-        const float al = als[q];
-        oacc[q][0] *= al;
-        oacc[q][1] *= al;
-      }
-    }
-    for (int jj = 0; jj < nk; ++jj) {
-      const float v0 = tid < dv ? Vs[jj * dv + tid] : 0.f;
-      const float v1 = tid + kAttnThreads < dv ? Vs[jj * dv + tid + kAttnThreads] : 0.f;
-#pragma unroll
-      for (int q = 0; q < kMaxQ; ++q) {
-        if (q < QG) {
-          const float pr = ps[q * kTileKeys + jj];
-          oacc[q][0] = fmaf(pr, v0, oacc[q][0]);
-          oacc[q][1] = fmaf(pr, v1, oacc[q][1]);
-        }
-      }
-    }
-    __syncthreads();
+    const float* Ks = reinterpret_cast<const float*>(smraw + (size_t)slot * Ly.stage_bytes);
+    const float* Vs = Ks + kTileKeys * Ly.kstride;
+    const int key0 = kbeg + (t_begin + t) * kTileKeys;
+    attend_tile<QPT>(a, Ks, Ly.kstride, Vs, min(kTileKeys, L - key0), key0, qs, ps, Ms, ls, als,
+                     oacc, QG, G);
+    if (warp == 0 && t + S < my_tiles) issue(t + S, slot);
   }
+  if (has_new)
+    attend_tile<QPT>(a, newk, dqk, newv, a.m, L, qs, ps, Ms, ls, als, oacc, QG, G);
 
-  // ---- partial of this split
-  const int pstride = dv + 2;
-  float* mypart = a.part + ((size_t)(kvh * a.nsplit + split) * QG) * pstride;
+  // ---- partial of this split: (M, l) pairs and unnormalised outputs
+  const size_t pidx = (size_t)(kvh * a.nsplit + split) * QG;
+  float* part_o = a.part + attn_part_o_offset(a.nkv, a.nsplit, QG);
+  {
+    const int nsl = kAttnThreads / dv;
+    const int d = tid % dv, q0 = tid / dv;
+    if (q0 < nsl) {
 #pragma unroll
-  for (int q = 0; q < kMaxQ; ++q) {
-    if (q < QG) {
-      if (tid < dv) mypart[q * pstride + 2 + tid] = oacc[q][0];
-      if (tid + kAttnThreads < dv) mypart[q * pstride + 2 + tid + kAttnThreads] = oacc[q][1];
+      for (int k = 0; k < QPT; ++k) {
+        const int q = q0 + k * nsl;
+        if (q < QG) part_o[(pidx + q) * dv + d] = oacc[k];
+      }
     }
   }
   if (tid < QG) {
-    mypart[tid * pstride + 0] = Ms[tid];
-    mypart[tid * pstride + 1] = ls[tid];
+    a.part[(pidx + tid) * 2 + 0] = Ms[tid];
+    a.part[(pidx + tid) * 2 + 1] = ls[tid];
   }
   __threadfence();
   __syncthreads();
@@ -223,38 +302,61 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
   if (!last) return;
   __threadfence();
 
-  // ---- merge (last CTA of this KV head)
-  float* fin = Ks;  // [QG][dv]
-  const float* kvpart = a.part + (size_t)kvh * a.nsplit * QG * pstride;
-  for (int qi = warp; qi < QG; qi += kAttnThreads / 32) {
-    const int h = kvh * G + qi % G;
-    float M = kNegBig;
-    for (int s = lane; s < a.nsplit; s += 32) M = fmaxf(M, __ldcg(kvpart + ((size_t)s * QG + qi) * pstride));
-    M = warp_max(M);
+  // ---- merge (last CTA of this KV head); the stage ring is free now
+  const int ns = a.nsplit;
+  float* wsm = reinterpret_cast<float*>(smraw);        // [ns][QG] split weights
+  float* fin = wsm + ns * QG;                          // [QG][dv]
+  const size_t base = (size_t)kvh * ns * QG;
+  for (int i = tid; i < ns * QG; i += kAttnThreads) wsm[i] = __ldcg(a.part + (base + i) * 2);
+  __syncthreads();
+  if (tid < QG) {
+    const int h = kvh * G + tid % G;
     const float sinkl2 = a.sinks ? a.sinks[h] * kLog2e : kNegBig;
-    M = fmaxf(M, sinkl2);
-    float den = 0.f;
-    for (int s = lane; s < a.nsplit; s += 32) {
-      const float* pp = kvpart + ((size_t)s * QG + qi) * pstride;
-      den += exp2f(__ldcg(pp) - M) * __ldcg(pp + 1);
-    }
-    den = warp_sum(den);
-    if (a.sinks) den += exp2f(sinkl2 - M);
+    float M = sinkl2;
+    for (int s = 0; s < ns; ++s) M = fmaxf(M, wsm[s * QG + tid]);
+    float den = a.sinks ? exp2f(sinkl2 - M) : 0.f;
+    for (int s = 0; s < ns; ++s)
+      den += exp2f(wsm[s * QG + tid] - M) * __ldcg(a.part + (base + s * QG + tid) * 2 + 1);
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int d = lane; d < dv; d += 32) {
-      float o = 0.f;
-      for (int s = 0; s < a.nsplit; ++s) {
-        const float* pp = kvpart + ((size_t)s * QG + qi) * pstride;
-        o = fmaf(exp2f(__ldcg(pp) - M), __ldcg(pp + 2 + d), o);
-      }
-      o *= inv;
-      if (a.gated) {
-        const int r = qi / G;
-        const float g = a.qp[(size_t)r * q_rows + (size_t)h * dqk * 2 + dqk + d];
-        o = o / (1.f + __expf(-g));
-      }
-      fin[qi * dv + d] = o;
+    for (int s = 0; s < ns; ++s) wsm[s * QG + tid] = exp2f(wsm[s * QG + tid] - M) * inv;
+  }
+  __syncthreads();
+  const int dv4 = dv / 4;
+  for (int it = tid; it < QG * dv4; it += kAttnThreads) {
+    const int qi = it / dv4, d4 = it - qi * dv4;
+    const float4* po = reinterpret_cast<const float4*>(part_o + (base + qi) * dv) + d4;
+    const size_t sstride = (size_t)QG * dv4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    int s = 0;
+    for (; s + 4 <= ns; s += 4) {
+      const float4 v0 = __ldcg(po + (size_t)s * sstride);
+      const float4 v1 = __ldcg(po + (size_t)(s + 1) * sstride);
+      const float4 v2 = __ldcg(po + (size_t)(s + 2) * sstride);
+      const float4 v3 = __ldcg(po + (size_t)(s + 3) * sstride);
+      const float w0 = wsm[s * QG + qi], w1 = wsm[(s + 1) * QG + qi];
+      const float w2 = wsm[(s + 2) * QG + qi], w3 = wsm[(s + 3) * QG + qi];
+      acc.x += w0 * v0.x + w1 * v1.x + w2 * v2.x + w3 * v3.x;
+      acc.y += w0 * v0.y + w1 * v1.y + w2 * v2.y + w3 * v3.y;
+      acc.z += w0 * v0.z + w1 * v1.z + w2 * v2.z + w3 * v3.z;
+      acc.w += w0 * v0.w + w1 * v1.w + w2 * v2.w + w3 * v3.w;
     }
+    for (; s < ns; ++s) {
+      const float4 v = __ldcg(po + (size_t)s * sstride);
+      const float w = wsm[s * QG + qi];
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    float o[4] = {acc.x, acc.y, acc.z, acc.w};
+    if (a.gated) {
+      const int r = qi / G, h = kvh * G + qi % G;
+      const float* g = a.qp + (size_t)r * q_rows + (size_t)h * dqk * 2 + dqk + d4 * 4;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[e] = o[e] / (1.f + __expf(-g[e]));
+    }
+#pragma unroll
+    for (int e = 0; e < 4; ++e) fin[qi * dv + d4 * 4 + e] = o[e];
   }
   __syncthreads();
   // fp32 output and packed copy: octets of (row, head, dims)
@@ -262,7 +364,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
   const int total_oct = QG * oct_per_q;
   for (int o0 = 0; o0 < total_oct; o0 += kAttnThreads) {
     const int oi = o0 + tid;
-    float sum = 0.f;
+    float2 sum = make_float2(0.f, 0.f);
     int r = 0, k = 0;
     if (oi < total_oct) {
       const int qi = oi / oct_per_q, oc = oi - qi * oct_per_q;
@@ -286,8 +388,10 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
     }
     if (a.out_xp) {
       // the four octets of a group are adjacent (dv % 32 == 0, kAttnThreads % 4 == 0)
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 1);
+      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
+      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
+      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 2);
       if (oi < total_oct && (oi & 3) == 0) a.out_xs[(k / kGroup) * a.m + r] = sum;
     }
   }
@@ -295,27 +399,28 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
 }
 
 int attn_splits(int nkv, int keys) {
-  const int target = 2 * sm_count();  // about two CTAs per SM
+  const int target = sm_count();  // about one CTA per SM
   int ns = (target + nkv - 1) / nkv;
-  const int max_by_keys = (keys + kTileKeys - 1) / kTileKeys;  // at least one tile per split
-  if (ns > max_by_keys) ns = max_by_keys;
+  const int max_by_tiles = (keys + kTileKeys - 1) / kTileKeys;  // at least one tile per split
+  if (ns > max_by_tiles) ns = max_by_tiles;
   if (ns < 1) ns = 1;
   return ns;
 }
 
 size_t attn_part_bytes(int nkv, int nsplit, int q_per_kv, int dv) {
-  return (size_t)nkv * nsplit * q_per_kv * (dv + 2) * sizeof(float);
+  return (attn_part_o_offset(nkv, nsplit, q_per_kv) + (size_t)nkv * nsplit * q_per_kv * dv) *
+         sizeof(float);
 }
 
-cudaError_t launch_attn(const AttnParams& a, cudaStream_t st) {
-  const int QG = (a.nh / a.nkv) * a.m;
-  const size_t smem = AttnSmem::bytes(a.dqk, a.dv, QG);
+template <int QPT>
+static cudaError_t launch_attn_t(const AttnParams& a, size_t smem, cudaStream_t st) {
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, 200 * 1024);
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<QPT>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kAttnSmemMax + 1024);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
@@ -329,7 +434,22 @@ cudaError_t launch_attn(const AttnParams& a, cudaStream_t st) {
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel, a);
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<QPT>, a);
+}
+
+cudaError_t launch_attn(const AttnParams& a, cudaStream_t st) {
+  const int QG = (a.nh / a.nkv) * a.m;
+  const AttnLayout Ly = attn_layout(a.dqk, a.dv, QG, a.m);
+  // the merge reuses the stage ring: split weights and the finished rows
+  const size_t merge = (size_t)a.nsplit * QG * 4 + (size_t)QG * a.dv * 4;
+  const size_t smem = Ly.total > merge ? Ly.total : merge;
+  if (smem > (size_t)kAttnSmemMax + 1024) return cudaErrorInvalidValue;
+  const int nsl = kAttnThreads / a.dv;
+  const int need = (QG + nsl - 1) / nsl;
+  if (need <= 1) return launch_attn_t<1>(a, smem, st);
+  if (need <= 2) return launch_attn_t<2>(a, smem, st);
+  if (need <= 4) return launch_attn_t<4>(a, smem, st);
+  return launch_attn_t<8>(a, smem, st);
 }
 
 }  // namespace mtp

@@ -3,13 +3,14 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
 namespace mtp {
 
 constexpr int kGroup = 32;               // affine quantisation group
-constexpr unsigned kWaitLimit = 1u << 24; // bounded device-side waits (iterations)
+constexpr unsigned kWaitLimit = 2000;     // bounded device-side waits (polls of at most 1 ms)
 
 // Workspace header shared by every entry point that takes a workspace.
 // word 0: device error code; words 1..: completion counters.
@@ -50,21 +51,21 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
+  // The hint lets the hardware suspend the thread (up to 1 ms) until the
+  // phase completes instead of spinning on issue slots.
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, 1000000;\n"
       " selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
 }
-// Waits for phase `parity` of `bar`; gives up after kWaitLimit polls and
-// returns false (the caller records the error and stops).
+// Waits for phase `parity` of `bar`; gives up after kWaitLimit polls (each
+// suspends at most 1 ms) and returns false (the caller records the error).
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
-  for (unsigned it = 0; it < kWaitLimit; ++it) {
+  for (unsigned it = 0; it < kWaitLimit; ++it)
     if (mbar_try_wait(bar, parity)) return true;
-    if (it > 64) __nanosleep(32);
-  }
   return false;
 }
 
@@ -73,6 +74,20 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
   uint64_t pol;
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
   return pol;
+}
+__device__ __forceinline__ uint64_t l2_policy_evict_last() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// 1-D bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
+                                          uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
 }
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* m) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(m)) : "memory");
@@ -89,12 +104,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
 }
 
 // ---------------------------------------------------------------- tensor core
-// D = A(16x16 bf16, row) * B(16x8 bf16, col) + D, fp32 accumulate.
-__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
-                                               uint32_t a2, uint32_t a3, uint32_t b0,
-                                               uint32_t b1) {
+// D = A(16x16 f16, row) * B(16x8 f16, col) + D, f32 accumulate.
+__device__ __forceinline__ void mma_f16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0,
+                                              uint32_t b1) {
   asm volatile(
-      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};\n"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -107,16 +122,14 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t
                : "r"(addr));
 }
 
-// Two 4-bit codes -> bf16x2 (128 + c_lo, 128 + c_hi): bits 0..3 and 16..19 of
-// `w` become the low mantissa bits of two bf16 values with exponent 2^7.
-__device__ __forceinline__ uint32_t codes_to_bf16x2_biased(uint32_t w) {
-  return (w & 0x000F000Fu) | 0x43004300u;
+// 4-bit codes -> f16x2 with the code in the mantissa of 1024 (exponent 2^10,
+// unit LSB): bits 0..3 and 16..19 of `w` give (1024 + c, 1024 + c');
+// bits 4..7 and 20..23 give (1024 + 16c, 1024 + 16c').  One LOP3 each.
+__device__ __forceinline__ uint32_t codes_lo_f16x2(uint32_t w) {
+  return (w & 0x000F000Fu) | 0x64006400u;
 }
-
-// fp32 -> (hi, lo) bf16 split with hi + lo ~= x to about 2^-16 relative.
-__device__ __forceinline__ void split_bf16(float x, __nv_bfloat16& hi, __nv_bfloat16& lo) {
-  hi = __float2bfloat16_rn(x);
-  lo = __float2bfloat16_rn(x - __bfloat162float(hi));
+__device__ __forceinline__ uint32_t codes_hi_f16x2(uint32_t w) {
+  return (w & 0x00F000F0u) | 0x64006400u;
 }
 
 __device__ __forceinline__ float warp_sum(float v) {

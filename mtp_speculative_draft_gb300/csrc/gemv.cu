@@ -47,13 +47,13 @@ __global__ void gemv_simple_kernel(const float* __restrict__ x, int m, int K,
 // One thread per (group, column, octet); the four octets of a group are
 // adjacent lanes and combine their sums with two shuffles.
 __global__ void pack_x_kernel(const float* __restrict__ x, int m, int K, uint4* __restrict__ xp,
-                              float* __restrict__ xs) {
+                              float2* __restrict__ xs) {
+  pdl_launch_dependents();  // the projection that follows only reads weights before its wait
   pdl_wait();
-  pdl_launch_dependents();
   const int G = K / kGroup;
   const int total = G * m * 4;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  float sum = 0.f;
+  float2 sum = make_float2(0.f, 0.f);
   if (i < total) {
     const int t = i & 3;
     const int gc = i >> 2;
@@ -67,8 +67,10 @@ __global__ void pack_x_kernel(const float* __restrict__ x, int m, int K, uint4* 
     xp[xp_index(g, c, t, 0, m)] = hi;
     xp[xp_index(g, c, t, 1, m)] = lo;
   }
-  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 1);
+  sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
+  sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
+  sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 2);
   if (i < total && (i & 3) == 0) {
     const int gc = i >> 2;
     xs[(gc / m) * m + gc % m] = sum;
@@ -83,23 +85,76 @@ static cudaLaunchAttribute pdl_attr() {
   return a;
 }
 
-template <int NMAT, int NT, int EPI>
-static cudaError_t launch_gemv_t(const GemvParams& p, int tiles, cudaStream_t st) {
-  constexpr int S = NMAT == 1 ? 4 : 2;
-  auto kern = gemv_tc_kernel<NMAT, NT, EPI, S>;
-  const int smem = gemv_smem_bytes<NMAT, S>();
+// Split-K plan: units of `spu` stages; a split is only used when all its
+// units fit in one round of the resident warps, and the plan minimises the
+// stages on a warp's critical path (plus a small cost per partial).
+struct Plan {
+  int ksplit, spu, units;
+};
+static Plan plan_split(int tiles, int KS, int warps_cap, int nacc, const GemvScratch& sc) {
+  Plan best = {1, KS, tiles};
+  double best_cost = 1e30;
+  for (int spu = KS; spu >= 1; --spu) {
+    const int ksplit = (KS + spu - 1) / spu;
+    if (ksplit > 1 && spu * (ksplit - 1) >= KS) continue;  // same split as a larger spu
+    const long long units = (long long)tiles * ksplit;
+    if (ksplit > 1) {
+      if (units > warps_cap) continue;
+      if (tiles > sc.cnt_len) continue;
+      if ((size_t)units * 32 * nacc * sizeof(float) > sc.part_bytes) continue;
+    }
+    const long long rounds = (units + warps_cap - 1) / warps_cap;
+    const double cost = (double)rounds * spu + (ksplit > 1 ? 1.0 + 0.15 * ksplit : 0.0);
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = {ksplit, spu, (int)units};
+    }
+  }
+  return best;
+}
+
+size_t gemv_scratch_part_bytes() {
+  // one round of resident warps (at most 16 per SM) x 32 lanes x 32 floats
+  return (size_t)sm_count() * 16 * 32 * 32 * sizeof(float);
+}
+
+// Stage depth of each warp's pipeline and whether m = 1 activations are
+// staged through shared memory (compile-time tuning knobs).
+#ifndef MTP_GEMV_STAGES
+#define MTP_GEMV_STAGES 2
+#endif
+#ifndef MTP_GEMV_STAGE_X1
+#define MTP_GEMV_STAGE_X1 0
+#endif
+
+template <int NMAT, int NT, int EPI, int XM, bool C1>
+static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
+                                 cudaStream_t st) {
+  constexpr int S = MTP_GEMV_STAGES;
+  auto kern = gemv_tc_kernel<NMAT, NT, EPI, S, XM, C1>;
+  const int smem = gemv_smem_bytes<NMAT, S, XM>();
   static thread_local int configured_dev = -1;
+  static thread_local int ctas_per_sm = 1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    int nb = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kGemvWarps * 32, smem);
+    if (e != cudaSuccess) return e;
+    ctas_per_sm = nb > 0 ? nb : 1;
     configured_dev = dev;
   }
-  const int ctas_per_sm = 2;
-  int grid = (tiles + kGemvWarps - 1) / kGemvWarps;
-  const int cap = sm_count() * ctas_per_sm;
-  if (grid > cap) grid = cap;
+  const int warps_cap = sm_count() * ctas_per_sm * kGemvWarps;
+  const int KS = (p.K / kGroup + 7) / 8;
+  const Plan pl = plan_split(tiles, KS, warps_cap, NMAT * 2 * NT * 4, sc);
+  p.ksplit = pl.ksplit;
+  p.spu = pl.spu;
+  p.part = sc.part;
+  p.tile_cnt = sc.cnt;
+  int warps = pl.units < warps_cap ? pl.units : warps_cap;
+  int grid = (warps + kGemvWarps - 1) / kGemvWarps;
   if (grid < 1) grid = 1;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -112,20 +167,31 @@ static cudaError_t launch_gemv_t(const GemvParams& p, int tiles, cudaStream_t st
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-cudaError_t launch_gemv(int nmat, int nt, int epi, const GemvParams& p, int tiles,
-                        cudaStream_t st) {
-  if (epi == kEpiArgmax) return launch_gemv_t<1, 1, kEpiArgmax>(p, tiles, st);
+cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
+                        const GemvScratch& sc, cudaStream_t st) {
+  const int m = p.m;
+  // activations staged per stage by bulk copy for up to 4 columns
+  const bool c1 = (m == 1);
+  constexpr int X1 = MTP_GEMV_STAGE_X1 ? 1 : 0;
+  if (epi == kEpiArgmax) {
+    if (m != 1) return cudaErrorInvalidValue;
+    return launch_gemv_t<1, 1, kEpiArgmax, X1, true>(p, tiles, sc, st);
+  }
   if (nmat == 1) {
     if (epi != kEpiStore) return cudaErrorInvalidValue;
-    return nt == 1 ? launch_gemv_t<1, 1, kEpiStore>(p, tiles, st)
-                   : launch_gemv_t<1, 2, kEpiStore>(p, tiles, st);
+    if (nt == 2) return launch_gemv_t<1, 2, kEpiStore, 0, false>(p, tiles, sc, st);
+    if (c1) return launch_gemv_t<1, 1, kEpiStore, X1, true>(p, tiles, sc, st);
+    if (m <= 4) return launch_gemv_t<1, 1, kEpiStore, 4, false>(p, tiles, sc, st);
+    return launch_gemv_t<1, 1, kEpiStore, 0, false>(p, tiles, sc, st);
   }
   if (epi != kEpiSwiglu) return cudaErrorInvalidValue;
-  return nt == 1 ? launch_gemv_t<2, 1, kEpiSwiglu>(p, tiles, st)
-                 : launch_gemv_t<2, 2, kEpiSwiglu>(p, tiles, st);
+  if (nt == 2) return launch_gemv_t<2, 2, kEpiSwiglu, 0, false>(p, tiles, sc, st);
+  if (c1) return launch_gemv_t<2, 1, kEpiSwiglu, X1, true>(p, tiles, sc, st);
+  if (m <= 4) return launch_gemv_t<2, 1, kEpiSwiglu, 4, false>(p, tiles, sc, st);
+  return launch_gemv_t<2, 1, kEpiSwiglu, 0, false>(p, tiles, sc, st);
 }
 
-cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float* xs, cudaStream_t st) {
+cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float2* xs, cudaStream_t st) {
   const int total = (K / kGroup) * m * 4;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((total + 255) / 256);

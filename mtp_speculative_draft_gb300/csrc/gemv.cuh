@@ -11,11 +11,14 @@
 // 1 KB of biases.  Codes go shared -> registers with ldmatrix, which hands
 // lane (g, t) word t of a group for rows g and g+8 -- exactly the
 // m16n8k16 A-fragment slots once the k order inside a group is permuted.
-// Two nibbles become one bf16x2 register with a single LOP3 (128 + code,
-// exact), the dot products run on the tensor pipe against the activations
-// split into bf16 hi + lo parts (fp32 accumulation), and the per-group scale
-// and bias are applied in fp32 after each group:
-//     y += s * D + (b - 128 s) * sum_group(x)          D = sum (128+code) x
+// Codes become f16x2 registers with one LOP3 each and no shift for two of
+// the four nibble pairs of a word: nibbles at bits 0-3/16-19 give 1024 + c,
+// nibbles at bits 4-7/20-23 give 1024 + 16c (both exact in f16).  The
+// activations are split into f16 hi + lo parts (about 22 bits), the slots
+// that meet a 16c code carry x/16, and the products run on the tensor pipe
+// with f32 accumulation.  The accumulator starts at -1024 * (sum of the
+// represented activations) so it ends at sum(code * x); the per-group scale
+// and bias are applied in f32 after each group:  y += s * D + b * sum(x).
 // Activations arrive pre-packed ("xpack") in the B-fragment order with the
 // per-group sums precomputed by the producer kernel.
 #pragma once
@@ -25,46 +28,67 @@
 namespace mtp {
 
 // ------------------------------------------------------------------ xpack
-// For activations X[m][K]: xp is uint4 [K/32][m][4][2] and xs float [K/32][m].
-// Entry (g, c, t, hl): hl = 0 holds the bf16 "hi" parts, 1 the "lo" parts, of
-// x[c][32g + 8t + p] for p in (0,4),(1,5),(2,6),(3,7) as bf16x2 words
-// (first element in the low half).  xs[g][c] = sum over the group of hi + lo.
+// For activations X[m][K]: xp is uint4 [G8][m][4][2] and xs float2 [G8][m]
+// (G8 = K/32 rounded up to whole stages of 8 groups).  Entry (g, c, t, hl):
+// hl = 0 holds the f16 "hi" parts, 1 the "lo" parts, of the eight values
+// x[c][32g + 8t + p] as f16x2 words (first element in the low half):
+//   word 0: (p0, p4)   word 1: (p1/16, p5/16)   word 2: (p2, p6)   word 3: (p3/16, p7/16)
+// xs[g][c] = (sum of the represented x over the group,
+//             1024 * sum of the represented stored values) -- the second
+// component is what the +1024 code bias adds to the tensor-core sum.
+// Activations must lie within the f16 range (|x| < 65504).
+__host__ __device__ inline int xpack_groups(int K) { return (K / kGroup + 7) / 8 * 8; }
+__host__ __device__ inline size_t xpack_xs_offset(int m, int K) {
+  return (size_t)xpack_groups(K) * m * 128;
+}
+// Buffers hold whole stages of 8 groups; groups past K/32 are read by the
+// GEMV (with zero weights) and must hold finite values (they start zeroed).
 __host__ __device__ inline size_t xpack_bytes(int m, int K) {
-  return (size_t)(K / kGroup) * m * 128 + (size_t)(K / kGroup) * m * 4;
+  return xpack_xs_offset(m, K) + (size_t)xpack_groups(K) * m * 8;
 }
 __device__ __forceinline__ int xp_index(int g, int c, int t, int hl, int m) {
   return ((g * m + c) * 4 + t) * 2 + hl;
 }
 
-// Packs the eight values of (g, c, t); returns their hi+lo sum.
-__device__ __forceinline__ float pack8(const float v[8], uint4& hi, uint4& lo) {
-  __nv_bfloat16 h[8], l[8];
-  float sum = 0.f;
+// f32 -> (hi, lo) f16 split; returns hi + lo as f32.
+__device__ __forceinline__ float split_f16(float x, __half& hi, __half& lo) {
+  hi = __float2half_rn(x);
+  const float h = __half2float(hi);
+  lo = __float2half_rn(x - h);
+  return h + __half2float(lo);
+}
+
+// Packs the eight values of (g, c, t); returns their (sum, correction) pair.
+__device__ __forceinline__ float2 pack8(const float v[8], uint4& hi, uint4& lo) {
+  __half h[8], l[8];
+  float sa = 0.f, sb = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    split_bf16(v[i], h[i], l[i]);
-    sum += __bfloat162float(h[i]) + __bfloat162float(l[i]);
+    const bool bslot = (i & 1) != 0;  // elements 1, 3, 5, 7 meet a 16*code
+    const float r = split_f16(bslot ? v[i] * 0.0625f : v[i], h[i], l[i]);
+    if (bslot) sb += r; else sa += r;
   }
-  auto pk = [](__nv_bfloat16 a, __nv_bfloat16 b) -> uint32_t {
-    return (uint32_t)__bfloat16_as_ushort(a) | ((uint32_t)__bfloat16_as_ushort(b) << 16);
+  auto pk = [](__half a, __half b) -> uint32_t {
+    return (uint32_t)__half_as_ushort(a) | ((uint32_t)__half_as_ushort(b) << 16);
   };
   hi = make_uint4(pk(h[0], h[4]), pk(h[1], h[5]), pk(h[2], h[6]), pk(h[3], h[7]));
   lo = make_uint4(pk(l[0], l[4]), pk(l[1], l[5]), pk(l[2], l[6]), pk(l[3], l[7]));
-  return sum;
+  return make_float2(sa + 16.f * sb, 1024.f * (sa + sb));
 }
 
-// Position of element p (0..7) of an (g, c, t) octet inside its uint4:
-// word p % 4, half p / 4.
-__device__ __forceinline__ void xp_store_elem(uint4* xp, int m, int g, int c, int t, int p,
-                                              float v, float* hilo_sum) {
-  __nv_bfloat16 h, l;
-  split_bf16(v, h, l);
+// Stores element p (0..7) of an (g, c, t) octet: word p % 4, half p / 4.
+// Returns its contribution to the group's (sum, correction) pair.
+__device__ __forceinline__ float2 xp_store_elem(uint4* xp, int m, int g, int c, int t, int p,
+                                               float v) {
+  const bool bslot = (p & 1) != 0;
+  __half h, l;
+  const float r = split_f16(bslot ? v * 0.0625f : v, h, l);
   unsigned short* base = reinterpret_cast<unsigned short*>(xp);
-  size_t w_hi = (size_t)xp_index(g, c, t, 0, m) * 8 + (p & 3) * 2 + (p >> 2);
-  size_t w_lo = (size_t)xp_index(g, c, t, 1, m) * 8 + (p & 3) * 2 + (p >> 2);
-  base[w_hi] = __bfloat16_as_ushort(h);
-  base[w_lo] = __bfloat16_as_ushort(l);
-  *hilo_sum = __bfloat162float(h) + __bfloat162float(l);
+  const size_t w_hi = (size_t)xp_index(g, c, t, 0, m) * 8 + (p & 3) * 2 + (p >> 2);
+  const size_t w_lo = (size_t)xp_index(g, c, t, 1, m) * 8 + (p & 3) * 2 + (p >> 2);
+  base[w_hi] = __half_as_ushort(h);
+  base[w_lo] = __half_as_ushort(l);
+  return make_float2(bslot ? 16.f * r : r, 1024.f * r);
 }
 
 // ------------------------------------------------------------------ params
@@ -94,7 +118,7 @@ constexpr int kMaxSeg = 10;
 struct GemvParams {
   QMat mat[4];
   const uint4* xp;
-  const float* xs;
+  const float2* xs;
   int m;
   int K;                 // reduction length (concatenated length in K-segment mode)
   int nseg;
@@ -109,7 +133,7 @@ struct GemvParams {
   int kseg_last_mat;     // < 0: every K segment is routed; else the last one reads this slot
   // SwiGLU pack target
   uint4* out_xp;
-  float* out_xs;
+  float2* out_xs;
   int out_m;
   // argmax
   unsigned long long* am_partial;  // [gridDim.x]
@@ -117,15 +141,33 @@ struct GemvParams {
   int* am_token;
   float* am_value;
   float* logits;                    // optional fp32 logits
+  // split-K over units of `spu` stages: partial fragments and per-tile counters
+  int ksplit;
+  int spu;
+  float* part;
+  unsigned* tile_cnt;
   int* err;
 };
 
 constexpr int kStageMatBytes = 6144;  // 4 KB codes + 1 KB scales + 1 KB biases
 constexpr int kGemvWarps = 4;
+constexpr int kXChunk = 1088;         // staged activations per column: 8 groups x (128 + 8) bytes
 
-template <int NMAT, int S>
-constexpr int gemv_smem_bytes() {
-  return kGemvWarps * S * NMAT * kStageMatBytes + 2048;  // + barriers + alignment slack
+// Bytes of staged activations per stage, padded so every tensor-map
+// destination stays 128-byte aligned.
+template <int XM>
+__host__ __device__ constexpr int gemv_xchunk_bytes() {
+  return (XM * kXChunk + 127) / 128 * 128;
+}
+// Per-stage shared-memory footprint: NMAT weight slabs plus, when XM > 0, the
+// activation fragments of the stage's 8 groups for up to XM columns.
+template <int NMAT, int XM>
+__host__ __device__ constexpr int gemv_stage_bytes() {
+  return NMAT * kStageMatBytes + gemv_xchunk_bytes<XM>();
+}
+template <int NMAT, int S, int XM>
+__host__ __device__ constexpr int gemv_smem_bytes() {
+  return kGemvWarps * S * gemv_stage_bytes<NMAT, XM>() + 2048;  // + barriers + alignment slack
 }
 
 __device__ __forceinline__ unsigned long long argmax_key(float v, int idx) {
@@ -142,10 +184,6 @@ __device__ __forceinline__ int argmax_key_index(unsigned long long k) {
   return (int)(0xFFFFFFFFu - (uint32_t)(k & 0xFFFFFFFFu));
 }
 
-struct StageInfo {
-  int seg, mat, row, kx, sx;
-};
-
 __device__ __forceinline__ int find_seg(const GemvParams& p, int tile) {
   int s = 0;
 #pragma unroll 1
@@ -153,35 +191,62 @@ __device__ __forceinline__ int find_seg(const GemvParams& p, int tile) {
   return s;
 }
 
-__device__ __forceinline__ StageInfo stage_info(const GemvParams& p, int tile, int ks) {
-  StageInfo si;
-  si.seg = find_seg(p, tile);
-  const GemvSeg& sg = p.seg[si.seg];
-  const int lt = tile - (si.seg ? p.seg[si.seg - 1].tile_end : 0);
-  if (p.kseg_len > 0) {
-    const int spk = p.kseg_len / 256;
-    const int kj = ks / spk;
-    const int kin = ks - kj * spk;
-    if (p.kseg_last_mat < 0 || kj < p.nkseg - 1) {
-      si.mat = sg.mat;
-      si.row = p.rowsel[kj] * p.kseg_row_mult + lt * 32;
-    } else {
-      si.mat = p.kseg_last_mat;
-      si.row = lt * 32;
+// Position of a warp in its sequence of work units.  A unit is (tile,
+// k-chunk): 32 output rows over stages [ks, ke) of the reduction.  The
+// segment, matrix slot and first weight row of the unit are resolved once
+// when the unit starts, so advancing by a stage costs a compare.
+struct Cursor {
+  int u, ks, ke, tile, seg, mat, row;
+  __device__ __forceinline__ void start(const GemvParams& p, int u0, int units, int ksplit,
+                                        int spu, int KS) {
+    u = u0;
+    if (u < units) {
+      tile = u / ksplit;
+      const int kc = u - tile * ksplit;
+      ks = kc * spu;
+      ke = min(KS, ks + spu);
+      seg = find_seg(p, tile);
+      const GemvSeg& sg = p.seg[seg];
+      const int lt = tile - (seg ? p.seg[seg - 1].tile_end : 0);
+      mat = sg.mat;
+      row = (sg.sel_idx >= 0 ? p.rowsel[sg.sel_idx] * sg.row_mult : 0) + lt * 32;
     }
-    si.kx = kin * 32;
-    si.sx = kin * 8;
-  } else {
-    si.mat = sg.mat;
-    si.row = (sg.sel_idx >= 0 ? p.rowsel[sg.sel_idx] * sg.row_mult : 0) + lt * 32;
-    si.kx = ks * 32;
-    si.sx = ks * 8;
   }
-  return si;
-}
+  // returns true when the unit just finished
+  __device__ __forceinline__ bool advance(const GemvParams& p, int W, int units, int ksplit,
+                                          int spu, int KS) {
+    if (++ks < ke) return false;
+    start(p, u + W, units, ksplit, spu, KS);
+    return true;
+  }
+  // weight coordinates of the current stage
+  __device__ __forceinline__ void coords(const GemvParams& p, int& m_out, int& r_out, int& kx,
+                                         int& sx) const {
+    if (p.kseg_len > 0) {
+      const int spk = p.kseg_len / 256;
+      const int kj = ks / spk;
+      const int kin = ks - kj * spk;
+      const int lt = row;  // row holds lt * 32 in this mode (no sel on the segment)
+      if (p.kseg_last_mat < 0 || kj < p.nkseg - 1) {
+        m_out = mat;
+        r_out = p.rowsel[kj] * p.kseg_row_mult + lt;
+      } else {
+        m_out = p.kseg_last_mat;
+        r_out = lt;
+      }
+      kx = kin * 32;
+      sx = kin * 8;
+    } else {
+      m_out = mat;
+      r_out = row;
+      kx = ks * 32;
+      sx = ks * 8;
+    }
+  }
+};
 
-template <int NMAT, int NT, int EPI, int S>
-__global__ void __launch_bounds__(kGemvWarps * 32)
+template <int NMAT, int NT, int EPI, int S, int XM, bool C1>
+__global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 2)
     gemv_tc_kernel(const __grid_constant__ GemvParams p) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of each codes tile is required by the 128B swizzle.
@@ -192,17 +257,21 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
   const int gid = lane >> 2;
   const int tq = lane & 3;
 
-  constexpr int kWarpBytes = S * NMAT * kStageMatBytes;
-  uint8_t* wbase = smem + warp * kWarpBytes;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kGemvWarps * kWarpBytes) + warp * S;
+  constexpr int kCode = NMAT * 4096;                   // codes per stage (1 KB aligned)
+  constexpr int kRest = NMAT * 2048 + gemv_xchunk_bytes<XM>();  // scales, biases, activations
+  uint8_t* code_base = smem + warp * S * kCode;
+  uint8_t* rest_base = smem + kGemvWarps * S * kCode + warp * S * kRest;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + kGemvWarps * S * (kCode + kRest)) + warp * S;
 
+  const int m = p.m;
   const int G = p.K / kGroup;
   const int KS = (G + 7) / 8;
+  const int ksplit = p.ksplit, spu = p.spu;
   const int W = gridDim.x * kGemvWarps;
   const int gw = warp * gridDim.x + blockIdx.x;
   const int total_tiles = p.seg[p.nseg - 1].tile_end;
-  const int my_tiles = gw < total_tiles ? (total_tiles - gw + W - 1) / W : 0;
-  const int total = my_tiles * KS;
+  const int units = total_tiles * ksplit;
 
   if (lane == 0) {
     for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
@@ -210,41 +279,66 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
   }
   __syncwarp();
 
-  const uint64_t pol = l2_policy_evict_first();
-  auto issue = [&](int i) {
-    const int ti = i / KS;
-    const int ks = i - ti * KS;
-    const StageInfo si = stage_info(p, gw + ti * W, ks);
-    const int slot = i % S;
-    uint8_t* st = wbase + slot * NMAT * kStageMatBytes;
-    mbar_arrive_expect_tx(&bars[slot], NMAT * kStageMatBytes);
+  const uint64_t pol_w = l2_policy_evict_first();
+  const uint64_t pol_x = l2_policy_evict_last();
+  auto issue_w = [&](const Cursor& c, int slot) {
+    int mat, row, kx, sx;
+    c.coords(p, mat, row, kx, sx);
+    uint8_t* cd = code_base + slot * kCode;
+    uint8_t* rs = rest_base + slot * kRest;
+    uint32_t bytes = NMAT * kStageMatBytes;
+    if (XM > 0) bytes += (uint32_t)8 * m * (128 + 8);
+    mbar_arrive_expect_tx(&bars[slot], bytes);
 #pragma unroll
     for (int mi = 0; mi < NMAT; ++mi) {
-      const QMat& mt = p.mat[si.mat + mi];
-      uint8_t* d = st + mi * kStageMatBytes;
-      tma_load_2d(d, &mt.q, &bars[slot], si.kx, si.row, pol);
-      tma_load_2d(d + 4096, &mt.s, &bars[slot], si.sx, si.row, pol);
-      tma_load_2d(d + 5120, &mt.b, &bars[slot], si.sx, si.row, pol);
+      const QMat& mt = p.mat[mat + mi];
+      tma_load_2d(cd + mi * 4096, &mt.q, &bars[slot], kx, row, pol_w);
+      tma_load_2d(rs + mi * 2048, &mt.s, &bars[slot], sx, row, pol_w);
+      tma_load_2d(rs + mi * 2048 + 1024, &mt.b, &bars[slot], sx, row, pol_w);
+    }
+  };
+  auto issue_x = [&](const Cursor& c, int slot) {
+    if constexpr (XM > 0) {
+      uint8_t* rs = rest_base + slot * kRest + NMAT * 2048;
+      const int g0 = c.ks * 8;
+      bulk_load(rs, p.xp + (size_t)g0 * m * 8, (uint32_t)8 * m * 128, &bars[slot], pol_x);
+      bulk_load(rs + XM * 1024, p.xs + (size_t)g0 * m, (uint32_t)8 * m * 8, &bars[slot], pol_x);
     }
   };
 
   // Weights never depend on the previous kernel: start streaming them before
-  // waiting on it, unless the rows to stream are chosen by it.
-  if (!p.rowsel_after_wait && lane == 0) {
-    for (int i = 0; i < S && i < total; ++i) issue(i);
+  // waiting on it, unless the rows to stream are chosen by it (then even the
+  // cursor, which resolves those rows, starts after the wait).
+  Cursor pc, cc;
+  int pre = 0;
+  Cursor pre_c[S];
+  if (!p.rowsel_after_wait) {
+    pc.start(p, gw, units, ksplit, spu, KS);
+    cc = pc;
+    if (lane == 0) {
+      for (; pre < S && pc.u < units; ++pre) {
+        pre_c[pre] = pc;
+        issue_w(pc, pre);
+        pc.advance(p, W, units, ksplit, spu, KS);
+      }
+    }
   }
   pdl_wait();
   pdl_launch_dependents();
-  if (p.rowsel_after_wait && lane == 0) {
-    for (int i = 0; i < S && i < total; ++i) issue(i);
+  if (p.rowsel_after_wait) {
+    pc.start(p, gw, units, ksplit, spu, KS);
+    cc = pc;
+  }
+  if (lane == 0) {
+    for (int i = 0; i < pre; ++i) issue_x(pre_c[i], i);
+    for (; pre < S && pc.u < units; ++pre) {
+      issue_w(pc, pre);
+      issue_x(pc, pre);
+      pc.advance(p, W, units, ksplit, spu, KS);
+    }
   }
 
   float acc[NMAT][2][NT][4];
-  unsigned long long best = 0ull;  // argmax key (0 < any real key)
-
-  int ti = 0, ks = 0;
-  int tile = gw;
-  int seg = total > 0 ? find_seg(p, tile) : 0;
 #pragma unroll
   for (int mi = 0; mi < NMAT; ++mi)
 #pragma unroll
@@ -253,174 +347,307 @@ __global__ void __launch_bounds__(kGemvWarps * 32)
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[mi][rt][nt][e] = 0.f;
+  unsigned long long best = 0ull;  // argmax key (0 < any real key)
 
-  for (int i = 0; i < total; ++i) {
+  // ldmatrix addressing: lane supplies row ri + 8*(mtx&1) of a 16-row tile
+  // and group 2*jp + (mtx>>1).  With the 128-byte swizzle that group's chunk
+  // sits at ((2*jp + (mtx>>1)) ^ ri) << 4 = (jp << 5) ^ (((mtx>>1) ^ ri) << 4),
+  // because 2*jp and mtx>>1 occupy different bits.
+  const int ri = lane & 7, mtx = lane >> 3;
+  const uint32_t ld_lane = smem_u32(code_base) + (uint32_t)(ri + 8 * (mtx & 1)) * 128;
+  const uint32_t ld_c = (uint32_t)(((mtx >> 1) ^ ri) << 4);
+  const int sb_lane = gid * 8;  // float offset of row gid in a [32][8] scale tile
+
+  for (int i = 0; cc.u < units; ++i) {
     const int slot = i % S;
     if (!mbar_wait_bounded(&bars[slot], (uint32_t)((i / S) & 1))) {
+      // give up on the remaining work of this warp; the CTA-level epilogue
+      // below still runs so no thread is left waiting at a barrier
       if (lane == 0) set_dev_error(p.err, kErrMbarTimeout);
-      return;
+      break;
     }
-    const uint8_t* st = wbase + slot * NMAT * kStageMatBytes;
-    const int gcount = min(8, G - ks * 8);
-    const int gbase = ks * 8;
+    const uint32_t cd = ld_lane + slot * kCode;
+    const uint8_t* rs = rest_base + slot * kRest;
+    const int gbase = cc.ks * 8;
 
-#pragma unroll
-    for (int jp = 0; jp < 4; ++jp) {  // pairs of groups
-      if (2 * jp >= gcount) break;
-      // B fragments (activations) for the two groups of this pair
-      uint4 bh[2][NT], bl[2][NT];
-      float xs0[2][NT], xs1[2][NT];
+    // B fragments (activations) of a pair of groups and their (sum,
+    // correction) pairs.  For one activation row every lane loads column 0:
+    // lanes of the other columns only feed accumulator columns that are
+    // never read, so no predicate is needed.
+    const uint4* xp_st = p.xp + (size_t)(gbase * m) * 8;
+    const float2* xs_st = p.xs + (size_t)gbase * m;
+    auto load_b = [&](int jp, uint4 (&bh)[2][NT], uint4 (&bl)[2][NT], float2 (&x0)[2][NT],
+                      float2 (&x1)[2][NT]) {
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
-        const int g = gbase + 2 * jp + h;
-        const bool gv = (2 * jp + h) < gcount;
+        const int j = 2 * jp + h;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const int c = nt * 8 + gid;
-          if (gv && c < p.m) {
-            const uint4* src = p.xp + xp_index(g, c, tq, 0, p.m);
+          if constexpr (C1) {
+            const uint4* src = xp_st + j * 8 + tq * 2;
             bh[h][nt] = __ldg(src);
             bl[h][nt] = __ldg(src + 1);
+            x0[h][nt] = __ldg(xs_st + j);
+            x1[h][nt] = x0[h][nt];
           } else {
             bh[h][nt] = make_uint4(0, 0, 0, 0);
             bl[h][nt] = make_uint4(0, 0, 0, 0);
+            x0[h][nt] = make_float2(0.f, 0.f);
+            x1[h][nt] = make_float2(0.f, 0.f);
+            const int c = nt * 8 + gid;
+            const int c0 = nt * 8 + 2 * tq;
+            if constexpr (XM > 0) {
+              const uint4* xps = reinterpret_cast<const uint4*>(rs + NMAT * 2048);
+              const float2* xss = reinterpret_cast<const float2*>(rs + NMAT * 2048 + XM * 1024);
+              if (c < m) {
+                bh[h][nt] = xps[xp_index(j, c, tq, 0, m)];
+                bl[h][nt] = xps[xp_index(j, c, tq, 1, m)];
+              }
+              if (c0 < m) x0[h][nt] = xss[j * m + c0];
+              if (c0 + 1 < m) x1[h][nt] = xss[j * m + c0 + 1];
+            } else {
+              if (c < m) {
+                const uint4* src = xp_st + xp_index(j, c, tq, 0, m);
+                bh[h][nt] = __ldg(src);
+                bl[h][nt] = __ldg(src + 1);
+              }
+              if (c0 < m) x0[h][nt] = __ldg(xs_st + j * m + c0);
+              if (c0 + 1 < m) x1[h][nt] = __ldg(xs_st + j * m + c0 + 1);
+            }
           }
-          const int c0 = nt * 8 + 2 * tq;
-          xs0[h][nt] = (gv && c0 < p.m) ? __ldg(p.xs + g * p.m + c0) : 0.f;
-          xs1[h][nt] = (gv && c0 + 1 < p.m) ? __ldg(p.xs + g * p.m + c0 + 1) : 0.f;
         }
       }
+    };
+    // Pairs of groups.  Each pair issues its tensor-core products, then loads
+    // the next pair's activations into the same registers (their latency
+    // overlaps the scale/bias epilogue), then applies scales and biases.
+    // Activations are zero-padded to whole stages of 8 groups.
+    uint4 bh[2][NT], bl[2][NT];
+    float2 xs0[2][NT], xs1[2][NT];
+    load_b(0, bh, bl, xs0, xs1);
+#pragma unroll 1
+    for (int jp = 0; jp < 4; ++jp) {
+      const uint32_t coff = ((uint32_t)jp << 5) ^ ld_c;
+      float d[NMAT][2][2][NT][4];
+      float sx0[2][NT], sx1[2][NT];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          sx0[h][nt] = xs0[h][nt].x;
+          sx1[h][nt] = xs1[h][nt].x;
+        }
 #pragma unroll
       for (int mi = 0; mi < NMAT; ++mi) {
-        const uint8_t* codes = st + mi * kStageMatBytes;
-        const float* ssm = reinterpret_cast<const float*>(codes + 4096);
-        const float* bsm = reinterpret_cast<const float*>(codes + 5120);
 #pragma unroll
         for (int rt = 0; rt < 2; ++rt) {
-          // ldmatrix.x4: (rows 0-7, group 2jp), (rows 8-15, 2jp), (rows 0-7, 2jp+1), (rows 8-15, 2jp+1)
-          const int mtx = lane >> 3, ri = lane & 7;
-          const int row = rt * 16 + ri + 8 * (mtx & 1);
-          const int jj = 2 * jp + (mtx >> 1);
-          const uint32_t addr = smem_u32(codes + row * 128 + ((jj ^ ri) << 4));
+          // (rows 0-7, group 2jp), (rows 8-15, 2jp), (rows 0-7, 2jp+1), (rows 8-15, 2jp+1)
           uint32_t w[4];
-          ldmatrix_x4(w[0], w[1], w[2], w[3], addr);
+          ldmatrix_x4(w[0], w[1], w[2], w[3], cd + mi * 4096 + rt * 2048 + coff);
 #pragma unroll
           for (int h = 0; h < 2; ++h) {
-            if (2 * jp + h >= gcount) break;
             const uint32_t wa = w[2 * h], wb = w[2 * h + 1];
-            const uint32_t a0 = codes_to_bf16x2_biased(wa);
-            const uint32_t a1 = codes_to_bf16x2_biased(wb);
-            const uint32_t a2 = codes_to_bf16x2_biased(wa >> 4);
-            const uint32_t a3 = codes_to_bf16x2_biased(wb >> 4);
-            const uint32_t a4 = codes_to_bf16x2_biased(wa >> 8);
-            const uint32_t a5 = codes_to_bf16x2_biased(wb >> 8);
-            const uint32_t a6 = codes_to_bf16x2_biased(wa >> 12);
-            const uint32_t a7 = codes_to_bf16x2_biased(wb >> 12);
-            const int j = 2 * jp + h;
-            const int r0 = rt * 16 + gid;
-            const float s0 = ssm[r0 * 8 + j], s1 = ssm[(r0 + 8) * 8 + j];
-            const float b0 = fmaf(-128.f, s0, bsm[r0 * 8 + j]);
-            const float b1 = fmaf(-128.f, s1, bsm[(r0 + 8) * 8 + j]);
+            const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+            const uint32_t a0 = codes_lo_f16x2(wa), a1 = codes_lo_f16x2(wb);
+            const uint32_t a2 = codes_hi_f16x2(wa), a3 = codes_hi_f16x2(wb);
+            const uint32_t a4 = codes_lo_f16x2(wa8), a5 = codes_lo_f16x2(wb8);
+            const uint32_t a6 = codes_hi_f16x2(wa8), a7 = codes_hi_f16x2(wb8);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
-              float d[4] = {0.f, 0.f, 0.f, 0.f};
-              mma_bf16_16816(d, a0, a1, a2, a3, bh[h][nt].x, bh[h][nt].y);
-              mma_bf16_16816(d, a0, a1, a2, a3, bl[h][nt].x, bl[h][nt].y);
-              mma_bf16_16816(d, a4, a5, a6, a7, bh[h][nt].z, bh[h][nt].w);
-              mma_bf16_16816(d, a4, a5, a6, a7, bl[h][nt].z, bl[h][nt].w);
+              float* dd = d[mi][rt][h][nt];
+              dd[0] = dd[2] = -xs0[h][nt].y;
+              dd[1] = dd[3] = -xs1[h][nt].y;
+              mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bh[h][nt].x, bh[h][nt].y);
+              mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bl[h][nt].x, bl[h][nt].y);
+              mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bh[h][nt].z, bh[h][nt].w);
+              mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bl[h][nt].z, bl[h][nt].w);
+            }
+          }
+        }
+      }
+      if (jp < 3) load_b(jp + 1, bh, bl, xs0, xs1);
+#pragma unroll
+      for (int mi = 0; mi < NMAT; ++mi) {
+        const float* ssm = reinterpret_cast<const float*>(rs + mi * 2048) + sb_lane + 2 * jp;
+        const float* bsm = ssm + 256;
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt) {
+          const float2 sa = *reinterpret_cast<const float2*>(ssm + rt * 128);
+          const float2 sb = *reinterpret_cast<const float2*>(ssm + rt * 128 + 64);
+          const float2 ba = *reinterpret_cast<const float2*>(bsm + rt * 128);
+          const float2 bb = *reinterpret_cast<const float2*>(bsm + rt * 128 + 64);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float s0 = h ? sa.y : sa.x, s1 = h ? sb.y : sb.x;
+            const float b0 = h ? ba.y : ba.x, b1 = h ? bb.y : bb.x;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const float* dd = d[mi][rt][h][nt];
               float* a = acc[mi][rt][nt];
-              a[0] = fmaf(s0, d[0], fmaf(b0, xs0[h][nt], a[0]));
-              a[1] = fmaf(s0, d[1], fmaf(b0, xs1[h][nt], a[1]));
-              a[2] = fmaf(s1, d[2], fmaf(b1, xs0[h][nt], a[2]));
-              a[3] = fmaf(s1, d[3], fmaf(b1, xs1[h][nt], a[3]));
+              a[0] = fmaf(s0, dd[0], fmaf(b0, sx0[h][nt], a[0]));
+              a[2] = fmaf(s1, dd[2], fmaf(b1, sx0[h][nt], a[2]));
+              if constexpr (!C1) {
+                a[1] = fmaf(s0, dd[1], fmaf(b0, sx1[h][nt], a[1]));
+                a[3] = fmaf(s1, dd[3], fmaf(b1, sx1[h][nt], a[3]));
+              }
             }
           }
         }
       }
     }
     __syncwarp();
-    if (lane == 0 && i + S < total) issue(i + S);
+    if (lane == 0 && pc.u < units) {
+      issue_w(pc, slot);
+      issue_x(pc, slot);
+      pc.advance(p, W, units, ksplit, spu, KS);
+    }
 
-    if (++ks == KS) {
-      // ---------------------------------------------------------- epilogue
-      const GemvSeg& sg = p.seg[seg];
-      const int lt = tile - (seg ? p.seg[seg - 1].tile_end : 0);
-      const int rbase = lt * 32;
-      if constexpr (EPI == kEpiStore) {
+    const int unit = cc.u;
+    const int tile = cc.tile;
+    const int seg = cc.seg;
+    if (!cc.advance(p, W, units, ksplit, spu, KS)) continue;
+
+    // ------------------------------------------------------------ unit done
+    if (ksplit > 1) {
+      // Deterministic split-K: every unit stores its fragment partial; the
+      // last unit of a tile to finish sums them in k order.
+      constexpr int NACC = NMAT * 2 * NT * 4;
+      float4* mine = reinterpret_cast<float4*>(p.part) + ((size_t)unit * 32 + lane) * (NACC / 4);
+      const float* af = &acc[0][0][0][0];
 #pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
+      for (int q = 0; q < NACC / 4; ++q)
+        mine[q] = make_float4(af[4 * q], af[4 * q + 1], af[4 * q + 2], af[4 * q + 3]);
+      __threadfence();
+      __syncwarp();
+      unsigned prev = 0;
+      if (lane == 0) prev = atomicAdd(p.tile_cnt + tile, 1u);
+      prev = __shfl_sync(0xffffffffu, prev, 0);
+      if (prev != (unsigned)ksplit - 1) {
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int row = rbase + rt * 16 + gid + ((e & 2) ? 8 : 0);
-              const int c = nt * 8 + 2 * tq + (e & 1);
-              if (row < sg.n && c < p.m) {
-                const size_t o = (size_t)c * sg.ld + sg.out_col0 + row;
-                float v = acc[0][rt][nt][e];
-                if (sg.res) v += sg.res[o];
-                sg.out[o] = v;
-              }
-            }
-      } else if constexpr (EPI == kEpiSwiglu) {
-        const float scale = sg.w_idx >= 0 ? p.segw[sg.w_idx] : 1.f;
-        const int g_out = (sg.out_col0 + rbase) / kGroup;
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          float part[2] = {0.f, 0.f};
+        for (int mi = 0; mi < NMAT; ++mi)
 #pragma unroll
           for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
-              const int c = nt * 8 + 2 * tq + (e & 1);
-              const float gv = acc[0][rt][nt][e];
-              const float uv = acc[1][rt][nt][e];
-              const float hv = gv / (1.f + __expf(-gv)) * uv * scale;
-              if (c < p.out_m) {
-                float hs;
-                xp_store_elem(p.out_xp, p.out_m, g_out, c, rloc >> 3, rloc & 7, hv, &hs);
-                part[e & 1] += hs;
-                if (sg.out) sg.out[(size_t)c * sg.ld + sg.out_col0 + rbase + rloc] = hv;
-              }
-            }
+            for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float v = part[e];
-            v += __shfl_xor_sync(0xffffffffu, v, 4);
-            v += __shfl_xor_sync(0xffffffffu, v, 8);
-            v += __shfl_xor_sync(0xffffffffu, v, 16);
-            const int c = nt * 8 + 2 * tq + e;
-            if (gid == 0 && c < p.out_m) p.out_xs[g_out * p.out_m + c] = v;
-          }
-        }
-      } else {  // argmax over column 0 (one activation row)
+              for (int e = 0; e < 4; ++e) acc[mi][rt][nt][e] = 0.f;
+        continue;
+      }
+      __threadfence();
+      float* aw = &acc[0][0][0][0];
 #pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
+      for (int q = 0; q < NACC; ++q) aw[q] = 0.f;
+      // k order is fixed (deterministic); loads of four partials are issued
+      // together so their L2 latencies overlap
+      const float4* src0 =
+          reinterpret_cast<const float4*>(p.part) + ((size_t)tile * ksplit * 32 + lane) * (NACC / 4);
+      const size_t pstride = (size_t)32 * (NACC / 4);
+      int s2 = 0;
+      for (; s2 + 4 <= ksplit; s2 += 4) {
+        float4 v[4][NACC / 4];
 #pragma unroll
-          for (int e = 0; e < 4; e += 2) {
-            const int row = rbase + rt * 16 + gid + ((e & 2) ? 8 : 0);
-            if (tq == 0 && row < sg.n) {
-              const float v = acc[0][rt][0][e];
-              if (p.logits) p.logits[row] = v;
-              const unsigned long long key = argmax_key(v, row);
-              best = key > best ? key : best;
-            }
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int q = 0; q < NACC / 4; ++q) v[u][q] = __ldcg(src0 + (s2 + u) * pstride + q);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+#pragma unroll
+          for (int q = 0; q < NACC / 4; ++q) {
+            aw[4 * q] += v[u][q].x;
+            aw[4 * q + 1] += v[u][q].y;
+            aw[4 * q + 2] += v[u][q].z;
+            aw[4 * q + 3] += v[u][q].w;
           }
       }
+      for (; s2 < ksplit; ++s2) {
 #pragma unroll
-      for (int mi = 0; mi < NMAT; ++mi)
+        for (int q = 0; q < NACC / 4; ++q) {
+          const float4 v = __ldcg(src0 + s2 * pstride + q);
+          aw[4 * q] += v.x;
+          aw[4 * q + 1] += v.y;
+          aw[4 * q + 2] += v.z;
+          aw[4 * q + 3] += v.w;
+        }
+      }
+      if (lane == 0) p.tile_cnt[tile] = 0u;  // leave the counter cleared
+    }
+
+    // ---------------------------------------------------------- epilogue
+    const GemvSeg& sg = p.seg[seg];
+    const int lt = tile - (seg ? p.seg[seg - 1].tile_end : 0);
+    const int rbase = lt * 32;
+    if constexpr (EPI == kEpiStore) {
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int row = rbase + rt * 16 + gid + ((e & 2) ? 8 : 0);
+            const int c = nt * 8 + 2 * tq + (e & 1);
+            if (row < sg.n && c < m) {
+              const size_t o = (size_t)c * sg.ld + sg.out_col0 + row;
+              float v = acc[0][rt][nt][e];
+              if (sg.res) v += sg.res[o];
+              sg.out[o] = v;
+            }
+          }
+    } else if constexpr (EPI == kEpiSwiglu) {
+      const float scale = sg.w_idx >= 0 ? p.segw[sg.w_idx] : 1.f;
+      const int g_out = (sg.out_col0 + rbase) / kGroup;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
+          for (int e = 0; e < 4; ++e) {
+            const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
+            const int c = nt * 8 + 2 * tq + (e & 1);
+            const float gv = acc[0][rt][nt][e];
+            const float uv = acc[1][rt][nt][e];
+            const float hv = gv / (1.f + __expf(-gv)) * uv * scale;
+            if (c < p.out_m) {
+              const float2 hs = xp_store_elem(p.out_xp, p.out_m, g_out, c, rloc >> 3, rloc & 7, hv);
+              part[e & 1].x += hs.x;
+              part[e & 1].y += hs.y;
+              if (sg.out) sg.out[(size_t)c * sg.ld + sg.out_col0 + rbase + rloc] = hv;
+            }
+          }
 #pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mi][rt][nt][e] = 0.f;
-      ks = 0;
-      ++ti;
-      tile += W;
-      if (ti < my_tiles) seg = find_seg(p, tile);
+        for (int e = 0; e < 2; ++e) {
+          float2 v = part[e];
+#pragma unroll
+          for (int o = 4; o < 32; o <<= 1) {
+            v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+            v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+          }
+          const int c = nt * 8 + 2 * tq + e;
+          if (gid == 0 && c < p.out_m) p.out_xs[g_out * p.out_m + c] = v;
+        }
+      }
+    } else {  // argmax over column 0 (one activation row)
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const int row = rbase + rt * 16 + gid + ((e & 2) ? 8 : 0);
+          if (tq == 0 && row < sg.n) {
+            const float v = acc[0][rt][0][e];
+            if (p.logits) p.logits[row] = v;
+            const unsigned long long key = argmax_key(v, row);
+            best = key > best ? key : best;
+          }
+        }
     }
+#pragma unroll
+    for (int mi = 0; mi < NMAT; ++mi)
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) acc[mi][rt][nt][e] = 0.f;
   }
 
   if constexpr (EPI == kEpiArgmax) {

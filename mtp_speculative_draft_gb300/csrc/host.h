@@ -28,10 +28,21 @@ mtp_status encode_qmat(QMat* out, const mtp_affine4& w, const char* name);
 // 16-byte aligned for the tensor maps.
 mtp_status check_affine(const mtp_affine4* w, int n, int k, const char* name, bool need_tma);
 
-// Launch helpers (programmatic dependent launch on `stream`).
-cudaError_t launch_gemv(int nmat, int nt, int epi, const GemvParams& p, int tiles,
-                        cudaStream_t stream);
-cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float* xs, cudaStream_t st);
+// Workspace regions a GEMV launch may use for split-K partial sums.
+struct GemvScratch {
+  float* part;       // partial fragments
+  size_t part_bytes;
+  unsigned* cnt;     // per-tile completion counters (cleared)
+  int cnt_len;
+};
+size_t gemv_scratch_part_bytes();
+constexpr int kGemvCounters = 4096;
+
+// Launch helpers (programmatic dependent launch on `stream`).  Fills in the
+// split-K plan of `p` (ksplit, spu, part, tile_cnt) from the scratch given.
+cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
+                        const GemvScratch& scratch, cudaStream_t stream);
+cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float2* xs, cudaStream_t st);
 cudaError_t launch_gemv_simple(const float* x, int m, int K, const mtp_affine4& w, float* y,
                                cudaStream_t st);
 
@@ -51,7 +62,7 @@ struct NormSeg {
 
 // Normalises m rows (up to two segments concatenated along K) and writes
 // the packed activations of the concatenation (xp may be null).
-cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, float* xs,
+cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, float2* xs,
                              int* err, cudaStream_t st);
 
 struct AttnParams {
@@ -62,10 +73,14 @@ struct AttnParams {
   int L, cap, m;
   float* out;          // [m][nh*dv] fp32 (may be null)
   uint4* out_xp;       // packed output for the next projection (may be null)
-  float* out_xs;
+  float2* out_xs;
   float* part;         // partials
   unsigned* counters;  // [nkv]
   int nsplit;
+  // 1: stream cached rows before waiting on the previous kernel.  Only valid
+  // when that kernel signals its dependents after its own wait (so every
+  // earlier kernel, including the step that wrote those rows, has finished).
+  int prefetch_before_wait;
   int* err;
 };
 int attn_splits(int nkv, int keys);
@@ -85,7 +100,7 @@ struct RouterParams {
   int* sel;              // [top_k]
   float* weight;         // [top_k + 1]
   uint4* xp;             // packed normalised row for the expert projections
-  float* xs;
+  float2* xs;
 };
 cudaError_t launch_router(const RouterParams& r, cudaStream_t st);
 

@@ -47,7 +47,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterPara
   if (blockIdx.x == 0 && r.xp) {
     for (int o0 = 0; o0 < H / 8; o0 += kRouterThreads) {
       const int o = o0 + tid;
-      float sum = 0.f;
+      float2 sum = make_float2(0.f, 0.f);
       if (o < H / 8) {
         float v[8];
 #pragma unroll
@@ -58,8 +58,10 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterPara
         r.xp[xp_index(g, 0, t, 0, 1)] = hi;
         r.xp[xp_index(g, 0, t, 1, 1)] = lo;
       }
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 1);
+      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
+      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
+      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 2);
       if (o < H / 8 && (o & 3) == 0) r.xs[o / 4] = sum;
     }
   }

@@ -13,7 +13,7 @@ struct NormPackArgs {
   int nseg;
   int m;
   uint4* xp;
-  float* xs;
+  float2* xs;
   int* err;
 };
 
@@ -44,8 +44,18 @@ __device__ __forceinline__ const float* seg_row(const NormSeg& s, int c, int* er
 
 __global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackArgs a) {
   __shared__ float red[kNormThreads / 32];
+#ifndef MTP_NORM_EARLY_TRIGGER
+#define MTP_NORM_EARLY_TRIGGER 0
+#endif
+#if MTP_NORM_EARLY_TRIGGER
+  // Lets the projection that follows launch (and start streaming weights)
+  // right away; measured slower on the draft step, so off by default.
+  pdl_launch_dependents();
+  pdl_wait();
+#else
   pdl_wait();
   pdl_launch_dependents();
+#endif
   const int c = blockIdx.x;
   float inv[2] = {1.f, 1.f};
   for (int si = 0; si < a.nseg; ++si) {
@@ -70,7 +80,7 @@ __global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackA
   const int octets = K / 8;
   for (int o0 = 0; o0 < octets; o0 += kNormThreads) {
     const int o = o0 + threadIdx.x;
-    float sum = 0.f;
+    float2 sum = make_float2(0.f, 0.f);
     if (o < octets) {
       const int k = o * 8;
       const int si = (a.nseg > 1 && k >= a.seg[0].dim) ? 1 : 0;
@@ -109,14 +119,16 @@ __global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackA
     }
     if (a.xp) {
       // octets o..o+3 of one group sit in adjacent lanes (kNormThreads % 4 == 0)
-      sum += __shfl_xor_sync(0xffffffffu, sum, 1);
-      sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 1);
+      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
+      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
+      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 2);
       if (o < octets && (o & 3) == 0) a.xs[(o / 4) * a.m + c] = sum;
     }
   }
 }
 
-cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, float* xs,
+cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, float2* xs,
                              int* err, cudaStream_t st) {
   NormPackArgs a = {};
   a.seg[0] = segs[0];
