@@ -225,7 +225,7 @@ mtp_status rmsnorm_residual(const float* d_a, const float* d_delta, const float*
   if (rows <= 0 || rows > 65535 || dim <= 0 || dim % 32)
     return fail(MTP_ERR_UNSUPPORTED, "rmsnorm_residual: rows in 1..65535, dim a multiple of 32");
   if (!(eps >= 0.f)) return fail(MTP_ERR_INVALID_ARG, "rmsnorm_residual: eps must be >= 0");
-  if (!aligned16(d_a) || (d_delta && !aligned16(d_delta)) || !aligned16(d_out_norm) ||
+  if (!aligned16(d_a) || !aligned16(d_w) || (d_delta && !aligned16(d_delta)) || !aligned16(d_out_norm) ||
       (d_out_sum && !aligned16(d_out_sum)))
     return fail(MTP_ERR_INVALID_ARG, "rmsnorm_residual: pointers must be 16-byte aligned");
   if (d_out_norm == d_a || d_out_norm == d_delta)
@@ -387,7 +387,7 @@ mtp_status lmhead_argmax(const float* d_y, const float* d_norm_w, float eps,
   if (!d_y || !d_token || !d_value) return fail(MTP_ERR_INVALID_ARG, "lmhead_argmax: null pointer");
   mtp_status s = check_affine(W, -1, -1, "lm_head", true);
   if (s != MTP_OK) return s;
-  if (!aligned16(d_y) || (d_logits && !aligned16(d_logits)) ||
+  if (!aligned16(d_y) || (d_norm_w && !aligned16(d_norm_w)) || (d_logits && !aligned16(d_logits)) ||
       (d_y_normed && !aligned16(d_y_normed)))
     return fail(MTP_ERR_INVALID_ARG, "lmhead_argmax: pointers must be 16-byte aligned");
   if (!(eps >= 0.f)) return fail(MTP_ERR_INVALID_ARG, "lmhead_argmax: eps must be >= 0");
@@ -625,7 +625,8 @@ static mtp_status check_layer(const mtp_layer_desc* L, int m) {
   if (!(L->eps >= 0.f)) return fail(MTP_ERR_INVALID_ARG, "layer: eps must be >= 0");
   const float* norms[] = {L->enorm, L->hnorm, L->attn_norm, L->post_norm, L->final_norm};
   for (const float* p : norms)
-    if (!p) return fail(MTP_ERR_INVALID_ARG, "layer: null norm weight");
+    if (!p || !aligned16(p))
+      return fail(MTP_ERR_INVALID_ARG, "layer: norm weights must be non-null and 16-byte aligned");
   const int qrows = g.n_heads * g.head_dim_qk * (g.gated_q ? 2 : 1);
   if ((s = check_affine(&L->eh_proj, H, 2 * H, "eh_proj", true)) != MTP_OK) return s;
   if ((s = check_affine(&L->wq, qrows, H, "wq", true)) != MTP_OK) return s;

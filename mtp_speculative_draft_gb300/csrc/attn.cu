@@ -37,8 +37,16 @@ constexpr int kPadQ = kQpt * (kAttnThreads / 32);
 struct AttnLayout {
   int stages;
   int kstride;       // padded K row (floats)
-  size_t stage_bytes, q_off, p_off, stat_off, newk_off, newv_off, bar_off, total;
+  size_t stage_bytes, q_off, p_off, red_off, stat_off, newk_off, newv_off, bar_off, total;
 };
+
+// Slices of the head dimension for the logits: a power of two <= 16 that
+// divides dqk/4, with at most 4 float4 per slice.
+__host__ __device__ inline int attn_nparts(int dqk) {
+  int n = 16;
+  while (n > 1 && ((dqk / 4) % n) != 0) n >>= 1;
+  return n;
+}
 
 // Partials: (M, l) pairs [nkv][nsplit][QG][2], then outputs [nkv][nsplit][QG][dv]
 // starting on a 16-byte boundary.
@@ -50,13 +58,15 @@ __host__ __device__ inline AttnLayout attn_layout(int dqk, int dv, int QG, int m
   AttnLayout L;
   L.kstride = dqk + 4;
   L.stage_bytes = (size_t)kTileKeys * L.kstride * 4 + (size_t)kTileKeys * dv * 4;
-  const size_t fixed = (size_t)QG * dqk * 4 + (size_t)kPadQ * kTileKeys * 4 + 3 * kPadQ * 4 +
+  const size_t red_bytes = (size_t)QG * attn_nparts(dqk) * kTileKeys * 4;
+  const size_t fixed = (size_t)QG * dqk * 4 + (size_t)kPadQ * kTileKeys * 4 + red_bytes + 3 * kPadQ * 4 +
                        (size_t)m * (dqk + dv) * 4 + 8 * 8 + 256;
   int s = (int)((kAttnSmemMax - fixed) / L.stage_bytes);
   L.stages = s > 3 ? 3 : (s < 1 ? 1 : s);
   L.q_off = L.stages * L.stage_bytes;
   L.p_off = L.q_off + (size_t)QG * dqk * 4;
-  L.stat_off = L.p_off + (size_t)kPadQ * kTileKeys * 4;
+  L.red_off = L.p_off + (size_t)kPadQ * kTileKeys * 4;
+  L.stat_off = L.red_off + red_bytes;
   L.newk_off = L.stat_off + 3 * kPadQ * 4;
   L.newv_off = L.newk_off + (size_t)m * dqk * 4;
   L.bar_off = (L.newv_off + (size_t)m * dv * 4 + 15) / 16 * 16;
@@ -100,24 +110,44 @@ __device__ __forceinline__ void warp_norm_rope(float* v, int d, const float* nw,
 template <int QPT>
 __device__ __forceinline__ void attend_tile(const AttnParams& a, const float* Ks, int kstride,
                                            const float* Vs, int nk, int key0, const float* qs,
-                                           float* ps, float* Ms, float* ls, float* als,
-                                           float (&oacc)[QPT], int QG, int G) {
+                                           float* ps, float* red, float* Ms, float* ls,
+                                           float* als, float (&oacc)[QPT], int QG, int G) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int dqk = a.dqk, dv = a.dv;
   const int kq4 = dqk / 4;
-  for (int pi = tid; pi < QG * kTileKeys; pi += kAttnThreads) {
-    const int jj = pi & (kTileKeys - 1), qi = pi / kTileKeys;
+  // logits: lane = key, warp = slice of the head dimension.  Each key
+  // element is read from shared memory once (into registers); the query
+  // slice is a warp-wide broadcast.  Slice partials meet in `red`.
+  const int nparts = attn_nparts(dqk);
+  const int pc4 = kq4 / nparts;  // float4 per slice
+  if (warp < nparts) {
+    const float4* kv = reinterpret_cast<const float4*>(Ks + lane * kstride) + warp * pc4;
+    // rows past nk are not read (the new-key tile holds only m rows)
+    float4 kr[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      kr[i] = (i < pc4 && lane < nk) ? kv[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int qi = 0; qi < QG; ++qi) {
+      const float4* qv = reinterpret_cast<const float4*>(qs + qi * dqk) + warp * pc4;
+      float acc = 0.f;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i < pc4) {
+          const float4 x = qv[i];
+          acc = fmaf(x.x, kr[i].x, fmaf(x.y, kr[i].y, fmaf(x.z, kr[i].z, fmaf(x.w, kr[i].w, acc))));
+        }
+      }
+      red[(qi * nparts + warp) * kTileKeys + lane] = acc;
+    }
+  }
+  __syncthreads();
+  for (int idx = tid; idx < QG * kTileKeys; idx += kAttnThreads) {
+    const int jj = idx & (kTileKeys - 1), qi = idx / kTileKeys;
     const int j = key0 + jj, p = a.L + qi / G;
     float l = kNegBig;
     if (jj < nk && j <= p && (a.window <= 0 || j > p - a.window)) {
-      const float4* qv = reinterpret_cast<const float4*>(qs + qi * dqk);
-      const float4* kv = reinterpret_cast<const float4*>(Ks + jj * kstride);
-      float acc = 0.f;
-      for (int d4 = 0; d4 < kq4; ++d4) {
-        const float4 x = qv[d4], y = kv[d4];
-        acc = fmaf(x.x, y.x, fmaf(x.y, y.y, fmaf(x.z, y.z, fmaf(x.w, y.w, acc))));
-      }
-      l = acc;
+      l = 0.f;
+      for (int pt = 0; pt < nparts; ++pt) l += red[(qi * nparts + pt) * kTileKeys + jj];
     }
     ps[qi * kTileKeys + jj] = l;
   }
@@ -143,7 +173,18 @@ __device__ __forceinline__ void attend_tile(const AttnParams& a, const float* Ks
     // rows past QG read zero probabilities and rescale factors (padded)
 #pragma unroll
     for (int k = 0; k < QPT; ++k) oacc[k] *= als[q0 + k * nsl];
-    for (int jj = 0; jj < nk; ++jj) {
+    // keys four at a time: independent loads ahead of their FMAs
+    int jj = 0;
+    for (; jj + 4 <= nk; jj += 4) {
+      const float v0 = Vs[jj * dv + d], v1 = Vs[(jj + 1) * dv + d];
+      const float v2 = Vs[(jj + 2) * dv + d], v3 = Vs[(jj + 3) * dv + d];
+#pragma unroll
+      for (int k = 0; k < QPT; ++k) {
+        const float4 pr = *reinterpret_cast<const float4*>(ps + (q0 + k * nsl) * kTileKeys + jj);
+        oacc[k] = fmaf(pr.x, v0, fmaf(pr.y, v1, fmaf(pr.z, v2, fmaf(pr.w, v3, oacc[k]))));
+      }
+    }
+    for (; jj < nk; ++jj) {
       const float v = Vs[jj * dv + d];
 #pragma unroll
       for (int k = 0; k < QPT; ++k)
@@ -167,6 +208,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
   const int S = Ly.stages;
   float* qs = reinterpret_cast<float*>(smraw + Ly.q_off);
   float* ps = reinterpret_cast<float*>(smraw + Ly.p_off);
+  float* red = reinterpret_cast<float*>(smraw + Ly.red_off);
   float* Ms = reinterpret_cast<float*>(smraw + Ly.stat_off);
   float* ls = Ms + kPadQ;
   float* als = ls + kPadQ;
@@ -267,12 +309,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
     const float* Ks = reinterpret_cast<const float*>(smraw + (size_t)slot * Ly.stage_bytes);
     const float* Vs = Ks + kTileKeys * Ly.kstride;
     const int key0 = kbeg + (t_begin + t) * kTileKeys;
-    attend_tile<QPT>(a, Ks, Ly.kstride, Vs, min(kTileKeys, L - key0), key0, qs, ps, Ms, ls, als,
-                     oacc, QG, G);
+    attend_tile<QPT>(a, Ks, Ly.kstride, Vs, min(kTileKeys, L - key0), key0, qs, ps, red, Ms, ls,
+                     als, oacc, QG, G);
     if (warp == 0 && t + S < my_tiles) issue(t + S, slot);
   }
   if (has_new)
-    attend_tile<QPT>(a, newk, dqk, newv, a.m, L, qs, ps, Ms, ls, als, oacc, QG, G);
+    attend_tile<QPT>(a, newk, dqk, newv, a.m, L, qs, ps, red, Ms, ls, als, oacc, QG, G);
 
   // ---- partial of this split: (M, l) pairs and unnormalised outputs
   const size_t pidx = (size_t)(kvh * a.nsplit + split) * QG;
@@ -305,9 +347,15 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
   // ---- merge (last CTA of this KV head); the stage ring is free now
   const int ns = a.nsplit;
   float* wsm = reinterpret_cast<float*>(smraw);        // [ns][QG] split weights
-  float* fin = wsm + ns * QG;                          // [QG][dv]
+  float* lsm = wsm + ns * QG;                          // [ns][QG] split denominators
+  float* fin = lsm + ns * QG;                          // [QG][dv]
   const size_t base = (size_t)kvh * ns * QG;
-  for (int i = tid; i < ns * QG; i += kAttnThreads) wsm[i] = __ldcg(a.part + (base + i) * 2);
+  // all (M, l) pairs in one parallel pass, so no loop below waits on memory
+  for (int i = tid; i < ns * QG; i += kAttnThreads) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part) + base + i);
+    wsm[i] = ml.x;
+    lsm[i] = ml.y;
+  }
   __syncthreads();
   if (tid < QG) {
     const int h = kvh * G + tid % G;
@@ -315,8 +363,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
     float M = sinkl2;
     for (int s = 0; s < ns; ++s) M = fmaxf(M, wsm[s * QG + tid]);
     float den = a.sinks ? exp2f(sinkl2 - M) : 0.f;
-    for (int s = 0; s < ns; ++s)
-      den += exp2f(wsm[s * QG + tid] - M) * __ldcg(a.part + (base + s * QG + tid) * 2 + 1);
+    for (int s = 0; s < ns; ++s) den += exp2f(wsm[s * QG + tid] - M) * lsm[s * QG + tid];
     const float inv = den > 0.f ? 1.f / den : 0.f;
     for (int s = 0; s < ns; ++s) wsm[s * QG + tid] = exp2f(wsm[s * QG + tid] - M) * inv;
   }
@@ -441,7 +488,7 @@ cudaError_t launch_attn(const AttnParams& a, cudaStream_t st) {
   const int QG = (a.nh / a.nkv) * a.m;
   const AttnLayout Ly = attn_layout(a.dqk, a.dv, QG, a.m);
   // the merge reuses the stage ring: split weights and the finished rows
-  const size_t merge = (size_t)a.nsplit * QG * 4 + (size_t)QG * a.dv * 4;
+  const size_t merge = (size_t)a.nsplit * QG * 8 + (size_t)QG * a.dv * 4;
   const size_t smem = Ly.total > merge ? Ly.total : merge;
   if (smem > (size_t)kAttnSmemMax + 1024) return cudaErrorInvalidValue;
   const int nsl = kAttnThreads / a.dv;

@@ -131,6 +131,13 @@ __device__ __forceinline__ uint32_t codes_lo_f16x2(uint32_t w) {
 __device__ __forceinline__ uint32_t codes_hi_f16x2(uint32_t w) {
   return (w & 0x00F000F0u) | 0x64006400u;
 }
+// Removes the 1024 bias of both halves (exact: 1024 + c and 1024 + 16c are
+// representable, so the difference is the exact code or 16 * code).
+__device__ __forceinline__ uint32_t unbias_f16x2(uint32_t v) {
+  uint32_t r;
+  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64006400u));
+  return r;
+}
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -91,15 +91,16 @@ static cudaLaunchAttribute pdl_attr() {
 struct Plan {
   int ksplit, spu, units;
 };
-static Plan plan_split(int tiles, int KS, int warps_cap, int nacc, const GemvScratch& sc) {
-  Plan best = {1, KS, tiles};
+static Plan plan_split(int tiles, int KS, int warps_cap, int nacc, int um,
+                       const GemvScratch& sc) {
+  Plan best = {0, 0, 0};
   double best_cost = 1e30;
   for (int spu = KS; spu >= 1; --spu) {
     const int ksplit = (KS + spu - 1) / spu;
     if (ksplit > 1 && spu * (ksplit - 1) >= KS) continue;  // same split as a larger spu
-    const long long units = (long long)tiles * ksplit;
-    if (ksplit > 1) {
-      if (units > warps_cap) continue;
+    const long long units = (long long)tiles * um * ksplit;
+    if (ksplit > 1 || um > 1) {
+      if (ksplit > 1 && units > warps_cap) continue;
       if (tiles > sc.cnt_len) continue;
       if ((size_t)units * 32 * nacc * sizeof(float) > sc.part_bytes) continue;
     }
@@ -127,11 +128,11 @@ size_t gemv_scratch_part_bytes() {
 #define MTP_GEMV_STAGE_X1 0
 #endif
 
-template <int NMAT, int NT, int EPI, int XM, bool C1>
+template <int NMAT, int NT, int EPI, int XM, bool C1, bool PAIRED = false>
 static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
                                  cudaStream_t st) {
   constexpr int S = MTP_GEMV_STAGES;
-  auto kern = gemv_tc_kernel<NMAT, NT, EPI, S, XM, C1>;
+  auto kern = gemv_tc_kernel<NMAT, NT, EPI, S, XM, C1, PAIRED>;
   const int smem = gemv_smem_bytes<NMAT, S, XM>();
   static thread_local int configured_dev = -1;
   static thread_local int ctas_per_sm = 1;
@@ -148,7 +149,8 @@ static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
   }
   const int warps_cap = sm_count() * ctas_per_sm * kGemvWarps;
   const int KS = (p.K / kGroup + 7) / 8;
-  const Plan pl = plan_split(tiles, KS, warps_cap, NMAT * 2 * NT * 4, sc);
+  const Plan pl = plan_split(tiles, KS, warps_cap, NMAT * 2 * NT * 4, PAIRED ? 2 : 1, sc);
+  if (pl.ksplit == 0) return cudaErrorInvalidValue;  // scratch too small for the split
   p.ksplit = pl.ksplit;
   p.spu = pl.spu;
   p.part = sc.part;
@@ -184,11 +186,12 @@ cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
     if (m <= 4) return launch_gemv_t<1, 1, kEpiStore, 4, false>(p, tiles, sc, st);
     return launch_gemv_t<1, 1, kEpiStore, 0, false>(p, tiles, sc, st);
   }
+  // SwiGLU: gate (slot mat) and up (slot mat + 1) tiles are separate units
   if (epi != kEpiSwiglu) return cudaErrorInvalidValue;
-  if (nt == 2) return launch_gemv_t<2, 2, kEpiSwiglu, 0, false>(p, tiles, sc, st);
-  if (c1) return launch_gemv_t<2, 1, kEpiSwiglu, X1, true>(p, tiles, sc, st);
-  if (m <= 4) return launch_gemv_t<2, 1, kEpiSwiglu, 4, false>(p, tiles, sc, st);
-  return launch_gemv_t<2, 1, kEpiSwiglu, 0, false>(p, tiles, sc, st);
+  if (nt == 2) return launch_gemv_t<1, 2, kEpiSwiglu, 0, false, true>(p, tiles, sc, st);
+  if (c1) return launch_gemv_t<1, 1, kEpiSwiglu, X1, true, true>(p, tiles, sc, st);
+  if (m <= 4) return launch_gemv_t<1, 1, kEpiSwiglu, 4, false, true>(p, tiles, sc, st);
+  return launch_gemv_t<1, 1, kEpiSwiglu, 0, false, true>(p, tiles, sc, st);
 }
 
 cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float2* xs, cudaStream_t st) {

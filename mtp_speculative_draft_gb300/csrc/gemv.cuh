@@ -14,11 +14,12 @@
 // Codes become f16x2 registers with one LOP3 each and no shift for two of
 // the four nibble pairs of a word: nibbles at bits 0-3/16-19 give 1024 + c,
 // nibbles at bits 4-7/20-23 give 1024 + 16c (both exact in f16).  The
-// activations are split into f16 hi + lo parts (about 22 bits), the slots
-// that meet a 16c code carry x/16, and the products run on the tensor pipe
-// with f32 accumulation.  The accumulator starts at -1024 * (sum of the
-// represented activations) so it ends at sum(code * x); the per-group scale
-// and bias are applied in f32 after each group:  y += s * D + b * sum(x).
+// 1024 bias is then removed with one f16x2 subtraction (exact), so the
+// tensor pipe accumulates sum(code * x) directly.  The activations are split
+// into f16 hi + lo parts (about 22 bits), the slots that meet a 16c code
+// carry x/16, and the products run on the tensor pipe with f32
+// accumulation.  The per-group scale and bias are applied in f32 after each
+// group:  y += s * D + b * sum(x).
 // Activations arrive pre-packed ("xpack") in the B-fragment order with the
 // per-group sums precomputed by the producer kernel.
 #pragma once
@@ -196,27 +197,30 @@ __device__ __forceinline__ int find_seg(const GemvParams& p, int tile) {
 // segment, matrix slot and first weight row of the unit are resolved once
 // when the unit starts, so advancing by a stage costs a compare.
 struct Cursor {
-  int u, ks, ke, tile, seg, mat, row;
+  int u, ks, ke, tile, seg, mat, row, mi;
+  // um = 2 when a tile's gate and up matrices are separate units (SwiGLU)
   __device__ __forceinline__ void start(const GemvParams& p, int u0, int units, int ksplit,
-                                        int spu, int KS) {
+                                        int spu, int KS, int um = 1) {
     u = u0;
     if (u < units) {
-      tile = u / ksplit;
-      const int kc = u - tile * ksplit;
+      tile = u / (um * ksplit);
+      const int rem = u - tile * (um * ksplit);
+      mi = rem / ksplit;
+      const int kc = rem - mi * ksplit;
       ks = kc * spu;
       ke = min(KS, ks + spu);
       seg = find_seg(p, tile);
       const GemvSeg& sg = p.seg[seg];
       const int lt = tile - (seg ? p.seg[seg - 1].tile_end : 0);
-      mat = sg.mat;
+      mat = sg.mat + mi;
       row = (sg.sel_idx >= 0 ? p.rowsel[sg.sel_idx] * sg.row_mult : 0) + lt * 32;
     }
   }
   // returns true when the unit just finished
   __device__ __forceinline__ bool advance(const GemvParams& p, int W, int units, int ksplit,
-                                          int spu, int KS) {
+                                          int spu, int KS, int um = 1) {
     if (++ks < ke) return false;
-    start(p, u + W, units, ksplit, spu, KS);
+    start(p, u + W, units, ksplit, spu, KS, um);
     return true;
   }
   // weight coordinates of the current stage
@@ -245,9 +249,13 @@ struct Cursor {
   }
 };
 
-template <int NMAT, int NT, int EPI, int S, int XM, bool C1>
+template <int NMAT, int NT, int EPI, int S, int XM, bool C1, bool PAIRED = false>
 __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 2)
     gemv_tc_kernel(const __grid_constant__ GemvParams p) {
+  // PAIRED: the SwiGLU gate and up matrices of a tile are separate work
+  // units (one matrix in flight per warp); their partial sums meet in the
+  // split-K reduction.
+  constexpr int UM = PAIRED ? 2 : 1;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of each codes tile is required by the 128B swizzle.
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -271,7 +279,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
   const int W = gridDim.x * kGemvWarps;
   const int gw = warp * gridDim.x + blockIdx.x;
   const int total_tiles = p.seg[p.nseg - 1].tile_end;
-  const int units = total_tiles * ksplit;
+  const int units = total_tiles * UM * ksplit;
 
   if (lane == 0) {
     for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
@@ -313,20 +321,20 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
   int pre = 0;
   Cursor pre_c[S];
   if (!p.rowsel_after_wait) {
-    pc.start(p, gw, units, ksplit, spu, KS);
+    pc.start(p, gw, units, ksplit, spu, KS, UM);
     cc = pc;
     if (lane == 0) {
       for (; pre < S && pc.u < units; ++pre) {
         pre_c[pre] = pc;
         issue_w(pc, pre);
-        pc.advance(p, W, units, ksplit, spu, KS);
+        pc.advance(p, W, units, ksplit, spu, KS, UM);
       }
     }
   }
   pdl_wait();
   pdl_launch_dependents();
   if (p.rowsel_after_wait) {
-    pc.start(p, gw, units, ksplit, spu, KS);
+    pc.start(p, gw, units, ksplit, spu, KS, UM);
     cc = pc;
   }
   if (lane == 0) {
@@ -334,7 +342,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     for (; pre < S && pc.u < units; ++pre) {
       issue_w(pc, pre);
       issue_x(pc, pre);
-      pc.advance(p, W, units, ksplit, spu, KS);
+      pc.advance(p, W, units, ksplit, spu, KS, UM);
     }
   }
 
@@ -358,6 +366,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
   const uint32_t ld_c = (uint32_t)(((mtx >> 1) ^ ri) << 4);
   const int sb_lane = gid * 8;  // float offset of row gid in a [32][8] scale tile
 
+  uint4 bh[2][NT], bl[2][NT];      // activation fragments of the next pair of groups
+  float2 xs0[2][NT], xs1[2][NT];
+  bool b_ready = false;
   for (int i = 0; cc.u < units; ++i) {
     const int slot = i % S;
     if (!mbar_wait_bounded(&bars[slot], (uint32_t)((i / S) & 1))) {
@@ -374,10 +385,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     // correction) pairs.  For one activation row every lane loads column 0:
     // lanes of the other columns only feed accumulator columns that are
     // never read, so no predicate is needed.
-    const uint4* xp_st = p.xp + (size_t)(gbase * m) * 8;
-    const float2* xs_st = p.xs + (size_t)gbase * m;
-    auto load_b = [&](int jp, uint4 (&bh)[2][NT], uint4 (&bl)[2][NT], float2 (&x0)[2][NT],
-                      float2 (&x1)[2][NT]) {
+    auto load_b_at = [&](int gb, int jp, uint4 (&bh)[2][NT], uint4 (&bl)[2][NT],
+                         float2 (&x0)[2][NT], float2 (&x1)[2][NT]) {
+      const uint4* xp_st = p.xp + (size_t)(gb * m) * 8;
+      const float2* xs_st = p.xs + (size_t)gb * m;
 #pragma unroll
       for (int h = 0; h < 2; ++h) {
         const int j = 2 * jp + h;
@@ -418,13 +429,17 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
         }
       }
     };
+    auto load_b = [&](int jp, uint4 (&bh)[2][NT], uint4 (&bl)[2][NT], float2 (&x0)[2][NT],
+                      float2 (&x1)[2][NT]) { load_b_at(gbase, jp, bh, bl, x0, x1); };
     // Pairs of groups.  Each pair issues its tensor-core products, then loads
     // the next pair's activations into the same registers (their latency
-    // overlaps the scale/bias epilogue), then applies scales and biases.
-    // Activations are zero-padded to whole stages of 8 groups.
-    uint4 bh[2][NT], bl[2][NT];
-    float2 xs0[2][NT], xs1[2][NT];
-    load_b(0, bh, bl, xs0, xs1);
+    // overlaps the scale/bias epilogue), then applies scales and biases.  The
+    // last pair of a stage loads the first pair of the next stage when it
+    // continues the same unit.  Activations are zero-padded to whole stages
+    // of 8 groups.
+    if (!b_ready) load_b(0, bh, bl, xs0, xs1);
+    // (staged activations live in the stage's own buffer: no early load then)
+    const bool next_same_unit = XM == 0 && cc.ks + 1 < cc.ke;
 #pragma unroll 1
     for (int jp = 0; jp < 4; ++jp) {
       const uint32_t coff = ((uint32_t)jp << 5) ^ ld_c;
@@ -448,15 +463,20 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
           for (int h = 0; h < 2; ++h) {
             const uint32_t wa = w[2 * h], wb = w[2 * h + 1];
             const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-            const uint32_t a0 = codes_lo_f16x2(wa), a1 = codes_lo_f16x2(wb);
-            const uint32_t a2 = codes_hi_f16x2(wa), a3 = codes_hi_f16x2(wb);
-            const uint32_t a4 = codes_lo_f16x2(wa8), a5 = codes_lo_f16x2(wb8);
-            const uint32_t a6 = codes_hi_f16x2(wa8), a7 = codes_hi_f16x2(wb8);
+            // exact codes (and 16 * codes) as f16: the accumulator only ever
+            // holds sums of code * x, so its rounding stays at that scale
+            const uint32_t a0 = unbias_f16x2(codes_lo_f16x2(wa));
+            const uint32_t a1 = unbias_f16x2(codes_lo_f16x2(wb));
+            const uint32_t a2 = unbias_f16x2(codes_hi_f16x2(wa));
+            const uint32_t a3 = unbias_f16x2(codes_hi_f16x2(wb));
+            const uint32_t a4 = unbias_f16x2(codes_lo_f16x2(wa8));
+            const uint32_t a5 = unbias_f16x2(codes_lo_f16x2(wb8));
+            const uint32_t a6 = unbias_f16x2(codes_hi_f16x2(wa8));
+            const uint32_t a7 = unbias_f16x2(codes_hi_f16x2(wb8));
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               float* dd = d[mi][rt][h][nt];
-              dd[0] = dd[2] = -xs0[h][nt].y;
-              dd[1] = dd[3] = -xs1[h][nt].y;
+              dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
               mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bh[h][nt].x, bh[h][nt].y);
               mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bl[h][nt].x, bl[h][nt].y);
               mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bh[h][nt].z, bh[h][nt].w);
@@ -465,7 +485,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
           }
         }
       }
-      if (jp < 3) load_b(jp + 1, bh, bl, xs0, xs1);
+      if (jp < 3)
+        load_b(jp + 1, bh, bl, xs0, xs1);
+      else if (next_same_unit)
+        load_b_at(gbase + 8, 0, bh, bl, xs0, xs1);
 #pragma unroll
       for (int mi = 0; mi < NMAT; ++mi) {
         const float* ssm = reinterpret_cast<const float*>(rs + mi * 2048) + sb_lane + 2 * jp;
@@ -495,20 +518,23 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
         }
       }
     }
+    b_ready = next_same_unit;
     __syncwarp();
     if (lane == 0 && pc.u < units) {
       issue_w(pc, slot);
       issue_x(pc, slot);
-      pc.advance(p, W, units, ksplit, spu, KS);
+      pc.advance(p, W, units, ksplit, spu, KS, UM);
     }
 
     const int unit = cc.u;
     const int tile = cc.tile;
     const int seg = cc.seg;
-    if (!cc.advance(p, W, units, ksplit, spu, KS)) continue;
+    if (!cc.advance(p, W, units, ksplit, spu, KS, UM)) continue;
 
     // ------------------------------------------------------------ unit done
-    if (ksplit > 1) {
+    // fin[um] is the tile's full sum for matrix um of the unit's tile
+    float fin[UM][NMAT][2][NT][4];
+    if (ksplit > 1 || PAIRED) {
       // Deterministic split-K: every unit stores its fragment partial; the
       // last unit of a tile to finish sums them in k order.
       constexpr int NACC = NMAT * 2 * NT * 4;
@@ -522,54 +548,67 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
       unsigned prev = 0;
       if (lane == 0) prev = atomicAdd(p.tile_cnt + tile, 1u);
       prev = __shfl_sync(0xffffffffu, prev, 0);
-      if (prev != (unsigned)ksplit - 1) {
 #pragma unroll
-        for (int mi = 0; mi < NMAT; ++mi)
+      for (int mi = 0; mi < NMAT; ++mi)
 #pragma unroll
-          for (int rt = 0; rt < 2; ++rt)
+        for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
-            for (int nt = 0; nt < NT; ++nt)
+          for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-              for (int e = 0; e < 4; ++e) acc[mi][rt][nt][e] = 0.f;
-        continue;
-      }
+            for (int e = 0; e < 4; ++e) acc[mi][rt][nt][e] = 0.f;
+      if (prev != (unsigned)(UM * ksplit) - 1) continue;
       __threadfence();
-      float* aw = &acc[0][0][0][0];
-#pragma unroll
-      for (int q = 0; q < NACC; ++q) aw[q] = 0.f;
       // k order is fixed (deterministic); loads of four partials are issued
       // together so their L2 latencies overlap
-      const float4* src0 =
-          reinterpret_cast<const float4*>(p.part) + ((size_t)tile * ksplit * 32 + lane) * (NACC / 4);
       const size_t pstride = (size_t)32 * (NACC / 4);
-      int s2 = 0;
-      for (; s2 + 4 <= ksplit; s2 += 4) {
-        float4 v[4][NACC / 4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+      for (int um = 0; um < UM; ++um) {
+        float* aw = &fin[um][0][0][0][0];
 #pragma unroll
-          for (int q = 0; q < NACC / 4; ++q) v[u][q] = __ldcg(src0 + (s2 + u) * pstride + q);
+        for (int q = 0; q < NACC; ++q) aw[q] = 0.f;
+        const float4* src0 = reinterpret_cast<const float4*>(p.part) +
+                             ((size_t)(tile * UM + um) * ksplit * 32 + lane) * (NACC / 4);
+        int s2 = 0;
+        for (; s2 + 4 <= ksplit; s2 += 4) {
+          float4 v[4][NACC / 4];
 #pragma unroll
-        for (int u = 0; u < 4; ++u)
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int q = 0; q < NACC / 4; ++q) v[u][q] = __ldcg(src0 + (s2 + u) * pstride + q);
+#pragma unroll
+          for (int u = 0; u < 4; ++u)
+#pragma unroll
+            for (int q = 0; q < NACC / 4; ++q) {
+              aw[4 * q] += v[u][q].x;
+              aw[4 * q + 1] += v[u][q].y;
+              aw[4 * q + 2] += v[u][q].z;
+              aw[4 * q + 3] += v[u][q].w;
+            }
+        }
+        for (; s2 < ksplit; ++s2) {
 #pragma unroll
           for (int q = 0; q < NACC / 4; ++q) {
-            aw[4 * q] += v[u][q].x;
-            aw[4 * q + 1] += v[u][q].y;
-            aw[4 * q + 2] += v[u][q].z;
-            aw[4 * q + 3] += v[u][q].w;
+            const float4 v = __ldcg(src0 + s2 * pstride + q);
+            aw[4 * q] += v.x;
+            aw[4 * q + 1] += v.y;
+            aw[4 * q + 2] += v.z;
+            aw[4 * q + 3] += v.w;
           }
-      }
-      for (; s2 < ksplit; ++s2) {
-#pragma unroll
-        for (int q = 0; q < NACC / 4; ++q) {
-          const float4 v = __ldcg(src0 + s2 * pstride + q);
-          aw[4 * q] += v.x;
-          aw[4 * q + 1] += v.y;
-          aw[4 * q + 2] += v.z;
-          aw[4 * q + 3] += v.w;
         }
       }
       if (lane == 0) p.tile_cnt[tile] = 0u;  // leave the counter cleared
+    } else {
+#pragma unroll
+      for (int mi = 0; mi < NMAT; ++mi)
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              fin[0][mi][rt][nt][e] = acc[mi][rt][nt][e];
+              acc[mi][rt][nt][e] = 0.f;
+            }
     }
 
     // ---------------------------------------------------------- epilogue
@@ -587,7 +626,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
             const int c = nt * 8 + 2 * tq + (e & 1);
             if (row < sg.n && c < m) {
               const size_t o = (size_t)c * sg.ld + sg.out_col0 + row;
-              float v = acc[0][rt][nt][e];
+              float v = fin[0][0][rt][nt][e];
               if (sg.res) v += sg.res[o];
               sg.out[o] = v;
             }
@@ -604,8 +643,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
           for (int e = 0; e < 4; ++e) {
             const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
             const int c = nt * 8 + 2 * tq + (e & 1);
-            const float gv = acc[0][rt][nt][e];
-            const float uv = acc[1][rt][nt][e];
+            const float gv = PAIRED ? fin[0][0][rt][nt][e] : fin[0][0][rt][nt][e];
+            const float uv = PAIRED ? fin[UM - 1][0][rt][nt][e] : fin[0][NMAT - 1][rt][nt][e];
             const float hv = gv / (1.f + __expf(-gv)) * uv * scale;
             if (c < p.out_m) {
               const float2 hs = xp_store_elem(p.out_xp, p.out_m, g_out, c, rloc >> 3, rloc & 7, hv);
@@ -633,21 +672,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
         for (int e = 0; e < 4; e += 2) {
           const int row = rbase + rt * 16 + gid + ((e & 2) ? 8 : 0);
           if (tq == 0 && row < sg.n) {
-            const float v = acc[0][rt][0][e];
+            const float v = fin[0][0][rt][0][e];
             if (p.logits) p.logits[row] = v;
             const unsigned long long key = argmax_key(v, row);
             best = key > best ? key : best;
           }
         }
     }
-#pragma unroll
-    for (int mi = 0; mi < NMAT; ++mi)
-#pragma unroll
-      for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) acc[mi][rt][nt][e] = 0.f;
   }
 
   if constexpr (EPI == kEpiArgmax) {

@@ -56,7 +56,9 @@ __global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackA
   pdl_wait();
   pdl_launch_dependents();
 #endif
-  const int c = blockIdx.x;
+  // grid = (slices, m): every CTA of row c computes the row's norms and
+  // writes octets [slice * per, (slice + 1) * per) of the packed output
+  const int c = blockIdx.y;
   float inv[2] = {1.f, 1.f};
   for (int si = 0; si < a.nseg; ++si) {
     const NormSeg& s = a.seg[si];
@@ -78,10 +80,14 @@ __global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackA
   // pass 2: octets of the concatenation
   const int K = a.seg[0].dim + (a.nseg > 1 ? a.seg[1].dim : 0);
   const int octets = K / 8;
-  for (int o0 = 0; o0 < octets; o0 += kNormThreads) {
+  // slices hold whole groups (4 octets) so the group sums stay in one CTA
+  const int per = (octets / 4 + gridDim.x - 1) / gridDim.x * 4;
+  const int o_begin = blockIdx.x * per;
+  const int o_end = min(octets, o_begin + per);
+  for (int o0 = o_begin; o0 < o_end; o0 += kNormThreads) {
     const int o = o0 + threadIdx.x;
     float2 sum = make_float2(0.f, 0.f);
-    if (o < octets) {
+    if (o < o_end) {
       const int k = o * 8;
       const int si = (a.nseg > 1 && k >= a.seg[0].dim) ? 1 : 0;
       const NormSeg& s = a.seg[si];
@@ -94,16 +100,21 @@ __global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackA
       v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
       v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
       if (dl) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] += dl[kk + i];
+        const float4 d0 = *reinterpret_cast<const float4*>(dl + kk);
+        const float4 d1 = *reinterpret_cast<const float4*>(dl + kk + 4);
+        v[0] += d0.x; v[1] += d0.y; v[2] += d0.z; v[3] += d0.w;
+        v[4] += d1.x; v[5] += d1.y; v[6] += d1.z; v[7] += d1.w;
       }
       if (s.out_sum) {
 #pragma unroll
         for (int i = 0; i < 8; ++i) s.out_sum[(size_t)c * s.dim + kk + i] = v[i];
       }
       if (s.w) {
+        const float4 w0 = *reinterpret_cast<const float4*>(s.w + kk);
+        const float4 w1 = *reinterpret_cast<const float4*>(s.w + kk + 4);
+        const float wv[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
 #pragma unroll
-        for (int i = 0; i < 8; ++i) v[i] = v[i] * inv[si] * s.w[kk + i];
+        for (int i = 0; i < 8; ++i) v[i] = v[i] * inv[si] * wv[i];
       }
       if (s.out_norm) {
 #pragma unroll
@@ -123,7 +134,7 @@ __global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackA
       sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
       sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
       sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 2);
-      if (o < octets && (o & 3) == 0) a.xs[(o / 4) * a.m + c] = sum;
+      if (o < o_end && (o & 3) == 0) a.xs[(o / 4) * a.m + c] = sum;
     }
   }
 }
@@ -138,8 +149,13 @@ cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, fl
   a.xp = xp;
   a.xs = xs;
   a.err = err;
+  // a few CTAs per row so one row's octets are packed in parallel
+  const int K = segs[0].dim + (nseg > 1 ? segs[1].dim : 0);
+  int slices = (K / 8 + kNormThreads - 1) / kNormThreads;
+  if (slices > 8) slices = 8;
+  if (m > 4) slices = 1;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(m);
+  cfg.gridDim = dim3(slices, m);
   cfg.blockDim = dim3(kNormThreads);
   cfg.stream = st;
   cudaLaunchAttribute attr;
