@@ -56,8 +56,8 @@ __host__ __device__ inline size_t attn_part_o_offset(int nkv, int nsplit, int QG
 
 __host__ __device__ inline AttnLayout attn_layout(int dqk, int dv, int QG, int m) {
   AttnLayout L;
-  L.kstride = dqk + 4;
-  L.stage_bytes = (size_t)kTileKeys * L.kstride * 4 + (size_t)kTileKeys * dv * 4;
+  L.kstride = dqk;  // K tiles are 128-byte-swizzled 32 x 32-float boxes (see attend_tile)
+  L.stage_bytes = (size_t)kTileKeys * dqk * 4 + (size_t)kTileKeys * dv * 4;  // multiple of 4 KB
   const size_t red_bytes = (size_t)QG * attn_nparts(dqk) * kTileKeys * 4;
   const size_t fixed = (size_t)QG * dqk * 4 + (size_t)kPadQ * kTileKeys * 4 + red_bytes + 3 * kPadQ * 4 +
                        (size_t)m * (dqk + dv) * 4 + 8 * 8 + 256;
@@ -70,7 +70,7 @@ __host__ __device__ inline AttnLayout attn_layout(int dqk, int dv, int QG, int m
   L.newk_off = L.stat_off + 3 * kPadQ * 4;
   L.newv_off = L.newk_off + (size_t)m * dqk * 4;
   L.bar_off = (L.newv_off + (size_t)m * dv * 4 + 15) / 16 * 16;
-  L.total = L.bar_off + 8 * 8;
+  L.total = L.bar_off + 8 * 8 + 1024;  // + alignment slack of the swizzled stages
   return L;
 }
 
@@ -108,7 +108,7 @@ __device__ __forceinline__ void warp_norm_rope(float* v, int d, const float* nw,
 // One tile of keys [key0, key0 + nk) from shared memory: logits, online
 // softmax update and P.V accumulation.  Ends with the CTA synchronised.
 template <int QPT>
-__device__ __forceinline__ void attend_tile(const AttnParams& a, const float* Ks, int kstride,
+__device__ __forceinline__ void attend_tile(const AttnParams& a, const float* Ks, bool kswz, int kstride,
                                            const float* Vs, int nk, int key0, const float* qs,
                                            float* ps, float* red, float* Ms, float* ls,
                                            float* als, float (&oacc)[QPT], int QG, int G) {
@@ -125,8 +125,19 @@ __device__ __forceinline__ void attend_tile(const AttnParams& a, const float* Ks
     // rows past nk are not read (the new-key tile holds only m rows)
     float4 kr[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-      kr[i] = (i < pc4 && lane < nk) ? kv[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int i = 0; i < 4; ++i) {
+      kr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < pc4 && lane < nk) {
+        if (kswz) {
+          // box f/8 of 32 rows x 128 bytes; 16-byte chunk c of row r at c ^ (r & 7)
+          const int f = warp * pc4 + i;
+          kr[i] = *reinterpret_cast<const float4*>(Ks + (f >> 3) * 1024 + lane * 32 +
+                                                   (((f & 7) ^ (lane & 7)) << 2));
+        } else {
+          kr[i] = kv[i];
+        }
+      }
+    }
     for (int qi = 0; qi < QG; ++qi) {
       const float4* qv = reinterpret_cast<const float4*>(qs + qi * dqk) + warp * pc4;
       float acc = 0.f;
@@ -195,8 +206,11 @@ __device__ __forceinline__ void attend_tile(const AttnParams& a, const float* Ks
 }
 
 template <int QPT>
-__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnParams a) {
-  extern __shared__ __align__(16) uint8_t smraw[];
+__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const __grid_constant__ AttnParams a) {
+  extern __shared__ __align__(1024) uint8_t smraw_unaligned[];
+  // the swizzled K boxes need 1024-byte-aligned stages
+  uint8_t* smraw = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smraw_unaligned) + 1023) & ~uintptr_t(1023));
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -225,7 +239,6 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
   const int t_begin = min(ntiles, split * tps);
   const int t_end = min(ntiles, t_begin + tps);
   const int my_tiles = t_end - t_begin;
-  const float* kbase = a.kc + (size_t)kvh * a.cap * dqk;
   const float* vbase = a.vc + (size_t)kvh * a.cap * dv;
 
   if (tid == 0) {
@@ -242,13 +255,14 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
     uint8_t* st = smraw + (size_t)slot * Ly.stage_bytes;
     float* Ks = reinterpret_cast<float*>(st);
     float* Vs = Ks + kTileKeys * Ly.kstride;
-    if (lane == 0) mbar_arrive_expect_tx(&bars[slot], (uint32_t)nk * (dqk + dv) * 4);
-    __syncwarp();
-    if (lane < nk)
-      bulk_load(Ks + lane * Ly.kstride, kbase + (size_t)(key0 + lane) * dqk, dqk * 4, &bars[slot],
-                pol);
-    if (lane == 0)
+    // K: dqk/32 tensor-map boxes of 32 rows (full boxes are counted even past
+    // the cache end, where the copy fills zeros); V: one bulk copy of nk rows
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&bars[slot], (uint32_t)kTileKeys * dqk * 4 + (uint32_t)nk * dv * 4);
+      for (int b = 0; b < dqk / 32; ++b)
+        tma_load_2d(Ks + b * 1024, &a.kmap, &bars[slot], b * 32, kvh * a.cap + key0, pol);
       bulk_load(Vs, vbase + (size_t)key0 * dv, (uint32_t)nk * dv * 4, &bars[slot], pol);
+    }
   };
   if (a.prefetch_before_wait && warp == 0)
     for (int t = 0; t < S && t < my_tiles; ++t) issue(t, t);
@@ -309,12 +323,12 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const AttnPar
     const float* Ks = reinterpret_cast<const float*>(smraw + (size_t)slot * Ly.stage_bytes);
     const float* Vs = Ks + kTileKeys * Ly.kstride;
     const int key0 = kbeg + (t_begin + t) * kTileKeys;
-    attend_tile<QPT>(a, Ks, Ly.kstride, Vs, min(kTileKeys, L - key0), key0, qs, ps, red, Ms, ls,
-                     als, oacc, QG, G);
+    attend_tile<QPT>(a, Ks, true, Ly.kstride, Vs, min(kTileKeys, L - key0), key0, qs, ps, red,
+                     Ms, ls, als, oacc, QG, G);
     if (warp == 0 && t + S < my_tiles) issue(t + S, slot);
   }
   if (has_new)
-    attend_tile<QPT>(a, newk, dqk, newv, a.m, L, qs, ps, red, Ms, ls, als, oacc, QG, G);
+    attend_tile<QPT>(a, newk, false, dqk, newv, a.m, L, qs, ps, red, Ms, ls, als, oacc, QG, G);
 
   // ---- partial of this split: (M, l) pairs and unnormalised outputs
   const size_t pidx = (size_t)(kvh * a.nsplit + split) * QG;
@@ -461,6 +475,7 @@ size_t attn_part_bytes(int nkv, int nsplit, int q_per_kv, int dv) {
 
 template <int QPT>
 static cudaError_t launch_attn_t(const AttnParams& a, size_t smem, cudaStream_t st) {
+  static_assert(sizeof(AttnParams) <= 4096, "kernel parameters fit the classic limit");
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
@@ -484,7 +499,10 @@ static cudaError_t launch_attn_t(const AttnParams& a, size_t smem, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, attn_decode_kernel<QPT>, a);
 }
 
-cudaError_t launch_attn(const AttnParams& a, cudaStream_t st) {
+cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
+  AttnParams a = a_in;
+  cudaError_t ke = encode_f32_tile_map(&a.kmap, a.kc, (uint64_t)a.nkv * a.cap, (uint64_t)a.dqk);
+  if (ke != cudaSuccess) return ke;
   const int QG = (a.nh / a.nkv) * a.m;
   const AttnLayout Ly = attn_layout(a.dqk, a.dv, QG, a.m);
   // the merge reuses the stage ring: split weights and the finished rows

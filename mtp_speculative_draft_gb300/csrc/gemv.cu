@@ -249,6 +249,13 @@ static CUresult encode2d(CUtensorMap* m, CUtensorMapDataType dt, const void* bas
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+cudaError_t encode_f32_tile_map(CUtensorMap* out, const float* base, uint64_t rows, uint64_t cols) {
+  // rows of `cols` floats, box 32 rows x 32 floats, 128-byte swizzle
+  CUresult r = encode2d(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, cols, rows, cols * 4, 32, 32,
+                        CU_TENSOR_MAP_SWIZZLE_128B);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 mtp_status encode_qmat(QMat* out, const mtp_affine4& w, const char* name) {
   const uint64_t kw = (uint64_t)w.k / 8, kg = (uint64_t)w.k / kGroup;
   CUresult r = encode2d(&out->q, CU_TENSOR_MAP_DATA_TYPE_UINT32, w.q, kw, (uint64_t)w.n, kw * 4,

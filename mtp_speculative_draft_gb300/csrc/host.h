@@ -65,7 +65,11 @@ struct NormSeg {
 cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, float2* xs,
                              int* err, cudaStream_t st);
 
-struct AttnParams {
+// Tensor map over float rows [rows][cols] with 32 x 32 boxes, 128-byte swizzle.
+cudaError_t encode_f32_tile_map(CUtensorMap* out, const float* base, uint64_t rows, uint64_t cols);
+
+struct alignas(64) AttnParams {
+  CUtensorMap kmap;     // K cache viewed as [n_kv * cap][dqk]
   int nh, nkv, dqk, dv, rot, window, gated;
   float eps, scale;
   const float *qp, *kp, *vp, *qn, *kn, *rope, *sinks;
