@@ -153,7 +153,7 @@ mtp_status mtp_rope_table(float *d_rope, int32_t max_pos, int32_t rot_dim, doubl
  *   d_k_cache [n_kv][cache_cap][dqk], d_v_cache [n_kv][cache_cap][dv]:
  *     rows < cache_len are read; rows cache_len .. cache_len+m-1 are written.
  *   d_out [m][n_heads*dv] float32.
- *   1 <= m <= 16; (n_heads/n_kv_heads)*m <= 64.
+ *   1 <= m <= 16; (n_heads/n_kv_heads)*m <= 16.
  *   Returns MTP_ERR_CAPACITY if cache_len + m > cache_cap.
  * ------------------------------------------------------------------------ */
 size_t attn_decode_sink_workspace_bytes(const mtp_attn_geom *g, int32_t m, int32_t cache_len);

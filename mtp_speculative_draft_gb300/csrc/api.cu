@@ -261,10 +261,8 @@ static mtp_status check_geom(const mtp_attn_geom* g, int m) {
   if (m < 1 || m > 16) return fail(MTP_ERR_UNSUPPORTED, "attention: m must be in 1..16");
   if ((g->n_heads / g->n_kv_heads) * m > 16)
     return fail(MTP_ERR_UNSUPPORTED, "attention: (n_heads/n_kv_heads)*m must be <= 16");
-  // the P.V split gives each thread (512 / head_dim_v) query slices of at most 8 rows
-  if (g->head_dim_v > 512 ||
-      ((g->n_heads / g->n_kv_heads) * m + (512 / g->head_dim_v) - 1) / (512 / g->head_dim_v) > 8)
-    return fail(MTP_ERR_UNSUPPORTED, "attention: too many query rows for head_dim_v");
+  if (!attn_supported((g->n_heads / g->n_kv_heads) * m, g->head_dim_qk, g->head_dim_v, m))
+    return fail(MTP_ERR_UNSUPPORTED, "attention: query rows and head dims exceed one CTA");
   if (!(g->eps >= 0.f) || !(g->scale >= 0.f))
     return fail(MTP_ERR_INVALID_ARG, "attention: eps and scale must be >= 0");
   return MTP_OK;
@@ -272,8 +270,8 @@ static mtp_status check_geom(const mtp_attn_geom* g, int m) {
 
 size_t attn_decode_sink_workspace_bytes(const mtp_attn_geom* g, int32_t m, int32_t cache_len) {
   if (!g || g->n_kv_heads <= 0 || m <= 0 || cache_len < 0) return 0;
-  const int keys = (g->window > 0 ? std::min(cache_len, g->window - 1) : cache_len) + m;
-  const int ns = attn_splits(g->n_kv_heads, keys);
+  const int cached = g->window > 0 ? std::min(cache_len, g->window - 1) : cache_len;
+  const int ns = attn_splits_bound(g->n_kv_heads, cached);
   const int qg = (g->n_heads / g->n_kv_heads) * m;
   return sizeof(WsHeader) + align256(attn_part_bytes(g->n_kv_heads, ns, qg, g->head_dim_v)) + 256;
 }
@@ -303,8 +301,7 @@ static AttnParams make_attn(const mtp_attn_geom* g, const float* qp, const float
   a.L = L;
   a.cap = cap;
   a.m = m;
-  const int keys = (g->window > 0 ? std::min(L, g->window - 1) : L) + m;
-  a.nsplit = attn_splits(a.nkv, keys);
+  a.nsplit = attn_splits(a.nkv, g->window > 0 ? std::min(L, g->window - 1) : L);
   return a;
 }
 
@@ -603,8 +600,8 @@ static void carve_layer(Carve& cv, const mtp_layer_desc* L, int m, LayerWs* w) {
   w->qp = cv.take<float>(sizeof(float) * m * qrows);
   w->kp = cv.take<float>(sizeof(float) * m * g.n_kv_heads * g.head_dim_qk);
   w->vp = cv.take<float>(sizeof(float) * m * g.n_kv_heads * g.head_dim_v);
-  const int keys = (g.window > 0 ? std::min(L->cache_cap, g.window - 1) : L->cache_cap) + m;
-  const int ns = attn_splits(g.n_kv_heads, keys);
+  const int cached = g.window > 0 ? std::min(L->cache_cap, g.window - 1) : L->cache_cap;
+  const int ns = attn_splits_bound(g.n_kv_heads, cached);
   w->part = cv.take<float>(attn_part_bytes(g.n_kv_heads, ns, (g.n_heads / g.n_kv_heads) * m,
                                            g.head_dim_v));
   w->am_partial = cv.take<unsigned long long>(8 * 4096);

@@ -7,46 +7,35 @@
 // apply_sigmoid_gate_multiply) and "cortiq-engine 0.8.49 src/mimo_mtp.rs"
 // (sliding window, per-head sinks).
 //
-// Split-K over the cache, one CTA per (split, KV head), about one CTA per
-// SM.  Each CTA serves all query heads of its KV head (grouped-query sharing
-// of the K/V stream) for all m new rows.  The cached keys and values stream
-// through a ring of shared-memory stages filled by bulk copies (one copy per
-// key row into a padded row, one copy per value tile) and completed on
-// mbarriers; the softmax is kept online in the log2 domain.  The m new keys
-// and values are normalised/rotated in shared memory, appended to the cache
-// with plain stores, and attended to by the last split from shared memory.
-// The last CTA of a KV head to finish (completion counter, no spinning)
-// merges the partials with precomputed split weights, adds the sink to the
-// denominator, applies the gate and writes the output both as fp32 and
-// packed for the o_proj GEMV.
+// Split-K over the cache, about one CTA per SM.  A CTA serves every query
+// row of its KV head (grouped-query sharing of the K/V stream: G heads x m
+// new rows).  It owns `nbuf` tile buffers of 32 keys; each buffer is read by
+// `qgroups` warps, each of which holds a slice of the query rows.  Warps work
+// on their buffer's tiles alone, with no CTA-wide barrier in the loop:
+//   * the tile arrives by TMA (K as 128-byte-swizzled boxes of 32 rows x 32
+//     floats, V as one bulk copy) and completes on the buffer's mbarrier;
+//   * logits with lane = key: a lane reads its key row once and keeps one
+//     accumulator per query row; query chunks are warp-wide broadcasts;
+//   * online softmax per query row in the log2 domain (warp shuffles);
+//   * P.V with lane = output dims; probabilities go through a per-warp row
+//     of shared memory and are read back four keys at a time.
+// The buffers' states meet once in shared memory and the CTA writes one
+// partial.  The m new keys and values are normalised/rotated, appended to the
+// cache by the last split and attended to from shared memory.  The last CTA
+// of a KV head to finish (completion counter, no spinning) merges the
+// partials, adds the sink to the denominator, applies the gate and writes the
+// output as fp32 and packed for the o_proj GEMV.
 #include "host.h"
 
 namespace mtp {
 
-constexpr int kAttnThreads = 512;
 constexpr int kTileKeys = 32;
-constexpr int kMaxQ = 16;            // query rows per KV head (heads per group x m)
 constexpr float kNegBig = -1e30f;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kAttnSmemMax = 200 * 1024;
-constexpr int kQpt = 8;              // largest per-thread query count of the P.V split
-// probability/statistics rows allocated for the padded query slices of P.V
-// (up to kQpt rows per slice, at most kAttnThreads / 32 slices)
-constexpr int kPadQ = kQpt * (kAttnThreads / 32);
-
-struct AttnLayout {
-  int stages;
-  int kstride;       // padded K row (floats)
-  size_t stage_bytes, q_off, p_off, red_off, stat_off, newk_off, newv_off, bar_off, total;
-};
-
-// Slices of the head dimension for the logits: a power of two <= 16 that
-// divides dqk/4, with at most 4 float4 per slice.
-__host__ __device__ inline int attn_nparts(int dqk) {
-  int n = 16;
-  while (n > 1 && ((dqk / 4) % n) != 0) n >>= 1;
-  return n;
-}
+constexpr int kAttnMaxWarps = 8;
+constexpr int kAttnQMax = 8;                     // query rows per warp (template bound)
+constexpr size_t kAttnSmemLimit = 226 * 1024;     // dynamic shared memory of one CTA (227 KB less static)
+constexpr size_t kAttnSlack = 1024;               // alignment of the swizzled K boxes
 
 // Partials: (M, l) pairs [nkv][nsplit][QG][2], then outputs [nkv][nsplit][QG][dv]
 // starting on a 16-byte boundary.
@@ -54,23 +43,25 @@ __host__ __device__ inline size_t attn_part_o_offset(int nkv, int nsplit, int QG
   return ((size_t)nkv * nsplit * QG * 2 + 3) / 4 * 4;
 }
 
-__host__ __device__ inline AttnLayout attn_layout(int dqk, int dv, int QG, int m) {
+__host__ __device__ inline size_t attn_tile_bytes(int dqk, int dv) {
+  return (size_t)kTileKeys * (dqk + dv) * 4;  // a multiple of 4 KB (dims are multiples of 32)
+}
+
+struct AttnLayout {
+  size_t q_off, newk_off, newv_off, ps_off, bar_off, total;
+};
+
+// [nbuf tile buffers][queries QG x dqk][new keys m x dqk][new values m x dv]
+// [probability rows: warps x kAttnQMax x 32][mbarriers]
+__host__ __device__ inline AttnLayout attn_layout(int dqk, int dv, int QG, int m, int nbuf,
+                                                  int warps) {
   AttnLayout L;
-  L.kstride = dqk;  // K tiles are 128-byte-swizzled 32 x 32-float boxes (see attend_tile)
-  L.stage_bytes = (size_t)kTileKeys * dqk * 4 + (size_t)kTileKeys * dv * 4;  // multiple of 4 KB
-  const size_t red_bytes = (size_t)QG * attn_nparts(dqk) * kTileKeys * 4;
-  const size_t fixed = (size_t)QG * dqk * 4 + (size_t)kPadQ * kTileKeys * 4 + red_bytes + 3 * kPadQ * 4 +
-                       (size_t)m * (dqk + dv) * 4 + 8 * 8 + 256;
-  int s = (int)((kAttnSmemMax - fixed) / L.stage_bytes);
-  L.stages = s > 3 ? 3 : (s < 1 ? 1 : s);
-  L.q_off = L.stages * L.stage_bytes;
-  L.p_off = L.q_off + (size_t)QG * dqk * 4;
-  L.red_off = L.p_off + (size_t)kPadQ * kTileKeys * 4;
-  L.stat_off = L.red_off + red_bytes;
-  L.newk_off = L.stat_off + 3 * kPadQ * 4;
+  L.q_off = (size_t)nbuf * attn_tile_bytes(dqk, dv);
+  L.newk_off = L.q_off + (size_t)QG * dqk * 4;
   L.newv_off = L.newk_off + (size_t)m * dqk * 4;
-  L.bar_off = (L.newv_off + (size_t)m * dv * 4 + 15) / 16 * 16;
-  L.total = L.bar_off + 8 * 8 + 1024;  // + alignment slack of the swizzled stages
+  L.ps_off = L.newv_off + (size_t)m * dv * 4;
+  L.bar_off = L.ps_off + (size_t)warps * kAttnQMax * kTileKeys * 4;
+  L.total = L.bar_off + (size_t)nbuf * 8;
   return L;
 }
 
@@ -101,179 +92,212 @@ __device__ __forceinline__ void warp_norm_rope(float* v, int d, const float* nw,
   __syncwarp();
 }
 
-// Work split of the P.V product: thread t owns output dim t % dv for the
-// query rows q = t / dv + k * (kAttnThreads / dv), k < QPT (a template
-// bound chosen on the host as the smallest power of two that covers QG).
-
-// One tile of keys [key0, key0 + nk) from shared memory: logits, online
-// softmax update and P.V accumulation.  Ends with the CTA synchronised.
-template <int QPT>
-__device__ __forceinline__ void attend_tile(const AttnParams& a, const float* Ks, bool kswz, int kstride,
-                                           const float* Vs, int nk, int key0, const float* qs,
-                                           float* ps, float* red, float* Ms, float* ls,
-                                           float* als, float (&oacc)[QPT], int QG, int G) {
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int dqk = a.dqk, dv = a.dv;
-  const int kq4 = dqk / 4;
-  // logits: lane = key, warp = slice of the head dimension.  Each key
-  // element is read from shared memory once (into registers); the query
-  // slice is a warp-wide broadcast.  Slice partials meet in `red`.
-  const int nparts = attn_nparts(dqk);
-  const int pc4 = kq4 / nparts;  // float4 per slice
-  if (warp < nparts) {
-    const float4* kv = reinterpret_cast<const float4*>(Ks + lane * kstride) + warp * pc4;
-    // rows past nk are not read (the new-key tile holds only m rows)
-    float4 kr[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      kr[i] = make_float4(0.f, 0.f, 0.f, 0.f);
-      if (i < pc4 && lane < nk) {
-        if (kswz) {
-          // box f/8 of 32 rows x 128 bytes; 16-byte chunk c of row r at c ^ (r & 7)
-          const int f = warp * pc4 + i;
-          kr[i] = *reinterpret_cast<const float4*>(Ks + (f >> 3) * 1024 + lane * 32 +
-                                                   (((f & 7) ^ (lane & 7)) << 2));
-        } else {
-          kr[i] = kv[i];
-        }
-      }
-    }
-    for (int qi = 0; qi < QG; ++qi) {
-      const float4* qv = reinterpret_cast<const float4*>(qs + qi * dqk) + warp * pc4;
-      float acc = 0.f;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        if (i < pc4) {
-          const float4 x = qv[i];
-          acc = fmaf(x.x, kr[i].x, fmaf(x.y, kr[i].y, fmaf(x.z, kr[i].z, fmaf(x.w, kr[i].w, acc))));
-        }
-      }
-      red[(qi * nparts + warp) * kTileKeys + lane] = acc;
-    }
-  }
-  __syncthreads();
-  for (int idx = tid; idx < QG * kTileKeys; idx += kAttnThreads) {
-    const int jj = idx & (kTileKeys - 1), qi = idx / kTileKeys;
-    const int j = key0 + jj, p = a.L + qi / G;
-    float l = kNegBig;
-    if (jj < nk && j <= p && (a.window <= 0 || j > p - a.window)) {
-      l = 0.f;
-      for (int pt = 0; pt < nparts; ++pt) l += red[(qi * nparts + pt) * kTileKeys + jj];
-    }
-    ps[qi * kTileKeys + jj] = l;
-  }
-  __syncthreads();
-  for (int qi = warp; qi < QG; qi += kAttnThreads / 32) {
-    const float l = ps[qi * kTileKeys + lane];
-    const float mold = Ms[qi];
-    const float mnew = fmaxf(mold, warp_max(l));
-    const float pr = l <= 0.5f * kNegBig ? 0.f : exp2f(l - mnew);
-    const float s = warp_sum(pr);
-    ps[qi * kTileKeys + lane] = pr;
-    if (lane == 0) {
-      const float alpha = exp2f(mold - mnew);
-      als[qi] = alpha;
-      ls[qi] = ls[qi] * alpha + s;
-      Ms[qi] = mnew;
-    }
-  }
-  __syncthreads();
-  const int nsl = kAttnThreads / dv;  // query slices
-  const int d = tid % dv, q0 = tid / dv;
-  if (q0 < nsl) {
-    // rows past QG read zero probabilities and rescale factors (padded)
-#pragma unroll
-    for (int k = 0; k < QPT; ++k) oacc[k] *= als[q0 + k * nsl];
-    // keys four at a time: independent loads ahead of their FMAs
-    int jj = 0;
-    for (; jj + 4 <= nk; jj += 4) {
-      const float v0 = Vs[jj * dv + d], v1 = Vs[(jj + 1) * dv + d];
-      const float v2 = Vs[(jj + 2) * dv + d], v3 = Vs[(jj + 3) * dv + d];
-#pragma unroll
-      for (int k = 0; k < QPT; ++k) {
-        const float4 pr = *reinterpret_cast<const float4*>(ps + (q0 + k * nsl) * kTileKeys + jj);
-        oacc[k] = fmaf(pr.x, v0, fmaf(pr.y, v1, fmaf(pr.z, v2, fmaf(pr.w, v3, oacc[k]))));
-      }
-    }
-    for (; jj < nk; ++jj) {
-      const float v = Vs[jj * dv + d];
-#pragma unroll
-      for (int k = 0; k < QPT; ++k)
-        oacc[k] = fmaf(ps[(q0 + k * nsl) * kTileKeys + jj], v, oacc[k]);
-    }
-  }
-  __syncthreads();
+// Named-barrier AND-reduction over `count` threads (all of them arrive).
+__device__ __forceinline__ bool bar_and(bool v, int id, int count) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\t"
+      "setp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.and.pred q, %2, %3, p;\n\t"
+      "selp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"((uint32_t)v), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
 }
 
-template <int QPT>
-__global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const __grid_constant__ AttnParams a) {
+__device__ __forceinline__ void bar_named(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// Retires an mbarrier before its shared memory is reused for other data.
+__device__ __forceinline__ void mbar_inval(uint64_t* bar) {
+  asm volatile("mbarrier.inval.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Output dims held by a lane: DV = dv / 32 values, in vectors of VW floats;
+// vector c of lane holds dims VW * (lane + 32 c) + [0, VW).
+template <int DV>
+struct LaneDims {
+  static constexpr int VW = DV % 4 == 0 ? 4 : (DV % 2 == 0 ? 2 : 1);
+  static constexpr int NV = DV / VW;
+  __device__ static int dim(int lane, int c) { return VW * (lane + 32 * c); }
+};
+
+template <int DV>
+__device__ __forceinline__ void load_dims(const float* row, int lane, float (&v)[DV]) {
+  using LD = LaneDims<DV>;
+#pragma unroll
+  for (int c = 0; c < LD::NV; ++c) {
+    const float* p = row + LD::dim(lane, c);
+    if constexpr (LD::VW == 4) {
+      const float4 t = *reinterpret_cast<const float4*>(p);
+      v[4 * c] = t.x; v[4 * c + 1] = t.y; v[4 * c + 2] = t.z; v[4 * c + 3] = t.w;
+    } else if constexpr (LD::VW == 2) {
+      const float2 t = *reinterpret_cast<const float2*>(p);
+      v[2 * c] = t.x; v[2 * c + 1] = t.y;
+    } else {
+      v[c] = *p;
+    }
+  }
+}
+
+// Running softmax state of one warp for its query rows.
+template <int QM, int DV>
+struct WarpState {
+  float M[QM], l[QM], o[QM][DV];
+};
+
+// One tile of nk keys starting at absolute key index key0, for the warp's
+// query rows q0 .. q0 + nq - 1.  `swz`: K in swizzled boxes (cached tiles),
+// else plain rows of dqk floats (the new keys).
+template <int QM, int DV>
+__device__ __forceinline__ void warp_tile(const AttnParams& a, WarpState<QM, DV>& st,
+                                          const float* Ks, bool swz, const float* Vs, int nk,
+                                          int key0, const float* qs, int q0, int nq, int G,
+                                          float* ps, int lane) {
+  const int dqk = a.dqk, dv = a.dv;
+  const int kq4 = dqk / 4;
+  const float* qrow = qs + (size_t)q0 * dqk;
+  // ---- logits: lane = key
+  float acc[QM];
+#pragma unroll
+  for (int q = 0; q < QM; ++q) acc[q] = 0.f;
+  if (lane < nk) {
+#pragma unroll 2
+    for (int f = 0; f < kq4; ++f) {
+      const float4 k = swz ? *reinterpret_cast<const float4*>(Ks + (f >> 3) * 1024 + lane * 32 +
+                                                               (((f & 7) ^ (lane & 7)) << 2))
+                           : *reinterpret_cast<const float4*>(Ks + lane * dqk + 4 * f);
+#pragma unroll
+      for (int q = 0; q < QM; ++q) {
+        if (q < nq) {
+          const float4 x = *reinterpret_cast<const float4*>(qrow + q * dqk + 4 * f);
+          acc[q] = fmaf(x.x, k.x, fmaf(x.y, k.y, fmaf(x.z, k.z, fmaf(x.w, k.w, acc[q]))));
+        }
+      }
+    }
+  }
+  // ---- online softmax per query row; probabilities to the warp's rows
+  const int j = key0 + lane;
+#pragma unroll
+  for (int q = 0; q < QM; ++q) {
+    if (q < nq) {
+      const int p = a.L + (q0 + q) / G;
+      const bool ok = lane < nk && j <= p && (a.window <= 0 || j > p - a.window);
+      const float l = ok ? acc[q] : kNegBig;
+      const float mnew = fmaxf(st.M[q], warp_max(l));
+      const float pr = ok ? exp2f(l - mnew) : 0.f;
+      const float alpha = exp2f(st.M[q] - mnew);
+      st.l[q] = st.l[q] * alpha + warp_sum(pr);
+      st.M[q] = mnew;
+      ps[q * kTileKeys + lane] = pr;
+#pragma unroll
+      for (int i = 0; i < DV; ++i) st.o[q][i] *= alpha;
+    }
+  }
+  __syncwarp();
+  // ---- P.V: lane = output dims, four keys per step (rows past nk hold p = 0
+  // and are read only from the V rows the copy filled)
+  int jj = 0;
+  for (; jj + 4 <= nk; jj += 4) {
+    float v[4][DV];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) load_dims<DV>(Vs + (size_t)(jj + u) * dv, lane, v[u]);
+#pragma unroll
+    for (int q = 0; q < QM; ++q) {
+      if (q < nq) {
+        const float4 p4 = *reinterpret_cast<const float4*>(ps + q * kTileKeys + jj);
+#pragma unroll
+        for (int i = 0; i < DV; ++i)
+          st.o[q][i] = fmaf(p4.x, v[0][i],
+                            fmaf(p4.y, v[1][i], fmaf(p4.z, v[2][i], fmaf(p4.w, v[3][i], st.o[q][i]))));
+      }
+    }
+  }
+  for (; jj < nk; ++jj) {
+    float v[DV];
+    load_dims<DV>(Vs + (size_t)jj * dv, lane, v);
+#pragma unroll
+    for (int q = 0; q < QM; ++q) {
+      if (q < nq) {
+        const float p = ps[q * kTileKeys + jj];
+#pragma unroll
+        for (int i = 0; i < DV; ++i) st.o[q][i] = fmaf(p, v[i], st.o[q][i]);
+      }
+    }
+  }
+  __syncwarp();
+}
+
+template <int QM, int DV>
+__global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
+    attn_decode_kernel(const __grid_constant__ AttnParams a) {
   extern __shared__ __align__(1024) uint8_t smraw_unaligned[];
-  // the swizzled K boxes need 1024-byte-aligned stages
+  // the swizzled K boxes need 1024-byte-aligned buffers
   uint8_t* smraw = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smraw_unaligned) + 1023) & ~uintptr_t(1023));
+  using LD = LaneDims<DV>;
   const int split = blockIdx.x;
   const int kvh = blockIdx.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int nthreads = blockDim.x, nw = nthreads >> 5;
   const int G = a.nh / a.nkv;
   const int QG = G * a.m;
   const int dqk = a.dqk, dv = a.dv;
   const int q_rows = a.nh * dqk * (a.gated ? 2 : 1);
-  const AttnLayout Ly = attn_layout(dqk, dv, QG, a.m);
-  const int S = Ly.stages;
+  const int nbuf = a.nbuf, qgroups = a.qgroups;
+  const int qpw = (QG + qgroups - 1) / qgroups;      // query rows per warp
+  const AttnLayout Ly = attn_layout(dqk, dv, QG, a.m, nbuf, nw);
+  const size_t tile_bytes = attn_tile_bytes(dqk, dv);
   float* qs = reinterpret_cast<float*>(smraw + Ly.q_off);
-  float* ps = reinterpret_cast<float*>(smraw + Ly.p_off);
-  float* red = reinterpret_cast<float*>(smraw + Ly.red_off);
-  float* Ms = reinterpret_cast<float*>(smraw + Ly.stat_off);
-  float* ls = Ms + kPadQ;
-  float* als = ls + kPadQ;
   float* newk = reinterpret_cast<float*>(smraw + Ly.newk_off);
   float* newv = reinterpret_cast<float*>(smraw + Ly.newv_off);
+  float* ps = reinterpret_cast<float*>(smraw + Ly.ps_off) + (size_t)warp * kAttnQMax * kTileKeys;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smraw + Ly.bar_off);
   __shared__ bool last;
 
-  // cached keys [kbeg, L) in whole tiles per split; new keys go to the last split
+  // this warp: buffer b, query rows [q0, q0 + nq)
+  const int b = warp / qgroups, qgi = warp % qgroups;
+  const int q0 = qgi * qpw;
+  const int nq = max(0, min(qpw, QG - q0));
+  const bool leader = qgi == 0 && lane == 0;
+  float* Kb = reinterpret_cast<float*>(smraw + (size_t)b * tile_bytes);
+  float* Vb = Kb + kTileKeys * dqk;
+
+  // cached keys [kbeg, L) in whole tiles per split; the new keys go to the last split
   const int L = a.L;
   const int kbeg = a.window > 0 ? max(0, L + 1 - a.window) : 0;
   const int ntiles = (L - kbeg + kTileKeys - 1) / kTileKeys;
   const int tps = (ntiles + a.nsplit - 1) / a.nsplit;
   const int t_begin = min(ntiles, split * tps);
   const int t_end = min(ntiles, t_begin + tps);
-  const int my_tiles = t_end - t_begin;
   const float* vbase = a.vc + (size_t)kvh * a.cap * dv;
 
-  if (tid == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(&bars[s], 1);
+  if (tid < nbuf) {
+    mbar_init(&bars[tid], 1);
     mbar_fence_init();
   }
   __syncthreads();
-
   const uint64_t pol = l2_policy_evict_first();
-  // Warp 0 fills stage `slot` with tile `t` (relative to t_begin).
-  auto issue = [&](int t, int slot) {
-    const int key0 = kbeg + (t_begin + t) * kTileKeys;
+  // the buffer's leader lane fills it with tile t (absolute index)
+  auto issue = [&](int t) {
+    const int key0 = kbeg + t * kTileKeys;
     const int nk = min(kTileKeys, L - key0);
-    uint8_t* st = smraw + (size_t)slot * Ly.stage_bytes;
-    float* Ks = reinterpret_cast<float*>(st);
-    float* Vs = Ks + kTileKeys * Ly.kstride;
-    // K: dqk/32 tensor-map boxes of 32 rows (full boxes are counted even past
-    // the cache end, where the copy fills zeros); V: one bulk copy of nk rows
-    if (lane == 0) {
-      mbar_arrive_expect_tx(&bars[slot], (uint32_t)kTileKeys * dqk * 4 + (uint32_t)nk * dv * 4);
-      for (int b = 0; b < dqk / 32; ++b)
-        tma_load_2d(Ks + b * 1024, &a.kmap, &bars[slot], b * 32, kvh * a.cap + key0, pol);
-      bulk_load(Vs, vbase + (size_t)key0 * dv, (uint32_t)nk * dv * 4, &bars[slot], pol);
-    }
+    mbar_arrive_expect_tx(&bars[b], (uint32_t)kTileKeys * dqk * 4 + (uint32_t)nk * dv * 4);
+    for (int bx = 0; bx < dqk / 32; ++bx)
+      tma_load_2d(Kb + bx * 1024, &a.kmap, &bars[b], bx * 32, kvh * a.cap + key0, pol);
+    bulk_load(Vb, vbase + (size_t)key0 * dv, (uint32_t)nk * dv * 4, &bars[b], pol);
   };
-  if (a.prefetch_before_wait && warp == 0)
-    for (int t = 0; t < S && t < my_tiles; ++t) issue(t, t);
+  const int t_first = t_begin + b;
+  if (a.prefetch_before_wait && leader && t_first < t_end) issue(t_first);
   pdl_wait();
   pdl_launch_dependents();
-  if (!a.prefetch_before_wait && warp == 0)
-    for (int t = 0; t < S && t < my_tiles; ++t) issue(t, t);
+  if (!a.prefetch_before_wait && leader && t_first < t_end) issue(t_first);
 
   // ---- queries of this KV head: norm, rotate, pre-scale (log2 domain)
   const float qscale = a.scale * kLog2e;
-  for (int qi = warp; qi < QG; qi += kAttnThreads / 32) {
+  for (int qi = warp; qi < QG; qi += nw) {
     const int r = qi / G, h = kvh * G + qi % G;
     const float* src = a.qp + (size_t)r * q_rows + (size_t)h * dqk * (a.gated ? 2 : 1);
     float* dst = qs + qi * dqk;
@@ -283,7 +307,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const __grid_
   // ---- new keys/values (last split): normalise, rotate, append to the cache
   const bool has_new = split == a.nsplit - 1;
   if (has_new) {
-    for (int r = warp; r < a.m; r += kAttnThreads / 32) {
+    for (int r = warp; r < a.m; r += nw) {
       const int pos = L + r;
       float* kn = newk + r * dqk;
       const float* ksrc = a.kp + (size_t)r * a.nkv * dqk + (size_t)kvh * dqk;
@@ -301,52 +325,81 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const __grid_
       }
     }
   }
-  for (int i = tid; i < kPadQ; i += kAttnThreads) {
-    Ms[i] = kNegBig;
-    ls[i] = 0.f;
-    als[i] = 0.f;
-  }
-  for (int i = tid; i < kPadQ * kTileKeys; i += kAttnThreads) ps[i] = 0.f;
   __syncthreads();
 
-  float oacc[QPT];
+  WarpState<QM, DV> st;
 #pragma unroll
-  for (int k = 0; k < QPT; ++k) oacc[k] = 0.f;
-
-  for (int t = 0; t < my_tiles; ++t) {
-    const int slot = t % S;
-    const bool ok = mbar_wait_bounded(&bars[slot], (uint32_t)((t / S) & 1));
-    if (__syncthreads_or(!ok)) {  // the whole CTA gives up together
-      if (tid == 0) set_dev_error(a.err, kErrMbarTimeout);
-      return;
-    }
-    const float* Ks = reinterpret_cast<const float*>(smraw + (size_t)slot * Ly.stage_bytes);
-    const float* Vs = Ks + kTileKeys * Ly.kstride;
-    const int key0 = kbeg + (t_begin + t) * kTileKeys;
-    attend_tile<QPT>(a, Ks, true, Ly.kstride, Vs, min(kTileKeys, L - key0), key0, qs, ps, red,
-                     Ms, ls, als, oacc, QG, G);
-    if (warp == 0 && t + S < my_tiles) issue(t + S, slot);
+  for (int q = 0; q < QM; ++q) {
+    st.M[q] = kNegBig;
+    st.l[q] = 0.f;
+#pragma unroll
+    for (int i = 0; i < DV; ++i) st.o[q][i] = 0.f;
   }
-  if (has_new)
-    attend_tile<QPT>(a, newk, false, dqk, newv, a.m, L, qs, ps, red, Ms, ls, als, oacc, QG, G);
+  // ---- the buffer's tiles: t_first, t_first + nbuf, ...
+  const int bar_id = 1 + b, bar_cnt = qgroups * 32;
+  bool dead = false;
+  uint32_t phase = 0;
+  for (int t = t_first; t < t_end; t += nbuf) {
+    const bool ok = mbar_wait_bounded(&bars[b], phase);
+    __syncwarp();
+    if (!bar_and(ok, bar_id, bar_cnt)) {  // the buffer's warps give up together
+      if (leader) set_dev_error(a.err, kErrMbarTimeout);
+      dead = true;
+      break;
+    }
+    phase ^= 1u;
+    const int key0 = kbeg + t * kTileKeys;
+    if (nq > 0)
+      warp_tile<QM, DV>(a, st, Kb, true, Vb, min(kTileKeys, L - key0), key0, qs, q0, nq, G, ps,
+                        lane);
+    if (t + nbuf < t_end) {
+      bar_named(bar_id, bar_cnt);  // every reader of the buffer is done with it
+      if (leader) issue(t + nbuf);
+    }
+  }
+  if (has_new && b == nbuf - 1 && nq > 0)
+    warp_tile<QM, DV>(a, st, newk, false, newv, a.m, L, qs, q0, nq, G, ps, lane);
+  if (__syncthreads_or(dead)) return;
+  if (tid < nbuf) mbar_inval(&bars[tid]);
+  __syncthreads();
 
-  // ---- partial of this split: (M, l) pairs and unnormalised outputs
+  // ---- the buffers' states meet in shared memory (the tile buffers are free)
+  float* wstat = reinterpret_cast<float*>(smraw);                 // [nw][QM][2]
+  float* wout = wstat + (size_t)kAttnMaxWarps * kAttnQMax * 2;    // [nw][QM][dv]
+#pragma unroll
+  for (int q = 0; q < QM; ++q) {
+    if (q < nq) {
+      if (lane == 0) {
+        wstat[(warp * QM + q) * 2] = st.M[q];
+        wstat[(warp * QM + q) * 2 + 1] = st.l[q];
+      }
+#pragma unroll
+      for (int c = 0; c < LD::NV; ++c)
+#pragma unroll
+        for (int e = 0; e < LD::VW; ++e)
+          wout[((size_t)warp * QM + q) * dv + LD::dim(lane, c) + e] = st.o[q][c * LD::VW + e];
+    }
+  }
+  __syncthreads();
   const size_t pidx = (size_t)(kvh * a.nsplit + split) * QG;
   float* part_o = a.part + attn_part_o_offset(a.nkv, a.nsplit, QG);
-  {
-    const int nsl = kAttnThreads / dv;
-    const int d = tid % dv, q0 = tid / dv;
-    if (q0 < nsl) {
-#pragma unroll
-      for (int k = 0; k < QPT; ++k) {
-        const int q = q0 + k * nsl;
-        if (q < QG) part_o[(pidx + q) * dv + d] = oacc[k];
-      }
+  for (int it = tid; it < QG * dv; it += nthreads) {
+    const int q = it / dv, d = it - q * dv;
+    const int g = q / qpw, ql = q - g * qpw;
+    float M = kNegBig;
+    for (int bb = 0; bb < nbuf; ++bb) M = fmaxf(M, wstat[((bb * qgroups + g) * QM + ql) * 2]);
+    float l = 0.f, o = 0.f;
+    for (int bb = 0; bb < nbuf; ++bb) {
+      const int w = bb * qgroups + g;
+      const float f = exp2f(wstat[(w * QM + ql) * 2] - M);
+      l += f * wstat[(w * QM + ql) * 2 + 1];
+      o += f * wout[((size_t)w * QM + ql) * dv + d];
     }
-  }
-  if (tid < QG) {
-    a.part[(pidx + tid) * 2 + 0] = Ms[tid];
-    a.part[(pidx + tid) * 2 + 1] = ls[tid];
+    part_o[(pidx + q) * dv + d] = o;
+    if (d == 0) {
+      a.part[(pidx + q) * 2 + 0] = M;
+      a.part[(pidx + q) * 2 + 1] = l;
+    }
   }
   __threadfence();
   __syncthreads();
@@ -358,63 +411,82 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const __grid_
   if (!last) return;
   __threadfence();
 
-  // ---- merge (last CTA of this KV head); the stage ring is free now
+  // ---- merge across splits (last CTA of this KV head)
   const int ns = a.nsplit;
   float* wsm = reinterpret_cast<float*>(smraw);        // [ns][QG] split weights
   float* lsm = wsm + ns * QG;                          // [ns][QG] split denominators
   float* fin = lsm + ns * QG;                          // [QG][dv]
   const size_t base = (size_t)kvh * ns * QG;
-  // all (M, l) pairs in one parallel pass, so no loop below waits on memory
-  for (int i = tid; i < ns * QG; i += kAttnThreads) {
+  const int dv4 = dv / 4;
+  const int items = QG * dv4;
+  // gate values of this thread's first item, loaded alongside the (M, l) pairs
+  float4 gate = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (a.gated && tid < items) {
+    const int qi = tid / dv4, d4 = tid - qi * dv4;
+    const int r = qi / G, h = kvh * G + qi % G;
+    gate = *reinterpret_cast<const float4*>(a.qp + (size_t)r * q_rows + (size_t)h * dqk * 2 + dqk +
+                                            d4 * 4);
+  }
+  for (int i = tid; i < ns * QG; i += nthreads) {
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part) + base + i);
     wsm[i] = ml.x;
     lsm[i] = ml.y;
   }
   __syncthreads();
-  if (tid < QG) {
-    const int h = kvh * G + tid % G;
+  // one warp per query row: lanes over the splits
+  for (int q = warp; q < QG; q += nw) {
+    const int h = kvh * G + q % G;
     const float sinkl2 = a.sinks ? a.sinks[h] * kLog2e : kNegBig;
     float M = sinkl2;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, wsm[s * QG + tid]);
-    float den = a.sinks ? exp2f(sinkl2 - M) : 0.f;
-    for (int s = 0; s < ns; ++s) den += exp2f(wsm[s * QG + tid] - M) * lsm[s * QG + tid];
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, wsm[s * QG + q]);
+    M = warp_max(M);
+    float den = 0.f;
+    for (int s = lane; s < ns; s += 32) den += exp2f(wsm[s * QG + q] - M) * lsm[s * QG + q];
+    den = warp_sum(den) + (a.sinks ? exp2f(sinkl2 - M) : 0.f);
     const float inv = den > 0.f ? 1.f / den : 0.f;
-    for (int s = 0; s < ns; ++s) wsm[s * QG + tid] = exp2f(wsm[s * QG + tid] - M) * inv;
+    __syncwarp();
+    for (int s = lane; s < ns; s += 32) wsm[s * QG + q] = exp2f(wsm[s * QG + q] - M) * inv;
   }
   __syncthreads();
-  const int dv4 = dv / 4;
-  for (int it = tid; it < QG * dv4; it += kAttnThreads) {
+  for (int it = tid; it < items; it += nthreads) {
     const int qi = it / dv4, d4 = it - qi * dv4;
     const float4* po = reinterpret_cast<const float4*>(part_o + (base + qi) * dv) + d4;
     const size_t sstride = (size_t)QG * dv4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int s = 0;
-    for (; s + 4 <= ns; s += 4) {
-      const float4 v0 = __ldcg(po + (size_t)s * sstride);
-      const float4 v1 = __ldcg(po + (size_t)(s + 1) * sstride);
-      const float4 v2 = __ldcg(po + (size_t)(s + 2) * sstride);
-      const float4 v3 = __ldcg(po + (size_t)(s + 3) * sstride);
-      const float w0 = wsm[s * QG + qi], w1 = wsm[(s + 1) * QG + qi];
-      const float w2 = wsm[(s + 2) * QG + qi], w3 = wsm[(s + 3) * QG + qi];
-      acc.x += w0 * v0.x + w1 * v1.x + w2 * v2.x + w3 * v3.x;
-      acc.y += w0 * v0.y + w1 * v1.y + w2 * v2.y + w3 * v3.y;
-      acc.z += w0 * v0.z + w1 * v1.z + w2 * v2.z + w3 * v3.z;
-      acc.w += w0 * v0.w + w1 * v1.w + w2 * v2.w + w3 * v3.w;
+    for (; s + 8 <= ns; s += 8) {  // eight independent loads in flight
+      float4 v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(po + (size_t)(s + u) * sstride);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float w = wsm[(s + u) * QG + qi];
+        acc.x = fmaf(w, v[u].x, acc.x);
+        acc.y = fmaf(w, v[u].y, acc.y);
+        acc.z = fmaf(w, v[u].z, acc.z);
+        acc.w = fmaf(w, v[u].w, acc.w);
+      }
     }
     for (; s < ns; ++s) {
       const float4 v = __ldcg(po + (size_t)s * sstride);
       const float w = wsm[s * QG + qi];
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
     }
     float o[4] = {acc.x, acc.y, acc.z, acc.w};
     if (a.gated) {
-      const int r = qi / G, h = kvh * G + qi % G;
-      const float* g = a.qp + (size_t)r * q_rows + (size_t)h * dqk * 2 + dqk + d4 * 4;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) o[e] = o[e] / (1.f + __expf(-g[e]));
+      float4 g = gate;
+      if (it != tid) {
+        const int r = qi / G, h = kvh * G + qi % G;
+        g = *reinterpret_cast<const float4*>(a.qp + (size_t)r * q_rows + (size_t)h * dqk * 2 +
+                                             dqk + d4 * 4);
+      }
+      o[0] = o[0] / (1.f + __expf(-g.x));
+      o[1] = o[1] / (1.f + __expf(-g.y));
+      o[2] = o[2] / (1.f + __expf(-g.z));
+      o[3] = o[3] / (1.f + __expf(-g.w));
     }
 #pragma unroll
     for (int e = 0; e < 4; ++e) fin[qi * dv + d4 * 4 + e] = o[e];
@@ -423,7 +495,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const __grid_
   // fp32 output and packed copy: octets of (row, head, dims)
   const int oct_per_q = dv / 8;
   const int total_oct = QG * oct_per_q;
-  for (int o0 = 0; o0 < total_oct; o0 += kAttnThreads) {
+  for (int o0 = 0; o0 < total_oct; o0 += nthreads) {
     const int oi = o0 + tid;
     float2 sum = make_float2(0.f, 0.f);
     int r = 0, k = 0;
@@ -436,8 +508,9 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const __grid_
 #pragma unroll
       for (int i = 0; i < 8; ++i) v[i] = fin[qi * dv + oc * 8 + i];
       if (a.out) {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a.out[(size_t)r * a.nh * dv + k + i] = v[i];
+        float4* dst = reinterpret_cast<float4*>(a.out + (size_t)r * a.nh * dv + k);
+        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
+        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
       }
       if (a.out_xp) {
         uint4 hi, lo;
@@ -448,7 +521,7 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const __grid_
       }
     }
     if (a.out_xp) {
-      // the four octets of a group are adjacent (dv % 32 == 0, kAttnThreads % 4 == 0)
+      // the four octets of a group are adjacent (dv % 32 == 0, blockDim % 32 == 0)
       sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 1);
       sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
       sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
@@ -459,13 +532,24 @@ __global__ void __launch_bounds__(kAttnThreads) attn_decode_kernel(const __grid_
   if (tid == 0) a.counters[kvh] = 0u;
 }
 
-int attn_splits(int nkv, int keys) {
-  const int target = sm_count();  // about one CTA per SM
-  int ns = (target + nkv - 1) / nkv;
-  const int max_by_tiles = (keys + kTileKeys - 1) / kTileKeys;  // at least one tile per split
-  if (ns > max_by_tiles) ns = max_by_tiles;
-  if (ns < 1) ns = 1;
-  return ns;
+// ------------------------------------------------------------------ host side
+static int ceil_div(int a, int b) { return (a + b - 1) / b; }
+
+// Upper bound of the split count for `cached` keys in the window (sizes the
+// partials); attn_splits never exceeds it and it grows with `cached`.
+int attn_splits_bound(int nkv, int cached) {
+  const int ntiles = ceil_div(cached, kTileKeys);
+  int ns = ceil_div(sm_count(), nkv);  // about one CTA per SM
+  if (ns > ntiles) ns = ntiles;
+  return ns < 1 ? 1 : ns;
+}
+
+int attn_splits(int nkv, int cached) {
+  const int ntiles = ceil_div(cached, kTileKeys);
+  const int bound = attn_splits_bound(nkv, cached);
+  if (ntiles == 0) return 1;
+  const int tps = ceil_div(ntiles, bound);
+  return ceil_div(ntiles, tps);  // no split without cached tiles
 }
 
 size_t attn_part_bytes(int nkv, int nsplit, int q_per_kv, int dv) {
@@ -473,22 +557,33 @@ size_t attn_part_bytes(int nkv, int nsplit, int q_per_kv, int dv) {
          sizeof(float);
 }
 
-template <int QPT>
+// Query rows per warp (the kernel's template bound): at most kAttnQMax and
+// at most 32 state floats per lane.
+static int attn_qmax(int dv) { return dv <= 128 ? kAttnQMax : 4; }
+
+bool attn_supported(int QG, int dqk, int dv, int m) {
+  const int qg = ceil_div(QG, attn_qmax(dv));
+  if (qg > kAttnMaxWarps) return false;
+  const AttnLayout Ly = attn_layout(dqk, dv, QG, m, 1, qg);
+  return Ly.total + kAttnSlack <= kAttnSmemLimit;
+}
+
+template <int QM, int DV>
 static cudaError_t launch_attn_t(const AttnParams& a, size_t smem, cudaStream_t st) {
   static_assert(sizeof(AttnParams) <= 4096, "kernel parameters fit the classic limit");
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<QPT>,
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<QM, DV>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kAttnSmemMax + 1024);
+                                         (int)kAttnSmemLimit);
     if (e != cudaSuccess) return e;
     configured_dev = dev;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(a.nsplit, a.nkv);
-  cfg.blockDim = dim3(kAttnThreads);
+  cfg.blockDim = dim3(a.nbuf * a.qgroups * 32);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr;
@@ -496,7 +591,22 @@ static cudaError_t launch_attn_t(const AttnParams& a, size_t smem, cudaStream_t 
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<QPT>, a);
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<QM, DV>, a);
+}
+
+// Query rows per warp: 8 for head_dim_v <= 128, else 4 (at most 32 state floats per lane).
+static cudaError_t launch_attn_dv(const AttnParams& a, size_t smem, cudaStream_t st) {
+  switch (a.dv / 32) {
+    case 1: return launch_attn_t<8, 1>(a, smem, st);
+    case 2: return launch_attn_t<8, 2>(a, smem, st);
+    case 3: return launch_attn_t<8, 3>(a, smem, st);
+    case 4: return launch_attn_t<8, 4>(a, smem, st);
+    case 5: return launch_attn_t<4, 5>(a, smem, st);
+    case 6: return launch_attn_t<4, 6>(a, smem, st);
+    case 7: return launch_attn_t<4, 7>(a, smem, st);
+    case 8: return launch_attn_t<4, 8>(a, smem, st);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
@@ -504,17 +614,33 @@ cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
   cudaError_t ke = encode_f32_tile_map(&a.kmap, a.kc, (uint64_t)a.nkv * a.cap, (uint64_t)a.dqk);
   if (ke != cudaSuccess) return ke;
   const int QG = (a.nh / a.nkv) * a.m;
-  const AttnLayout Ly = attn_layout(a.dqk, a.dv, QG, a.m);
-  // the merge reuses the stage ring: split weights and the finished rows
+  // warps per buffer: the fewest that keep each warp within attn_qmax rows
+  const int qmax = attn_qmax(a.dv);
+  a.qgroups = ceil_div(QG, qmax);
+  // buffers: as many as the split has tiles, within the warp and smem limits
+  const int kbeg = a.window > 0 ? (a.L + 1 - a.window > 0 ? a.L + 1 - a.window : 0) : 0;
+  const int ntiles = ceil_div(a.L - kbeg, kTileKeys);
+  const int tps = ntiles > 0 ? ceil_div(ntiles, a.nsplit) : 1;
+  int nbuf = tps;
+  if (nbuf > kAttnMaxWarps / a.qgroups) nbuf = kAttnMaxWarps / a.qgroups;
+  if (nbuf > 15) nbuf = 15;  // named barriers 1..15 (0 is the CTA barrier)
+  while (nbuf > 1 &&
+         attn_layout(a.dqk, a.dv, QG, a.m, nbuf, nbuf * a.qgroups).total + kAttnSlack >
+             kAttnSmemLimit)
+    --nbuf;
+  if (nbuf < 1) nbuf = 1;
+  a.nbuf = nbuf;
+  const int nw = nbuf * a.qgroups;
+  const AttnLayout Ly = attn_layout(a.dqk, a.dv, QG, a.m, nbuf, nw);
+  // the tile buffers are reused for the buffers' states, then the merge
+  const size_t combine = ((size_t)kAttnMaxWarps * kAttnQMax * 2 + (size_t)nw * qmax * a.dv) * 4;
   const size_t merge = (size_t)a.nsplit * QG * 8 + (size_t)QG * a.dv * 4;
-  const size_t smem = Ly.total > merge ? Ly.total : merge;
-  if (smem > (size_t)kAttnSmemMax + 1024) return cudaErrorInvalidValue;
-  const int nsl = kAttnThreads / a.dv;
-  const int need = (QG + nsl - 1) / nsl;
-  if (need <= 1) return launch_attn_t<1>(a, smem, st);
-  if (need <= 2) return launch_attn_t<2>(a, smem, st);
-  if (need <= 4) return launch_attn_t<4>(a, smem, st);
-  return launch_attn_t<8>(a, smem, st);
+  size_t smem = Ly.total;
+  if (combine > smem) smem = combine;
+  if (merge > smem) smem = merge;
+  smem += kAttnSlack;
+  if (smem > kAttnSmemLimit) return cudaErrorInvalidValue;
+  return launch_attn_dv(a, smem, st);
 }
 
 }  // namespace mtp

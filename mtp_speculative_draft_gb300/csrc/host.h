@@ -81,13 +81,20 @@ struct alignas(64) AttnParams {
   float* part;         // partials
   unsigned* counters;  // [nkv]
   int nsplit;
+  int nbuf;            // tile buffers per CTA (set by launch_attn)
+  int qgroups;         // warps per buffer, each with a slice of the query rows (set by launch_attn)
   // 1: stream cached rows before waiting on the previous kernel.  Only valid
   // when that kernel signals its dependents after its own wait (so every
   // earlier kernel, including the step that wrote those rows, has finished).
   int prefetch_before_wait;
   int* err;
 };
-int attn_splits(int nkv, int keys);
+// Split count for `cached` keys inside the window, and an upper bound of it
+// that grows with `cached` (sizes the partials).
+int attn_splits(int nkv, int cached);
+int attn_splits_bound(int nkv, int cached);
+// Whether one CTA can serve QG query rows of the given head dims and m.
+bool attn_supported(int QG, int dqk, int dv, int m);
 size_t attn_part_bytes(int nkv, int nsplit, int q_per_kv, int dv);
 cudaError_t launch_attn(const AttnParams& a, cudaStream_t st);
 
