@@ -23,7 +23,8 @@
  * Conventions for every entry point:
  *  - Pointers named d_* or documented as device are device pointers owned by
  *    the caller; host pointers are named h_* or are descriptor structs.  The
- *    library never allocates device memory and keeps no state between calls.
+ *    library never allocates device memory and keeps no state between calls
+ *    (attn_decode_sink_noalloc alone keeps a static device scratch).
  *  - All work is enqueued on `stream` (a cudaStream_t, NULL = legacy
  *    default stream); no call synchronises the device, so calls can be
  *    captured into a CUDA graph (tensor maps are encoded on the host at
@@ -162,6 +163,31 @@ mtp_status attn_decode_sink(const mtp_attn_geom *g, const float *d_qp, const flo
                             const float *d_rope, const float *d_sinks, float *d_k_cache,
                             float *d_v_cache, int32_t cache_len, int32_t cache_cap, int32_t m,
                             float *d_out, void *d_ws, size_t ws_bytes, void *stream);
+
+/* attn_decode_sink_noalloc: attn_decode_sink with the library's own static
+ * device scratch (1 MiB, a file-scope __device__ array) in place of d_ws.
+ * The draft-layer method has no counterpart of this call: it exists for
+ * callers that hold no device memory to lend, such as a host runtime whose
+ * device memory all sits in its own pools, or a plugin interface whose
+ * signature carries no workspace.  It allocates no device memory.
+ *  - The first call on a device looks up the scratch address and clears its
+ *    header with a synchronous cudaMemset; make that first call before any
+ *    stream capture.  Later calls enqueue a clear of the completion counters
+ *    on `stream`, then the same launch as attn_decode_sink.
+ *  - Geometries whose scratch (attn_decode_sink_workspace_bytes) exceeds
+ *    1 MiB return MTP_ERR_WORKSPACE without launching anything.
+ *  - Calls that overlap on one device share the scratch and race: order
+ *    them (one stream, or events).
+ *  - A device-side wait that gives up records its code in the scratch
+ *    header, which this call does not expose; use attn_decode_sink with a
+ *    workspace where that status is needed.
+ * Arguments, layouts and other errors as attn_decode_sink. */
+mtp_status attn_decode_sink_noalloc(const mtp_attn_geom *g, const float *d_qp,
+                                    const float *d_kp, const float *d_vp,
+                                    const float *d_q_norm, const float *d_k_norm,
+                                    const float *d_rope, const float *d_sinks, float *d_k_cache,
+                                    float *d_v_cache, int32_t cache_len, int32_t cache_cap,
+                                    int32_t m, float *d_out, void *stream);
 
 /* ------------------------------------------------------------------------
  * lmhead_argmax: y_n = RMSNorm(y)*norm_w (or y when norm_w is NULL);

@@ -76,6 +76,8 @@ EXPORTS = {
     "attn_decode_sink_workspace_bytes": (sz, [C.POINTER(AttnGeom), i32, i32]),
     "attn_decode_sink": (C.c_int, [C.POINTER(AttnGeom), vp, vp, vp, vp, vp, vp, vp, vp, vp, i32,
                                    i32, i32, vp, vp, sz, vp]),
+    "attn_decode_sink_noalloc": (C.c_int, [C.POINTER(AttnGeom), vp, vp, vp, vp, vp, vp, vp, vp,
+                                           vp, i32, i32, i32, vp, vp]),
     "lmhead_argmax_workspace_bytes": (sz, [i32, i32]),
     "lmhead_argmax": (C.c_int, [vp, vp, f32, C.POINTER(Affine4), vp, vp, vp, vp, vp, sz, vp]),
     "moe_ffn_workspace_bytes": (sz, [C.POINTER(MoeWeights), i32]),

@@ -97,6 +97,16 @@ def attn_decode_sink(g: AttnGeom, qp, kp, vp, q_norm, k_norm, rope, sinks, k_cac
     return ws
 
 
+def attn_decode_sink_noalloc(g: AttnGeom, qp, kp, vp, q_norm, k_norm, rope, sinks, k_cache,
+                             v_cache, cache_len, cache_cap, m, out, stream=None):
+    """attn_decode_sink on the library's static device scratch (no workspace argument)."""
+    check(L.load().attn_decode_sink_noalloc(C.byref(g), _p(qp), _p(kp), _p(vp), _p(q_norm),
+                                            _p(k_norm), _p(rope), _p(sinks), _p(k_cache),
+                                            _p(v_cache), cache_len, cache_cap, m, _p(out),
+                                            _stream(stream)),
+          "attn_decode_sink_noalloc")
+
+
 def lmhead_argmax(y, norm_w, eps, w: Affine4, token, value, logits=None, y_normed=None, ws=None,
                   stream=None):
     lib = L.load()

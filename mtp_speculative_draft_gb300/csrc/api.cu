@@ -869,3 +869,78 @@ mtp_status mtp_draft_chain(const mtp_layer_desc* layers, int32_t n_layers, const
 }
 
 }  // extern "C"
+
+// ------------------------------------------------ attention without a workspace
+namespace mtp {
+
+// Scratch of attn_decode_sink_noalloc: the workspace header (device error
+// word + completion counters) followed by the split partials.  1 MiB holds
+// the partials of every geometry up to nkv * splits * (G*m) * (dv + 2)
+// floats of about 255 K, e.g. 8 KV heads x 19 splits x 5 rows x 130 floats
+// (395 KB) for a 40/8-head, 128-dim cache of 4096 rows.
+constexpr size_t kNoallocScratchBytes = size_t(1) << 20;
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
+constexpr int kNoallocMaxDevices = 64;
+
+// Device address of the static scratch on the current device.  The first
+// call on a device looks the address up and clears the header (a synchronous
+// cudaMemset); later calls only read the cached address.
+static mtp_status noalloc_scratch(void** out) {
+  static std::mutex mu;
+  static void* addr[kNoallocMaxDevices] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode_sink_noalloc: cudaGetDevice");
+  if (dev < 0 || dev >= kNoallocMaxDevices)
+    return fail(MTP_ERR_UNSUPPORTED, "attn_decode_sink_noalloc: device ordinal above 63");
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_sink_noalloc: cudaGetSymbolAddress");
+    e = cudaMemset(p, 0, sizeof(WsHeader));
+    if (e != cudaSuccess) return cuda_fail(e, "attn_decode_sink_noalloc: clearing the scratch header");
+    addr[dev] = p;
+  }
+  *out = addr[dev];
+  return MTP_OK;
+}
+
+}  // namespace mtp
+
+extern "C" {
+
+// Same operation as attn_decode_sink, with the library's static scratch in
+// place of a caller workspace, for callers that hold no device memory to
+// lend: a host runtime whose device memory all sits in its own pools, or a
+// plugin interface whose signature has no workspace argument.  It allocates
+// no device memory.  The completion counters are cleared on `stream` before
+// every launch; concurrent or overlapping calls on one device share the
+// scratch and race, so they must be ordered (one stream, or events).
+mtp_status attn_decode_sink_noalloc(const mtp_attn_geom* g, const float* d_qp, const float* d_kp,
+                                    const float* d_vp, const float* d_q_norm,
+                                    const float* d_k_norm, const float* d_rope,
+                                    const float* d_sinks, float* d_k_cache, float* d_v_cache,
+                                    int32_t cache_len, int32_t cache_cap, int32_t m,
+                                    float* d_out, void* stream) {
+  mtp_status s = check_geom(g, m);
+  if (s != MTP_OK) return s;
+  if (cache_len < 0) return fail(MTP_ERR_INVALID_ARG, "attn_decode_sink_noalloc: bad cache length");
+  const size_t need = attn_decode_sink_workspace_bytes(g, m, cache_len);
+  if (need > kNoallocScratchBytes)
+    return fail(MTP_ERR_WORKSPACE,
+                "attn_decode_sink_noalloc: this geometry needs " + std::to_string(need) +
+                    " bytes of scratch, the static scratch holds " +
+                    std::to_string(kNoallocScratchBytes) + " (use attn_decode_sink)");
+  void* scratch = nullptr;
+  s = noalloc_scratch(&scratch);
+  if (s != MTP_OK) return s;
+  cudaError_t e = cudaMemsetAsync(header(scratch)->counters + kCntAttn, 0, sizeof(unsigned) * 64,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attn_decode_sink_noalloc: clearing the counters");
+  return attn_decode_sink(g, d_qp, d_kp, d_vp, d_q_norm, d_k_norm, d_rope, d_sinks, d_k_cache,
+                          d_v_cache, cache_len, cache_cap, m, d_out, scratch,
+                          kNoallocScratchBytes, stream);
+}
+
+}  // extern "C"
