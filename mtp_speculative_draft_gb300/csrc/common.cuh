@@ -122,22 +122,15 @@ __device__ __forceinline__ void ldmatrix_x4(uint32_t& r0, uint32_t& r1, uint32_t
                : "r"(addr));
 }
 
-// 4-bit codes -> f16x2 with the code in the mantissa of 1024 (exponent 2^10,
-// unit LSB): bits 0..3 and 16..19 of `w` give (1024 + c, 1024 + c');
-// bits 4..7 and 20..23 give (1024 + 16c, 1024 + 16c').  One LOP3 each.
-__device__ __forceinline__ uint32_t codes_lo_f16x2(uint32_t w) {
-  return (w & 0x000F000Fu) | 0x64006400u;
-}
-__device__ __forceinline__ uint32_t codes_hi_f16x2(uint32_t w) {
-  return (w & 0x00F000F0u) | 0x64006400u;
-}
-// Removes the 1024 bias of both halves (exact: 1024 + c and 1024 + 16c are
-// representable, so the difference is the exact code or 16 * code).
-__device__ __forceinline__ uint32_t unbias_f16x2(uint32_t v) {
-  uint32_t r;
-  asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(v), "r"(0x64006400u));
-  return r;
-}
+// 4-bit codes -> f16x2 as subnormal halves: a half with a zero exponent
+// field is mantissa * 2^-24, so masking alone gives exact values with no
+// offset.  Bits 0..3 and 16..19 of `w` give (c * 2^-24, c' * 2^-24); bits
+// 4..7 and 20..23 give (16c * 2^-24, 16c' * 2^-24).  One LOP3 each; the
+// 2^24 is restored in f32 after the tensor-core sums.
+constexpr float kCodeScale = 16777216.f;   // 2^24
+constexpr float kCodeUnscale = 1.f / 16777216.f;
+__device__ __forceinline__ uint32_t codes_lo_f16x2(uint32_t w) { return w & 0x000F000Fu; }
+__device__ __forceinline__ uint32_t codes_hi_f16x2(uint32_t w) { return w & 0x00F000F0u; }
 
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll

@@ -11,15 +11,16 @@
 // 1 KB of biases.  Codes go shared -> registers with ldmatrix, which hands
 // lane (g, t) word t of a group for rows g and g+8 -- exactly the
 // m16n8k16 A-fragment slots once the k order inside a group is permuted.
-// Codes become f16x2 registers with one LOP3 each and no shift for two of
-// the four nibble pairs of a word: nibbles at bits 0-3/16-19 give 1024 + c,
-// nibbles at bits 4-7/20-23 give 1024 + 16c (both exact in f16).  The
-// 1024 bias is then removed with one f16x2 subtraction (exact), so the
-// tensor pipe accumulates sum(code * x) directly.  The activations are split
-// into f16 hi + lo parts (about 22 bits), the slots that meet a 16c code
-// carry x/16, and the products run on the tensor pipe with f32
-// accumulation.  The per-group scale and bias are applied in f32 after each
-// group:  y += s * D + b * sum(x).
+// Codes become f16x2 registers with one mask (LOP3) each and no shift for
+// two of the four nibble pairs of a word: kept in place with a zero exponent
+// field they are exact subnormal halves, c * 2^-24 (bits 0-3/16-19) and
+// 16c * 2^-24 (bits 4-7/20-23), so the tensor pipe accumulates
+// 2^-24 * sum(code * x) with no offset term.  The activations are split into
+// f16 hi + lo parts (about 22 bits), the slots that meet a 16c code carry
+// x/16, and the products run on the tensor pipe with f32 accumulation.  The
+// per-group scale and bias are applied in f32 after each group, with the
+// group sums pre-scaled by 2^-24:  y' += s * D' + b * 2^-24 sum(x), and the
+// finished tile is multiplied by 2^24 (exact).
 // Activations arrive pre-packed ("xpack") in the B-fragment order with the
 // per-group sums precomputed by the producer kernel.
 #pragma once
@@ -34,9 +35,8 @@ namespace mtp {
 // hl = 0 holds the f16 "hi" parts, 1 the "lo" parts, of the eight values
 // x[c][32g + 8t + p] as f16x2 words (first element in the low half):
 //   word 0: (p0, p4)   word 1: (p1/16, p5/16)   word 2: (p2, p6)   word 3: (p3/16, p7/16)
-// xs[g][c] = (sum of the represented x over the group,
-//             1024 * sum of the represented stored values) -- the second
-// component is what the +1024 code bias adds to the tensor-core sum.
+// xs[g][c] = (2^-24 * sum of the represented x over the group, 0): the sum
+// meets the bias b at the scale of the tensor-core sums (see above).
 // Activations must lie within the f16 range (|x| < 65504).
 __host__ __device__ inline int xpack_groups(int K) { return (K / kGroup + 7) / 8 * 8; }
 __host__ __device__ inline size_t xpack_xs_offset(int m, int K) {
@@ -74,7 +74,7 @@ __device__ __forceinline__ float2 pack8(const float v[8], uint4& hi, uint4& lo) 
   };
   hi = make_uint4(pk(h[0], h[4]), pk(h[1], h[5]), pk(h[2], h[6]), pk(h[3], h[7]));
   lo = make_uint4(pk(l[0], l[4]), pk(l[1], l[5]), pk(l[2], l[6]), pk(l[3], l[7]));
-  return make_float2(sa + 16.f * sb, 1024.f * (sa + sb));
+  return make_float2((sa + 16.f * sb) * kCodeUnscale, 0.f);
 }
 
 // Stores element p (0..7) of an (g, c, t) octet: word p % 4, half p / 4.
@@ -89,7 +89,7 @@ __device__ __forceinline__ float2 xp_store_elem(uint4* xp, int m, int g, int c, 
   const size_t w_lo = (size_t)xp_index(g, c, t, 1, m) * 8 + (p & 3) * 2 + (p >> 2);
   base[w_hi] = __half_as_ushort(h);
   base[w_lo] = __half_as_ushort(l);
-  return make_float2(bslot ? 16.f * r : r, 1024.f * r);
+  return make_float2((bslot ? 16.f * r : r) * kCodeUnscale, 0.f);
 }
 
 // ------------------------------------------------------------------ params
@@ -463,16 +463,16 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
           for (int h = 0; h < 2; ++h) {
             const uint32_t wa = w[2 * h], wb = w[2 * h + 1];
             const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-            // exact codes (and 16 * codes) as f16: the accumulator only ever
-            // holds sums of code * x, so its rounding stays at that scale
-            const uint32_t a0 = unbias_f16x2(codes_lo_f16x2(wa));
-            const uint32_t a1 = unbias_f16x2(codes_lo_f16x2(wb));
-            const uint32_t a2 = unbias_f16x2(codes_hi_f16x2(wa));
-            const uint32_t a3 = unbias_f16x2(codes_hi_f16x2(wb));
-            const uint32_t a4 = unbias_f16x2(codes_lo_f16x2(wa8));
-            const uint32_t a5 = unbias_f16x2(codes_lo_f16x2(wb8));
-            const uint32_t a6 = unbias_f16x2(codes_hi_f16x2(wa8));
-            const uint32_t a7 = unbias_f16x2(codes_hi_f16x2(wb8));
+            // exact codes (and 16 * codes) times 2^-24 as f16: the accumulator
+            // only ever holds sums of code * x, so its rounding stays at that scale
+            const uint32_t a0 = codes_lo_f16x2(wa);
+            const uint32_t a1 = codes_lo_f16x2(wb);
+            const uint32_t a2 = codes_hi_f16x2(wa);
+            const uint32_t a3 = codes_hi_f16x2(wb);
+            const uint32_t a4 = codes_lo_f16x2(wa8);
+            const uint32_t a5 = codes_lo_f16x2(wb8);
+            const uint32_t a6 = codes_hi_f16x2(wa8);
+            const uint32_t a7 = codes_hi_f16x2(wb8);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
               float* dd = d[mi][rt][h][nt];
@@ -609,6 +609,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
               fin[0][mi][rt][nt][e] = acc[mi][rt][nt][e];
               acc[mi][rt][nt][e] = 0.f;
             }
+    }
+    // undo the 2^-24 of the subnormal codes (exact)
+#pragma unroll
+    for (int um = 0; um < UM; ++um) {
+      float* fw = &fin[um][0][0][0][0];
+#pragma unroll
+      for (int q = 0; q < NMAT * 2 * NT * 4; ++q) fw[q] *= kCodeScale;
     }
 
     // ---------------------------------------------------------- epilogue
