@@ -124,9 +124,6 @@ size_t gemv_scratch_part_bytes() {
 #ifndef MTP_GEMV_STAGES
 #define MTP_GEMV_STAGES 2
 #endif
-#ifndef MTP_GEMV_STAGE_X1
-#define MTP_GEMV_STAGE_X1 0
-#endif
 
 template <int NMAT, int NT, int EPI, int XM, bool C1, bool PAIRED = false>
 static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
@@ -174,7 +171,7 @@ cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
   const int m = p.m;
   // activations staged per stage by bulk copy for up to 4 columns
   const bool c1 = (m == 1);
-  constexpr int X1 = MTP_GEMV_STAGE_X1 ? 1 : 0;
+  constexpr int X1 = 1;  // one activation row: staged with each weight stage
   if (epi == kEpiArgmax) {
     if (m != 1) return cudaErrorInvalidValue;
     return launch_gemv_t<1, 1, kEpiArgmax, X1, true>(p, tiles, sc, st);

@@ -256,6 +256,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
   // units (one matrix in flight per warp); their partial sums meet in the
   // split-K reduction.
   constexpr int UM = PAIRED ? 2 : 1;
+  static_assert(!C1 || (XM == 1 && NMAT == 1 && NT == 1), "one-row layout: staged activations");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of each codes tile is required by the 128B swizzle.
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -281,6 +282,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
   const int total_tiles = p.seg[p.nseg - 1].tile_end;
   const int units = total_tiles * UM * ksplit;
 
+  __shared__ __align__(16) uint4 zero_b[16];  // B fragments of lanes outside their group's column
+  if constexpr (C1) {
+    if (threadIdx.x < 16) zero_b[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+    __syncthreads();
+  }
   if (lane == 0) {
     for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
@@ -366,6 +372,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
   const uint32_t ld_c = (uint32_t)(((mtx >> 1) ^ ri) << 4);
   const int sb_lane = gid * 8;  // float offset of row gid in a [32][8] scale tile
 
+  // one-row layout (C1): code chunks of this lane's groups, the B-fragment
+  // source of this lane (its group's hi or lo part, or zeros)
+  const int a_chunk[2] = {((2 * tq) ^ gid) << 4, ((2 * tq + 1) ^ gid) << 4};
+  const bool b_active = (gid >> 1) == tq;
+  const int b_off = (gid >> 1) * 2 * 8 + (gid & 1);
   uint4 bh[2][NT], bl[2][NT];      // activation fragments of the next pair of groups
   float2 xs0[2][NT], xs1[2][NT];
   bool b_ready = false;
@@ -394,13 +405,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
         const int j = 2 * jp + h;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          if constexpr (C1) {
-            const uint4* src = xp_st + j * 8 + tq * 2;
-            bh[h][nt] = __ldg(src);
-            bl[h][nt] = __ldg(src + 1);
-            x0[h][nt] = __ldg(xs_st + j);
-            x1[h][nt] = x0[h][nt];
-          } else {
+          {
             bh[h][nt] = make_uint4(0, 0, 0, 0);
             bl[h][nt] = make_uint4(0, 0, 0, 0);
             x0[h][nt] = make_float2(0.f, 0.f);
@@ -437,88 +442,145 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     // last pair of a stage loads the first pair of the next stage when it
     // continues the same unit.  Activations are zero-padded to whole stages
     // of 8 groups.
-    if (!b_ready) load_b(0, bh, bl, xs0, xs1);
-    // (staged activations live in the stage's own buffer: no early load then)
-    const bool next_same_unit = XM == 0 && cc.ks + 1 < cc.ke;
-#pragma unroll 1
-    for (int jp = 0; jp < 4; ++jp) {
-      const uint32_t coff = ((uint32_t)jp << 5) ^ ld_c;
-      float d[NMAT][2][2][NT][4];
-      float sx0[2][NT], sx1[2][NT];
+    if constexpr (C1) {
+      // One activation row.  The eight MMA columns carry (group, hi/lo)
+      // pairs instead of activation columns: in set st (0, 1) lane (gid, tq)
+      // feeds k-slots {2tq, 2tq+1, 2tq+8, 2tq+9} with codes of group
+      // 2tq + st of rows gid and gid + 8, and column 2j + h of B holds part h
+      // (hi, lo) of that group's activations in lane j's slots (zeros in the
+      // others).  So D[row][2tq + h] is part h of the row's product with
+      // group 2tq + st, and each lane applies the scales of its own groups.
+      const uint8_t* ct = code_base + slot * kCode;
+      const uint4* xps = reinterpret_cast<const uint4*>(rs + NMAT * 2048);
+      const float4 sxv =
+          *reinterpret_cast<const float4*>(rs + NMAT * 2048 + XM * 1024 + tq * 16);
+      const uint4* bsrc = b_active ? xps + b_off : zero_b;
+      uint4 B[2][4];
 #pragma unroll
-      for (int h = 0; h < 2; ++h)
+      for (int st = 0; st < 2; ++st)
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) {
-          sx0[h][nt] = xs0[h][nt].x;
-          sx1[h][nt] = xs1[h][nt].x;
+        for (int w = 0; w < 4; ++w) B[st][w] = bsrc[st * 8 + w * 2];
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt) {
+        // rows rt*16 + gid and + 8: 16-byte chunk 2tq + st, 128B-swizzled
+        const uint8_t* rp = ct + rt * 2048 + gid * 128;
+        uint4 Wc[2][2];
+#pragma unroll
+        for (int st = 0; st < 2; ++st) {
+          Wc[0][st] = *reinterpret_cast<const uint4*>(rp + a_chunk[st]);
+          Wc[1][st] = *reinterpret_cast<const uint4*>(rp + 1024 + a_chunk[st]);
         }
+        const float* sr = reinterpret_cast<const float*>(rs) + (rt * 16 + gid) * 8 + 2 * tq;
+        const float2 s0 = *reinterpret_cast<const float2*>(sr);
+        const float2 s1 = *reinterpret_cast<const float2*>(sr + 64);
+        const float2 b0 = *reinterpret_cast<const float2*>(sr + 256);
+        const float2 b1 = *reinterpret_cast<const float2*>(sr + 256 + 64);
+        float d[2][4];
 #pragma unroll
-      for (int mi = 0; mi < NMAT; ++mi) {
+        for (int st = 0; st < 2; ++st) {
+          d[st][0] = d[st][1] = d[st][2] = d[st][3] = 0.f;
+          const uint32_t w0[4] = {Wc[0][st].x, Wc[0][st].y, Wc[0][st].z, Wc[0][st].w};
+          const uint32_t w1[4] = {Wc[1][st].x, Wc[1][st].y, Wc[1][st].z, Wc[1][st].w};
 #pragma unroll
-        for (int rt = 0; rt < 2; ++rt) {
-          // (rows 0-7, group 2jp), (rows 8-15, 2jp), (rows 0-7, 2jp+1), (rows 8-15, 2jp+1)
-          uint32_t w[4];
-          ldmatrix_x4(w[0], w[1], w[2], w[3], cd + mi * 4096 + rt * 2048 + coff);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const uint32_t wa = w[2 * h], wb = w[2 * h + 1];
-            const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-            // exact codes (and 16 * codes) times 2^-24 as f16: the accumulator
-            // only ever holds sums of code * x, so its rounding stays at that scale
-            const uint32_t a0 = codes_lo_f16x2(wa);
-            const uint32_t a1 = codes_lo_f16x2(wb);
-            const uint32_t a2 = codes_hi_f16x2(wa);
-            const uint32_t a3 = codes_hi_f16x2(wb);
-            const uint32_t a4 = codes_lo_f16x2(wa8);
-            const uint32_t a5 = codes_lo_f16x2(wb8);
-            const uint32_t a6 = codes_hi_f16x2(wa8);
-            const uint32_t a7 = codes_hi_f16x2(wb8);
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              float* dd = d[mi][rt][h][nt];
-              dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
-              mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bh[h][nt].x, bh[h][nt].y);
-              mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bl[h][nt].x, bl[h][nt].y);
-              mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bh[h][nt].z, bh[h][nt].w);
-              mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bl[h][nt].z, bl[h][nt].w);
+          for (int w = 0; w < 4; ++w) {
+            const uint32_t x0 = w0[w], x1 = w1[w];
+            mma_f16_16816(d[st], codes_lo_f16x2(x0), codes_lo_f16x2(x1), codes_hi_f16x2(x0),
+                          codes_hi_f16x2(x1), B[st][w].x, B[st][w].y);
+            const uint32_t y0 = x0 >> 8, y1 = x1 >> 8;
+            mma_f16_16816(d[st], codes_lo_f16x2(y0), codes_lo_f16x2(y1), codes_hi_f16x2(y0),
+                          codes_hi_f16x2(y1), B[st][w].z, B[st][w].w);
+          }
+        }
+        float* a = acc[0][rt][0];
+        a[0] = fmaf(s0.x, d[0][0] + d[0][1], fmaf(b0.x, sxv.x, a[0]));
+        a[0] = fmaf(s0.y, d[1][0] + d[1][1], fmaf(b0.y, sxv.z, a[0]));
+        a[2] = fmaf(s1.x, d[0][2] + d[0][3], fmaf(b1.x, sxv.x, a[2]));
+        a[2] = fmaf(s1.y, d[1][2] + d[1][3], fmaf(b1.y, sxv.z, a[2]));
+      }
+    } else {
+      if (!b_ready) load_b(0, bh, bl, xs0, xs1);
+      // (staged activations live in the stage's own buffer: no early load then)
+      const bool next_same_unit = XM == 0 && cc.ks + 1 < cc.ke;
+  #pragma unroll 1
+      for (int jp = 0; jp < 4; ++jp) {
+        const uint32_t coff = ((uint32_t)jp << 5) ^ ld_c;
+        float d[NMAT][2][2][NT][4];
+        float sx0[2][NT], sx1[2][NT];
+  #pragma unroll
+        for (int h = 0; h < 2; ++h)
+  #pragma unroll
+          for (int nt = 0; nt < NT; ++nt) {
+            sx0[h][nt] = xs0[h][nt].x;
+            sx1[h][nt] = xs1[h][nt].x;
+          }
+  #pragma unroll
+        for (int mi = 0; mi < NMAT; ++mi) {
+  #pragma unroll
+          for (int rt = 0; rt < 2; ++rt) {
+            // (rows 0-7, group 2jp), (rows 8-15, 2jp), (rows 0-7, 2jp+1), (rows 8-15, 2jp+1)
+            uint32_t w[4];
+            ldmatrix_x4(w[0], w[1], w[2], w[3], cd + mi * 4096 + rt * 2048 + coff);
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t wa = w[2 * h], wb = w[2 * h + 1];
+              const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+              // exact codes (and 16 * codes) times 2^-24 as f16: the accumulator
+              // only ever holds sums of code * x, so its rounding stays at that scale
+              const uint32_t a0 = codes_lo_f16x2(wa);
+              const uint32_t a1 = codes_lo_f16x2(wb);
+              const uint32_t a2 = codes_hi_f16x2(wa);
+              const uint32_t a3 = codes_hi_f16x2(wb);
+              const uint32_t a4 = codes_lo_f16x2(wa8);
+              const uint32_t a5 = codes_lo_f16x2(wb8);
+              const uint32_t a6 = codes_hi_f16x2(wa8);
+              const uint32_t a7 = codes_hi_f16x2(wb8);
+  #pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                float* dd = d[mi][rt][h][nt];
+                dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
+                mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bh[h][nt].x, bh[h][nt].y);
+                mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bl[h][nt].x, bl[h][nt].y);
+                mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bh[h][nt].z, bh[h][nt].w);
+                mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bl[h][nt].z, bl[h][nt].w);
+              }
             }
           }
         }
-      }
-      if (jp < 3)
-        load_b(jp + 1, bh, bl, xs0, xs1);
-      else if (next_same_unit)
-        load_b_at(gbase + 8, 0, bh, bl, xs0, xs1);
-#pragma unroll
-      for (int mi = 0; mi < NMAT; ++mi) {
-        const float* ssm = reinterpret_cast<const float*>(rs + mi * 2048) + sb_lane + 2 * jp;
-        const float* bsm = ssm + 256;
-#pragma unroll
-        for (int rt = 0; rt < 2; ++rt) {
-          const float2 sa = *reinterpret_cast<const float2*>(ssm + rt * 128);
-          const float2 sb = *reinterpret_cast<const float2*>(ssm + rt * 128 + 64);
-          const float2 ba = *reinterpret_cast<const float2*>(bsm + rt * 128);
-          const float2 bb = *reinterpret_cast<const float2*>(bsm + rt * 128 + 64);
-#pragma unroll
-          for (int h = 0; h < 2; ++h) {
-            const float s0 = h ? sa.y : sa.x, s1 = h ? sb.y : sb.x;
-            const float b0 = h ? ba.y : ba.x, b1 = h ? bb.y : bb.x;
-#pragma unroll
-            for (int nt = 0; nt < NT; ++nt) {
-              const float* dd = d[mi][rt][h][nt];
-              float* a = acc[mi][rt][nt];
-              a[0] = fmaf(s0, dd[0], fmaf(b0, sx0[h][nt], a[0]));
-              a[2] = fmaf(s1, dd[2], fmaf(b1, sx0[h][nt], a[2]));
-              if constexpr (!C1) {
-                a[1] = fmaf(s0, dd[1], fmaf(b0, sx1[h][nt], a[1]));
-                a[3] = fmaf(s1, dd[3], fmaf(b1, sx1[h][nt], a[3]));
+        if (jp < 3)
+          load_b(jp + 1, bh, bl, xs0, xs1);
+        else if (next_same_unit)
+          load_b_at(gbase + 8, 0, bh, bl, xs0, xs1);
+  #pragma unroll
+        for (int mi = 0; mi < NMAT; ++mi) {
+          const float* ssm = reinterpret_cast<const float*>(rs + mi * 2048) + sb_lane + 2 * jp;
+          const float* bsm = ssm + 256;
+  #pragma unroll
+          for (int rt = 0; rt < 2; ++rt) {
+            const float2 sa = *reinterpret_cast<const float2*>(ssm + rt * 128);
+            const float2 sb = *reinterpret_cast<const float2*>(ssm + rt * 128 + 64);
+            const float2 ba = *reinterpret_cast<const float2*>(bsm + rt * 128);
+            const float2 bb = *reinterpret_cast<const float2*>(bsm + rt * 128 + 64);
+  #pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const float s0 = h ? sa.y : sa.x, s1 = h ? sb.y : sb.x;
+              const float b0 = h ? ba.y : ba.x, b1 = h ? bb.y : bb.x;
+  #pragma unroll
+              for (int nt = 0; nt < NT; ++nt) {
+                const float* dd = d[mi][rt][h][nt];
+                float* a = acc[mi][rt][nt];
+                a[0] = fmaf(s0, dd[0], fmaf(b0, sx0[h][nt], a[0]));
+                a[2] = fmaf(s1, dd[2], fmaf(b1, sx0[h][nt], a[2]));
+                if constexpr (!C1) {
+                  a[1] = fmaf(s0, dd[1], fmaf(b0, sx1[h][nt], a[1]));
+                  a[3] = fmaf(s1, dd[3], fmaf(b1, sx1[h][nt], a[3]));
+                }
               }
             }
           }
         }
       }
+      b_ready = next_same_unit;
     }
-    b_ready = next_same_unit;
     __syncwarp();
     if (lane == 0 && pc.u < units) {
       issue_w(pc, slot);
@@ -530,6 +592,18 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     const int tile = cc.tile;
     const int seg = cc.seg;
     if (!cc.advance(p, W, units, ksplit, spu, KS, UM)) continue;
+    if constexpr (C1) {
+      // a row's four lanes each hold two groups per stage: sum them (fixed order)
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          float v = acc[0][rt][0][e];
+          v += __shfl_xor_sync(0xffffffffu, v, 1);
+          v += __shfl_xor_sync(0xffffffffu, v, 2);
+          acc[0][rt][0][e] = v;
+        }
+    }
 
     // ------------------------------------------------------------ unit done
     // fin[um] is the tile's full sum for matrix um of the unit's tile
