@@ -68,9 +68,10 @@ def layer_bytes(cfg):
 
 
 def launches_per_step(cfg):
-    # norm/pack, eh_proj, norm/pack, qkv, attention, o_proj, (norm, gate/up, down | router,
-    # expert gate/up, expert down), final norm, lm_head
-    return 11 if not cfg.moe else 10
+    # dense: norm/pack, eh_proj, qkv, attention, o_proj, gate/up, down, lm_head (the other
+    # three RMSNorms are folded into the projections); MoE: norm/pack, eh_proj, qkv,
+    # attention, o_proj, router, expert gate/up, expert down, final norm, lm_head
+    return 8 if not cfg.moe else 10
 
 
 # --------------------------------------------------------------- clocks

@@ -569,6 +569,7 @@ struct LayerWs {
   float *u, *u1, *u2, *qp, *kp, *vp;
   float* part;
   unsigned long long* am_partial;
+  float *ss0, *ss1, *ss2;  // per-tile sums of squares of u, u1, u2 (folded RMSNorms)
   GemvScratch gemv;
   MoeScratch moe;
 };
@@ -605,6 +606,9 @@ static void carve_layer(Carve& cv, const mtp_layer_desc* L, int m, LayerWs* w) {
   w->part = cv.take<float>(attn_part_bytes(g.n_kv_heads, ns, (g.n_heads / g.n_kv_heads) * m,
                                            g.head_dim_v));
   w->am_partial = cv.take<unsigned long long>(8 * 4096);
+  w->ss0 = cv.take<float>(sizeof(float) * m * (H / kGroup));
+  w->ss1 = cv.take<float>(sizeof(float) * m * (H / kGroup));
+  w->ss2 = cv.take<float>(sizeof(float) * m * (H / kGroup));
   w->gemv = carve_scratch(cv);
   if (L->moe) carve_moe(cv, L->moe, H, &w->moe);
 }
@@ -699,19 +703,20 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   p.nseg = 1;
   p.seg[0] = plain_seg(tiles_of(H), H, 0, w.u, H, nullptr);
   p.err = err;
+  // the attention RMSNorm is folded into the q/k/v projection: pack u * attn_norm
+  // and the per-tile sums of u^2 here, scale the projections' rows there
+  const int ht = H / kGroup;
+  p.pack_w = L->attn_norm;
+  p.pack_c0 = 0;
+  p.out_xp = w.xb;
+  p.out_xs = w.xsb;
+  p.out_m = m;
+  p.ss_out = w.ss0;
   const int nt = m > 8 ? 2 : 1;
   if ((e = launch_gemv(1, nt, kEpiStore, p, tiles_of(H), w.gemv, st)) != cudaSuccess)
     return cuda_fail(e, "eh_proj launch");
 
-  // 3. x = RMSNorm(u) * attn_norm
-  NormSeg n1 = {};
-  n1.src = w.u;
-  n1.w = L->attn_norm;
-  n1.eps = L->eps;
-  n1.dim = H;
-  n1.src_ld = H;
-  if ((e = launch_norm_pack(&n1, 1, m, w.xa, w.xsa, err, st)) != cudaSuccess)
-    return cuda_fail(e, "attn norm launch");
+  // 3. x = RMSNorm(u) * attn_norm: folded (rows of step 4 scaled by rsqrt(mean u^2 + eps))
 
   // 4. q (+gate), k, v projections in one launch
   const int qrows = g.n_heads * g.head_dim_qk * (g.gated_q ? 2 : 1);
@@ -720,11 +725,15 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   if ((s = qmat_cached(&q.mat[0], L->wq, "wq")) != MTP_OK) return s;
   if ((s = qmat_cached(&q.mat[1], L->wk, "wk")) != MTP_OK) return s;
   if ((s = qmat_cached(&q.mat[2], L->wv, "wv")) != MTP_OK) return s;
-  q.xp = w.xa;
-  q.xs = w.xsa;
+  q.xp = w.xb;
+  q.xs = w.xsb;
   q.m = m;
   q.K = H;
   q.nseg = 3;
+  q.in_ss = w.ss0;
+  q.in_ss_n = ht;
+  q.in_ss_dim = H;
+  q.in_ss_eps = L->eps;
   const int tq = tiles_of(qrows), tk = tiles_of(krows), tv = tiles_of(vrows);
   q.seg[0] = plain_seg(tq, qrows, 0, w.qp, qrows, nullptr);
   q.seg[1] = plain_seg(tq + tk, krows, 1, w.kp, krows, nullptr);
@@ -756,6 +765,14 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   o.nseg = 1;
   o.seg[0] = plain_seg(tiles_of(H), H, 0, w.u1, H, w.u);
   o.err = err;
+  if (!L->moe) {  // post-attention RMSNorm folded into the gate/up projection
+    o.pack_w = L->post_norm;
+    o.pack_c0 = 0;
+    o.out_xp = w.xb;
+    o.out_xs = w.xsb;
+    o.out_m = m;
+    o.ss_out = w.ss1;
+  }
   if ((e = launch_gemv(1, nt, kEpiStore, o, tiles_of(H), w.gemv, st)) != cudaSuccess)
     return cuda_fail(e, "o_proj launch");
 
@@ -764,28 +781,24 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     s = enqueue_moe(L->moe, w.u1, L->post_norm, L->eps, H, u2, w.moe, ws, st);
     if (s != MTP_OK) return s;
   } else {
-    // 7. f = RMSNorm(u1) * post_norm
-    NormSeg n2 = {};
-    n2.src = w.u1;
-    n2.w = L->post_norm;
-    n2.eps = L->eps;
-    n2.dim = H;
-    n2.src_ld = H;
-    if ((e = launch_norm_pack(&n2, 1, m, w.xa, w.xsa, err, st)) != cudaSuccess)
-      return cuda_fail(e, "post norm launch");
+    // 7. f = RMSNorm(u1) * post_norm: folded into step 8
     // 8. h = silu(W_gate f) * (W_up f), packed
     const int I = L->intermediate;
     GemvParams gu = {};
     if ((s = qmat_cached(&gu.mat[0], L->ffn_gate, "ffn_gate")) != MTP_OK) return s;
     if ((s = qmat_cached(&gu.mat[1], L->ffn_up, "ffn_up")) != MTP_OK) return s;
-    gu.xp = w.xa;
-    gu.xs = w.xsa;
+    gu.xp = w.xb;
+    gu.xs = w.xsb;
     gu.m = m;
     gu.K = H;
     gu.nseg = 1;
+    gu.in_ss = w.ss1;
+    gu.in_ss_n = ht;
+    gu.in_ss_dim = H;
+    gu.in_ss_eps = L->eps;
     gu.seg[0] = plain_seg(tiles_of(I), I, 0, nullptr, I, nullptr);
-    gu.out_xp = w.xb;
-    gu.out_xs = w.xsb;
+    gu.out_xp = w.xa;
+    gu.out_xs = w.xsa;
     gu.out_m = m;
     gu.err = err;
     if ((e = launch_gemv(2, nt, kEpiSwiglu, gu, tiles_of(I), w.gemv, st)) != cudaSuccess)
@@ -793,15 +806,47 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     // 9. u2 = u1 + W_down h
     GemvParams dn = {};
     if ((s = qmat_cached(&dn.mat[0], L->ffn_down, "ffn_down")) != MTP_OK) return s;
-    dn.xp = w.xb;
-    dn.xs = w.xsb;
+    dn.xp = w.xa;
+    dn.xs = w.xsa;
     dn.m = m;
     dn.K = I;
     dn.nseg = 1;
     dn.seg[0] = plain_seg(tiles_of(H), H, 0, u2, H, w.u1);
     dn.err = err;
+    // final RMSNorm of the last row folded into the lm_head
+    dn.pack_w = L->final_norm;
+    dn.pack_c0 = m - 1;
+    dn.out_xp = w.xb;
+    dn.out_xs = w.xsb;
+    dn.out_m = 1;
+    dn.ss_out = w.ss2;
     if ((e = launch_gemv(1, nt, kEpiStore, dn, tiles_of(H), w.gemv, st)) != cudaSuccess)
       return cuda_fail(e, "down launch");
+    // 10-11. lm_head + argmax of RMSNorm(u2[m-1]) * final_norm (folded)
+    GemvParams hd = {};
+    if ((s = qmat_cached(&hd.mat[0], L->lm_head, "lm_head")) != MTP_OK) return s;
+    hd.xp = w.xb;
+    hd.xs = w.xsb;
+    hd.m = 1;
+    hd.K = H;
+    hd.nseg = 1;
+    hd.seg[0] = plain_seg(tiles_of(L->vocab), L->vocab, 0, nullptr, L->vocab, nullptr);
+    hd.in_ss = w.ss2;
+    hd.in_ss_n = ht;
+    hd.in_ss_dim = H;
+    hd.in_ss_eps = L->eps;
+    hd.normed_src = u2 + (size_t)(m - 1) * H;
+    hd.normed_w = L->final_norm;
+    hd.normed_out = out->d_hidden_out;
+    hd.am_partial = w.am_partial;
+    hd.am_counter = header(ws)->counters + kCntArgmax;
+    hd.am_token = out->d_token;
+    hd.am_value = out->d_value;
+    hd.logits = out->d_logits;
+    hd.err = err;
+    if ((e = launch_gemv(1, 1, kEpiArgmax, hd, tiles_of(L->vocab), w.gemv, st)) != cudaSuccess)
+      return cuda_fail(e, "lm head launch");
+    return MTP_OK;
   }
 
   // 10-11. final norm of the last row, lm_head + argmax

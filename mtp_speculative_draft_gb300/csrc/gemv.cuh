@@ -148,7 +148,32 @@ struct GemvParams {
   float* part;
   unsigned* tile_cnt;
   int* err;
+  // RMSNorm folded into the projection: the input rows x' = u * w are packed
+  // unnormalised and the outputs of row c are scaled by
+  // r[c] = rsqrt(sum_{i < in_ss_n} in_ss[i * m + c] / in_ss_dim + in_ss_eps).
+  const float* in_ss;    // per-tile sums of u^2 written by the producer, or null
+  int in_ss_n;
+  int in_ss_dim;
+  float in_ss_eps;
+  // Store epilogue (one segment): also packs rows c >= pack_c0 of the stored
+  // value v, times pack_w[row], into out_xp/out_xs (column c - pack_c0 of
+  // out_m) and writes the tile's sum of v^2 per packed row to ss_out[tile * out_m + c'].
+  const float* pack_w;
+  int pack_c0;
+  float* ss_out;
+  // Argmax epilogue: CTA 0 also writes normed_out[k] = normed_src[k] * r[0] * normed_w[k]
+  const float* normed_src;
+  const float* normed_w;
+  float* normed_out;
 };
+
+// Sum over i < n of part[i * m + c], taken by the whole warp in a fixed order
+// (every lane gets the same value).
+__device__ __forceinline__ float warp_col_sum(const float* part, int n, int m, int c) {
+  float s = 0.f;
+  for (int i = threadIdx.x & 31; i < n; i += 32) s += __ldcg(part + (size_t)i * m + c);
+  return warp_sum(s);
+}
 
 constexpr int kStageMatBytes = 6144;  // 4 KB codes + 1 KB scales + 1 KB biases
 constexpr int kGemvWarps = 4;
@@ -350,6 +375,27 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
       issue_x(pc, pre);
       pc.advance(p, W, units, ksplit, spu, KS, UM);
     }
+  }
+  // (after the first activation copies are in flight: these loads wait on L2)
+  // per-lane output scales of the activation rows this lane's fragments hold
+  float rsc[NT][2];
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) rsc[nt][0] = rsc[nt][1] = 1.f;
+  if (p.in_ss) {
+    for (int c = 0; c < m; ++c) {
+      const float ss = warp_col_sum(p.in_ss, p.in_ss_n, m, c);
+      const float r = rsqrtf(ss / (float)p.in_ss_dim + p.in_ss_eps);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e)
+          if (nt * 8 + 2 * tq + e == c || (C1 && c == 0)) rsc[nt][e] = r;
+    }
+  }
+  if constexpr (EPI == kEpiArgmax) {
+    if (p.normed_out && blockIdx.x == 0)
+      for (int k = threadIdx.x; k < p.K; k += blockDim.x)
+        p.normed_out[k] = p.normed_src[k] * rsc[0][0] * p.normed_w[k];
   }
 
   float acc[NMAT][2][NT][4];
@@ -684,34 +730,71 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
               acc[mi][rt][nt][e] = 0.f;
             }
     }
-    // undo the 2^-24 of the subnormal codes (exact)
+    // undo the 2^-24 of the subnormal codes (exact) and apply the input-row
+    // scales of a folded RMSNorm
 #pragma unroll
-    for (int um = 0; um < UM; ++um) {
-      float* fw = &fin[um][0][0][0][0];
+    for (int um = 0; um < UM; ++um)
 #pragma unroll
-      for (int q = 0; q < NMAT * 2 * NT * 4; ++q) fw[q] *= kCodeScale;
-    }
+      for (int mi = 0; mi < NMAT; ++mi)
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) fin[um][mi][rt][nt][e] *= kCodeScale * rsc[nt][e & 1];
 
     // ---------------------------------------------------------- epilogue
     const GemvSeg& sg = p.seg[seg];
     const int lt = tile - (seg ? p.seg[seg - 1].tile_end : 0);
     const int rbase = lt * 32;
     if constexpr (EPI == kEpiStore) {
+      const bool packing = p.pack_w != nullptr;  // full tiles, one segment (checked by the host)
+      const int g_out = (sg.out_col0 + rbase) / kGroup;
 #pragma unroll
-      for (int rt = 0; rt < 2; ++rt)
+      for (int nt = 0; nt < NT; ++nt) {
+        float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float ssq[2] = {0.f, 0.f};
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
+        for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int row = rbase + rt * 16 + gid + ((e & 2) ? 8 : 0);
+            const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
+            const int row = rbase + rloc;
             const int c = nt * 8 + 2 * tq + (e & 1);
             if (row < sg.n && c < m) {
               const size_t o = (size_t)c * sg.ld + sg.out_col0 + row;
               float v = fin[0][0][rt][nt][e];
               if (sg.res) v += sg.res[o];
               sg.out[o] = v;
+              if (packing && c >= p.pack_c0) {
+                const float2 hs = xp_store_elem(p.out_xp, p.out_m, g_out, c - p.pack_c0,
+                                                rloc >> 3, rloc & 7,
+                                                v * p.pack_w[sg.out_col0 + row]);
+                part[e & 1].x += hs.x;
+                part[e & 1].y += hs.y;
+                ssq[e & 1] = fmaf(v, v, ssq[e & 1]);
+              }
             }
           }
+        if (packing) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float2 v = part[e];
+            float q2 = ssq[e];
+#pragma unroll
+            for (int o = 4; o < 32; o <<= 1) {
+              v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+              v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+              q2 += __shfl_xor_sync(0xffffffffu, q2, o);
+            }
+            const int c = nt * 8 + 2 * tq + e;
+            if (gid == 0 && c < m && c >= p.pack_c0) {
+              p.out_xs[g_out * p.out_m + (c - p.pack_c0)] = v;
+              p.ss_out[lt * p.out_m + (c - p.pack_c0)] = q2;
+            }
+          }
+        }
+      }
     } else if constexpr (EPI == kEpiSwiglu) {
       const float scale = sg.w_idx >= 0 ? p.segw[sg.w_idx] : 1.f;
       const int g_out = (sg.out_col0 + rbase) / kGroup;
