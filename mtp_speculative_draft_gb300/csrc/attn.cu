@@ -51,13 +51,14 @@ struct AttnLayout {
   size_t q_off, newk_off, newv_off, ps_off, bar_off, total;
 };
 
-// [nbuf tile buffers][queries QG x dqk][new keys m x dqk][new values m x dv]
-// [probability rows: warps x kAttnQMax x 32][mbarriers]
-__host__ __device__ inline AttnLayout attn_layout(int dqk, int dv, int QG, int m, int nbuf,
+// [nbuf tile buffers][query slots qslots x dqk][new keys m x dqk][new values m x dv]
+// [probability rows: warps x kAttnQMax x 32][mbarriers].  Query slots: each
+// group of query rows owns QM slots; slots past the group's rows hold zeros.
+__host__ __device__ inline AttnLayout attn_layout(int dqk, int dv, int qslots, int m, int nbuf,
                                                   int warps) {
   AttnLayout L;
   L.q_off = (size_t)nbuf * attn_tile_bytes(dqk, dv);
-  L.newk_off = L.q_off + (size_t)QG * dqk * 4;
+  L.newk_off = L.q_off + (size_t)qslots * dqk * 4;
   L.newv_off = L.newk_off + (size_t)m * dqk * 4;
   L.ps_off = L.newv_off + (size_t)m * dv * 4;
   L.bar_off = L.ps_off + (size_t)warps * kAttnQMax * kTileKeys * 4;
@@ -65,26 +66,48 @@ __host__ __device__ inline AttnLayout attn_layout(int dqk, int dv, int QG, int m
   return L;
 }
 
-// Per-head RMSNorm (optional) then rotary embedding of one head vector held
-// in shared memory by one warp; the result is multiplied by `post_scale`.
-__device__ __forceinline__ void warp_norm_rope(float* v, int d, const float* nw, float eps,
-                                               const float* rope_row, int rot, float post_scale,
-                                               int lane) {
+// One head vector (d <= 256) read from global memory by one warp: per-head
+// RMSNorm (when nw is given), rotary embedding of the first rot dims (pairs
+// i, i + rot/2), times post_scale; the result goes to v in shared memory.
+// All global loads are issued before any arithmetic.
+__device__ __forceinline__ void warp_norm_rope(float* v, const float* src, int d, const float* nw,
+                                               float eps, const float* rope_row, int rot,
+                                               float post_scale, int lane) {
+  float x[8], w[8], cs[4], sn[4];
+  const int half = rot / 2;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = lane + 32 * j;
+    x[j] = i < d ? src[i] : 0.f;
+    w[j] = (nw && i < d) ? nw[i] : 1.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = lane + 32 * j;
+    cs[j] = i < half ? rope_row[2 * i] : 1.f;
+    sn[j] = i < half ? rope_row[2 * i + 1] : 0.f;
+  }
+  float inv = 1.f;
   if (nw) {
     float ss = 0.f;
-    for (int i = lane; i < d; i += 32) ss += v[i] * v[i];
-    ss = warp_sum(ss);
-    const float inv = rsqrtf(ss / (float)d + eps);
-    __syncwarp();
-    for (int i = lane; i < d; i += 32) v[i] = v[i] * inv * nw[i];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += x[j] * x[j];
+    inv = rsqrtf(warp_sum(ss) / (float)d + eps);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = lane + 32 * j;
+    if (i < d) v[i] = x[j] * inv * w[j];
   }
   __syncwarp();
-  const int half = rot / 2;
-  for (int i = lane; i < half; i += 32) {
-    const float c = rope_row[2 * i], s = rope_row[2 * i + 1];
-    const float a = v[i], b = v[i + half];
-    v[i] = a * c - b * s;
-    v[i + half] = a * s + b * c;
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = lane + 32 * j;
+    if (i < half) {
+      const float a = v[i], b = v[i + half];
+      v[i] = a * cs[j] - b * sn[j];
+      v[i + half] = a * sn[j] + b * cs[j];
+    }
   }
   __syncwarp();
   if (post_scale != 1.f)
@@ -148,17 +171,18 @@ struct WarpState {
   float M[QM], l[QM], o[QM][DV];
 };
 
-// One tile of nk keys starting at absolute key index key0, for the warp's
-// query rows q0 .. q0 + nq - 1.  `swz`: K in swizzled boxes (cached tiles),
-// else plain rows of dqk floats (the new keys).
+// One tile of nk keys starting at absolute key index key0, for the warp's QM
+// query slots (query rows q0 .. q0 + QM - 1; slots past the group's rows are
+// zero vectors whose results are never used, so no row is branched on).
+// `swz`: K in swizzled boxes (cached tiles), else plain rows of dqk floats
+// (the new keys).
 template <int QM, int DV>
 __device__ __forceinline__ void warp_tile(const AttnParams& a, WarpState<QM, DV>& st,
                                           const float* Ks, bool swz, const float* Vs, int nk,
-                                          int key0, const float* qs, int q0, int nq, int G,
-                                          float* ps, int lane) {
+                                          int key0, const float* qrow, int q0, int G, float* ps,
+                                          int lane) {
   const int dqk = a.dqk, dv = a.dv;
   const int kq4 = dqk / 4;
-  const float* qrow = qs + (size_t)q0 * dqk;
   // ---- logits: lane = key
   float acc[QM];
 #pragma unroll
@@ -171,10 +195,8 @@ __device__ __forceinline__ void warp_tile(const AttnParams& a, WarpState<QM, DV>
                            : *reinterpret_cast<const float4*>(Ks + lane * dqk + 4 * f);
 #pragma unroll
       for (int q = 0; q < QM; ++q) {
-        if (q < nq) {
-          const float4 x = *reinterpret_cast<const float4*>(qrow + q * dqk + 4 * f);
-          acc[q] = fmaf(x.x, k.x, fmaf(x.y, k.y, fmaf(x.z, k.z, fmaf(x.w, k.w, acc[q]))));
-        }
+        const float4 x = *reinterpret_cast<const float4*>(qrow + q * dqk + 4 * f);
+        acc[q] = fmaf(x.x, k.x, fmaf(x.y, k.y, fmaf(x.z, k.z, fmaf(x.w, k.w, acc[q]))));
       }
     }
   }
@@ -182,19 +204,17 @@ __device__ __forceinline__ void warp_tile(const AttnParams& a, WarpState<QM, DV>
   const int j = key0 + lane;
 #pragma unroll
   for (int q = 0; q < QM; ++q) {
-    if (q < nq) {
-      const int p = a.L + (q0 + q) / G;
-      const bool ok = lane < nk && j <= p && (a.window <= 0 || j > p - a.window);
-      const float l = ok ? acc[q] : kNegBig;
-      const float mnew = fmaxf(st.M[q], warp_max(l));
-      const float pr = ok ? exp2f(l - mnew) : 0.f;
-      const float alpha = exp2f(st.M[q] - mnew);
-      st.l[q] = st.l[q] * alpha + warp_sum(pr);
-      st.M[q] = mnew;
-      ps[q * kTileKeys + lane] = pr;
+    const int p = a.L + (q0 + q) / G;
+    const bool ok = lane < nk && j <= p && (a.window <= 0 || j > p - a.window);
+    const float l = ok ? acc[q] : kNegBig;
+    const float mnew = fmaxf(st.M[q], warp_max(l));
+    const float pr = ok ? exp2f(l - mnew) : 0.f;
+    const float alpha = exp2f(st.M[q] - mnew);
+    st.l[q] = st.l[q] * alpha + warp_sum(pr);
+    st.M[q] = mnew;
+    ps[q * kTileKeys + lane] = pr;
 #pragma unroll
-      for (int i = 0; i < DV; ++i) st.o[q][i] *= alpha;
-    }
+    for (int i = 0; i < DV; ++i) st.o[q][i] *= alpha;
   }
   __syncwarp();
   // ---- P.V: lane = output dims, four keys per step (rows past nk hold p = 0
@@ -206,13 +226,11 @@ __device__ __forceinline__ void warp_tile(const AttnParams& a, WarpState<QM, DV>
     for (int u = 0; u < 4; ++u) load_dims<DV>(Vs + (size_t)(jj + u) * dv, lane, v[u]);
 #pragma unroll
     for (int q = 0; q < QM; ++q) {
-      if (q < nq) {
-        const float4 p4 = *reinterpret_cast<const float4*>(ps + q * kTileKeys + jj);
+      const float4 p4 = *reinterpret_cast<const float4*>(ps + q * kTileKeys + jj);
 #pragma unroll
-        for (int i = 0; i < DV; ++i)
-          st.o[q][i] = fmaf(p4.x, v[0][i],
-                            fmaf(p4.y, v[1][i], fmaf(p4.z, v[2][i], fmaf(p4.w, v[3][i], st.o[q][i]))));
-      }
+      for (int i = 0; i < DV; ++i)
+        st.o[q][i] = fmaf(p4.x, v[0][i],
+                          fmaf(p4.y, v[1][i], fmaf(p4.z, v[2][i], fmaf(p4.w, v[3][i], st.o[q][i]))));
     }
   }
   for (; jj < nk; ++jj) {
@@ -220,11 +238,9 @@ __device__ __forceinline__ void warp_tile(const AttnParams& a, WarpState<QM, DV>
     load_dims<DV>(Vs + (size_t)jj * dv, lane, v);
 #pragma unroll
     for (int q = 0; q < QM; ++q) {
-      if (q < nq) {
-        const float p = ps[q * kTileKeys + jj];
+      const float p = ps[q * kTileKeys + jj];
 #pragma unroll
-        for (int i = 0; i < DV; ++i) st.o[q][i] = fmaf(p, v[i], st.o[q][i]);
-      }
+      for (int i = 0; i < DV; ++i) st.o[q][i] = fmaf(p, v[i], st.o[q][i]);
     }
   }
   __syncwarp();
@@ -247,8 +263,9 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   const int dqk = a.dqk, dv = a.dv;
   const int q_rows = a.nh * dqk * (a.gated ? 2 : 1);
   const int nbuf = a.nbuf, qgroups = a.qgroups;
-  const int qpw = (QG + qgroups - 1) / qgroups;      // query rows per warp
-  const AttnLayout Ly = attn_layout(dqk, dv, QG, a.m, nbuf, nw);
+  const int qpw = (QG + qgroups - 1) / qgroups;      // query rows per warp (<= QM)
+  const int qslots = qgroups * QM;
+  const AttnLayout Ly = attn_layout(dqk, dv, qslots, a.m, nbuf, nw);
   const size_t tile_bytes = attn_tile_bytes(dqk, dv);
   float* qs = reinterpret_cast<float*>(smraw + Ly.q_off);
   float* newk = reinterpret_cast<float*>(smraw + Ly.newk_off);
@@ -257,10 +274,11 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smraw + Ly.bar_off);
   __shared__ bool last;
 
-  // this warp: buffer b, query rows [q0, q0 + nq)
+  // this warp: buffer b, query rows [q0, q0 + nq) in slots [qgi * QM, qgi * QM + QM)
   const int b = warp / qgroups, qgi = warp % qgroups;
   const int q0 = qgi * qpw;
   const int nq = max(0, min(qpw, QG - q0));
+  const float* qrow = nullptr;  // set once the slots are filled
   const bool leader = qgi == 0 && lane == 0;
   float* Kb = reinterpret_cast<float*>(smraw + (size_t)b * tile_bytes);
   float* Vb = Kb + kTileKeys * dqk;
@@ -295,15 +313,23 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   pdl_launch_dependents();
   if (!a.prefetch_before_wait && leader && t_first < t_end) issue(t_first);
 
-  // ---- queries of this KV head: norm, rotate, pre-scale (log2 domain)
+  // ---- query slots of this KV head: norm, rotate, pre-scale (log2 domain);
+  // slots past a group's rows are zeroed
   const float qscale = a.scale * kLog2e;
-  for (int qi = warp; qi < QG; qi += nw) {
-    const int r = qi / G, h = kvh * G + qi % G;
-    const float* src = a.qp + (size_t)r * q_rows + (size_t)h * dqk * (a.gated ? 2 : 1);
-    float* dst = qs + qi * dqk;
-    for (int i = lane; i < dqk; i += 32) dst[i] = src[i];
-    warp_norm_rope(dst, dqk, a.qn, a.eps, a.rope + (size_t)(L + r) * a.rot, a.rot, qscale, lane);
+  for (int sl = warp; sl < qslots; sl += nw) {
+    const int g = sl / QM, l = sl - g * QM;
+    const int qi = g * qpw + l;
+    float* dst = qs + (size_t)sl * dqk;
+    if (l < qpw && qi < QG) {
+      const int r = qi / G, h = kvh * G + qi % G;
+      const float* src = a.qp + (size_t)r * q_rows + (size_t)h * dqk * (a.gated ? 2 : 1);
+      warp_norm_rope(dst, src, dqk, a.qn, a.eps, a.rope + (size_t)(L + r) * a.rot, a.rot, qscale,
+                     lane);
+    } else {
+      for (int i = lane; i < dqk; i += 32) dst[i] = 0.f;
+    }
   }
+  qrow = qs + (size_t)qgi * QM * dqk;
   // ---- new keys/values (last split): normalise, rotate, append to the cache
   const bool has_new = split == a.nsplit - 1;
   if (has_new) {
@@ -311,8 +337,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
       const int pos = L + r;
       float* kn = newk + r * dqk;
       const float* ksrc = a.kp + (size_t)r * a.nkv * dqk + (size_t)kvh * dqk;
-      for (int i = lane; i < dqk; i += 32) kn[i] = ksrc[i];
-      warp_norm_rope(kn, dqk, a.kn, a.eps, a.rope + (size_t)pos * a.rot, a.rot, 1.f, lane);
+      warp_norm_rope(kn, ksrc, dqk, a.kn, a.eps, a.rope + (size_t)pos * a.rot, a.rot, 1.f, lane);
       float* kdst = a.kc + ((size_t)kvh * a.cap + pos) * dqk;
       for (int i = lane; i < dqk; i += 32) kdst[i] = kn[i];
       float* vn = newv + r * dv;
@@ -350,7 +375,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
     phase ^= 1u;
     const int key0 = kbeg + t * kTileKeys;
     if (nq > 0)
-      warp_tile<QM, DV>(a, st, Kb, true, Vb, min(kTileKeys, L - key0), key0, qs, q0, nq, G, ps,
+      warp_tile<QM, DV>(a, st, Kb, true, Vb, min(kTileKeys, L - key0), key0, qrow, q0, G, ps,
                         lane);
     if (t + nbuf < t_end) {
       bar_named(bar_id, bar_cnt);  // every reader of the buffer is done with it
@@ -358,7 +383,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
     }
   }
   if (has_new && b == nbuf - 1 && nq > 0)
-    warp_tile<QM, DV>(a, st, newk, false, newv, a.m, L, qs, q0, nq, G, ps, lane);
+    warp_tile<QM, DV>(a, st, newk, false, newv, a.m, L, qrow, q0, G, ps, lane);
   if (__syncthreads_or(dead)) return;
   if (tid < nbuf) mbar_inval(&bars[tid]);
   __syncthreads();
@@ -419,13 +444,23 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   const size_t base = (size_t)kvh * ns * QG;
   const int dv4 = dv / 4;
   const int items = QG * dv4;
-  // gate values of this thread's first item, loaded alongside the (M, l) pairs
+  const size_t sstride = (size_t)QG * dv4;
+  // The first kMergePre partial outputs and the gate of this thread's first
+  // item are loaded together with the (M, l) pairs: one round trip to L2.
+  constexpr int kMergePre = 16;
   float4 gate = make_float4(0.f, 0.f, 0.f, 0.f);
-  if (a.gated && tid < items) {
+  float4 pre[kMergePre];
+  if (tid < items) {
     const int qi = tid / dv4, d4 = tid - qi * dv4;
-    const int r = qi / G, h = kvh * G + qi % G;
-    gate = *reinterpret_cast<const float4*>(a.qp + (size_t)r * q_rows + (size_t)h * dqk * 2 + dqk +
-                                            d4 * 4);
+    const float4* po = reinterpret_cast<const float4*>(part_o + (base + qi) * dv) + d4;
+#pragma unroll
+    for (int u = 0; u < kMergePre; ++u)
+      pre[u] = u < ns ? __ldcg(po + (size_t)u * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
+    if (a.gated) {
+      const int r = qi / G, h = kvh * G + qi % G;
+      gate = *reinterpret_cast<const float4*>(a.qp + (size_t)r * q_rows + (size_t)h * dqk * 2 +
+                                              dqk + d4 * 4);
+    }
   }
   for (int i = tid; i < ns * QG; i += nthreads) {
     const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part) + base + i);
@@ -451,9 +486,19 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   for (int it = tid; it < items; it += nthreads) {
     const int qi = it / dv4, d4 = it - qi * dv4;
     const float4* po = reinterpret_cast<const float4*>(part_o + (base + qi) * dv) + d4;
-    const size_t sstride = (size_t)QG * dv4;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     int s = 0;
+    if (it == tid) {
+#pragma unroll
+      for (int u = 0; u < kMergePre; ++u) {
+        const float w = u < ns ? wsm[u * QG + qi] : 0.f;
+        acc.x = fmaf(w, pre[u].x, acc.x);
+        acc.y = fmaf(w, pre[u].y, acc.y);
+        acc.z = fmaf(w, pre[u].z, acc.z);
+        acc.w = fmaf(w, pre[u].w, acc.w);
+      }
+      s = ns < kMergePre ? ns : kMergePre;
+    }
     for (; s + 8 <= ns; s += 8) {  // eight independent loads in flight
       float4 v[8];
 #pragma unroll
@@ -561,10 +606,19 @@ size_t attn_part_bytes(int nkv, int nsplit, int q_per_kv, int dv) {
 // at most 32 state floats per lane.
 static int attn_qmax(int dv) { return dv <= 128 ? kAttnQMax : 4; }
 
+// Query groups per buffer and the slots per group (the kernel's QM: the
+// smallest instantiated size that holds a group's rows).
+static void attn_groups(int QG, int dv, int* qgroups, int* qm) {
+  *qgroups = ceil_div(QG, attn_qmax(dv));
+  const int qpw = ceil_div(QG, *qgroups);
+  *qm = qpw <= 2 ? 2 : qpw <= 4 ? 4 : qpw <= 6 ? 6 : 8;
+}
+
 bool attn_supported(int QG, int dqk, int dv, int m) {
-  const int qg = ceil_div(QG, attn_qmax(dv));
+  int qg, qm;
+  attn_groups(QG, dv, &qg, &qm);
   if (qg > kAttnMaxWarps) return false;
-  const AttnLayout Ly = attn_layout(dqk, dv, QG, m, 1, qg);
+  const AttnLayout Ly = attn_layout(dqk, dv, qg * qm, m, 1, qg);
   return Ly.total + kAttnSlack <= kAttnSmemLimit;
 }
 
@@ -594,17 +648,30 @@ static cudaError_t launch_attn_t(const AttnParams& a, size_t smem, cudaStream_t 
   return cudaLaunchKernelEx(&cfg, attn_decode_kernel<QM, DV>, a);
 }
 
-// Query rows per warp: 8 for head_dim_v <= 128, else 4 (at most 32 state floats per lane).
-static cudaError_t launch_attn_dv(const AttnParams& a, size_t smem, cudaStream_t st) {
+template <int DV>
+static cudaError_t launch_attn_qm(const AttnParams& a, int qm, size_t smem, cudaStream_t st) {
+  switch (qm) {
+    case 2: return launch_attn_t<2, DV>(a, smem, st);
+    case 4: return launch_attn_t<4, DV>(a, smem, st);
+    case 6: if constexpr (DV <= 4) return launch_attn_t<6, DV>(a, smem, st); else break;
+    case 8: if constexpr (DV <= 4) return launch_attn_t<8, DV>(a, smem, st); else break;
+    default: break;
+  }
+  return cudaErrorInvalidValue;
+}
+
+// Slots per query group: up to 8 for head_dim_v <= 128, else 4 (at most 32
+// state floats per lane).
+static cudaError_t launch_attn_dv(const AttnParams& a, int qm, size_t smem, cudaStream_t st) {
   switch (a.dv / 32) {
-    case 1: return launch_attn_t<8, 1>(a, smem, st);
-    case 2: return launch_attn_t<8, 2>(a, smem, st);
-    case 3: return launch_attn_t<8, 3>(a, smem, st);
-    case 4: return launch_attn_t<8, 4>(a, smem, st);
-    case 5: return launch_attn_t<4, 5>(a, smem, st);
-    case 6: return launch_attn_t<4, 6>(a, smem, st);
-    case 7: return launch_attn_t<4, 7>(a, smem, st);
-    case 8: return launch_attn_t<4, 8>(a, smem, st);
+    case 1: return launch_attn_qm<1>(a, qm, smem, st);
+    case 2: return launch_attn_qm<2>(a, qm, smem, st);
+    case 3: return launch_attn_qm<3>(a, qm, smem, st);
+    case 4: return launch_attn_qm<4>(a, qm, smem, st);
+    case 5: return launch_attn_qm<5>(a, qm, smem, st);
+    case 6: return launch_attn_qm<6>(a, qm, smem, st);
+    case 7: return launch_attn_qm<7>(a, qm, smem, st);
+    case 8: return launch_attn_qm<8>(a, qm, smem, st);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -615,8 +682,9 @@ cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
   if (ke != cudaSuccess) return ke;
   const int QG = (a.nh / a.nkv) * a.m;
   // warps per buffer: the fewest that keep each warp within attn_qmax rows
-  const int qmax = attn_qmax(a.dv);
-  a.qgroups = ceil_div(QG, qmax);
+  int qm = 0;
+  attn_groups(QG, a.dv, &a.qgroups, &qm);
+  const int qslots = a.qgroups * qm;
   // buffers: as many as the split has tiles, within the warp and smem limits
   const int kbeg = a.window > 0 ? (a.L + 1 - a.window > 0 ? a.L + 1 - a.window : 0) : 0;
   const int ntiles = ceil_div(a.L - kbeg, kTileKeys);
@@ -625,22 +693,22 @@ cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
   if (nbuf > kAttnMaxWarps / a.qgroups) nbuf = kAttnMaxWarps / a.qgroups;
   if (nbuf > 15) nbuf = 15;  // named barriers 1..15 (0 is the CTA barrier)
   while (nbuf > 1 &&
-         attn_layout(a.dqk, a.dv, QG, a.m, nbuf, nbuf * a.qgroups).total + kAttnSlack >
+         attn_layout(a.dqk, a.dv, qslots, a.m, nbuf, nbuf * a.qgroups).total + kAttnSlack >
              kAttnSmemLimit)
     --nbuf;
   if (nbuf < 1) nbuf = 1;
   a.nbuf = nbuf;
   const int nw = nbuf * a.qgroups;
-  const AttnLayout Ly = attn_layout(a.dqk, a.dv, QG, a.m, nbuf, nw);
+  const AttnLayout Ly = attn_layout(a.dqk, a.dv, qslots, a.m, nbuf, nw);
   // the tile buffers are reused for the buffers' states, then the merge
-  const size_t combine = ((size_t)kAttnMaxWarps * kAttnQMax * 2 + (size_t)nw * qmax * a.dv) * 4;
+  const size_t combine = ((size_t)kAttnMaxWarps * kAttnQMax * 2 + (size_t)nw * qm * a.dv) * 4;
   const size_t merge = (size_t)a.nsplit * QG * 8 + (size_t)QG * a.dv * 4;
   size_t smem = Ly.total;
   if (combine > smem) smem = combine;
   if (merge > smem) smem = merge;
   smem += kAttnSlack;
   if (smem > kAttnSmemLimit) return cudaErrorInvalidValue;
-  return launch_attn_dv(a, smem, st);
+  return launch_attn_dv(a, qm, smem, st);
 }
 
 }  // namespace mtp
