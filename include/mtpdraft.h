@@ -81,7 +81,10 @@ int mtp_version(void);
 mtp_status mtp_workspace_init(void *d_ws, size_t bytes, void *stream);
 
 /* Reads the device error word of a workspace (synchronous device-to-host
- * copy).  0 = no device-side wait has timed out since mtp_workspace_init. */
+ * copy); the first error since mtp_workspace_init is kept:
+ *   0 none; 1 a wait for a TMA copy gave up; 2 a token id outside
+ *   [0, vocab) (row 0 was used); 3 a wait inside a multi-projection launch
+ *   for the previous projection's output gave up. */
 mtp_status mtp_workspace_status(const void *d_ws, int32_t *h_code, void *stream);
 
 /* ------------------------------------------------------------------------

@@ -106,7 +106,8 @@ static GemvScratch carve_scratch(Carve& cv) {
   sc.part_bytes = gemv_scratch_part_bytes();
   sc.part = cv.take<float>(sc.part_bytes);
   sc.cnt = cv.take<unsigned>(sizeof(unsigned) * kGemvCounters);
-  sc.cnt_len = kGemvCounters;
+  sc.cnt_len = kGemvCounters - kMaxPhases;
+  sc.phase_done = sc.cnt ? sc.cnt + sc.cnt_len : nullptr;
   return sc;
 }
 
@@ -712,8 +713,11 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   p.out_xs = w.xsb;
   p.out_m = m;
   p.ss_out = w.ss0;
+  p.epi = kEpiStore;
   const int nt = m > 8 ? 2 : 1;
-  if ((e = launch_gemv(1, nt, kEpiStore, p, tiles_of(H), w.gemv, st)) != cudaSuccess)
+  // one activation row: consecutive projections share one launch (phases)
+  const bool rows = (m == 1);
+  if (!rows && (e = launch_gemv(1, nt, kEpiStore, p, tiles_of(H), w.gemv, st)) != cudaSuccess)
     return cuda_fail(e, "eh_proj launch");
 
   // 3. x = RMSNorm(u) * attn_norm: folded (rows of step 4 scaled by rsqrt(mean u^2 + eps))
@@ -739,8 +743,15 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   q.seg[1] = plain_seg(tq + tk, krows, 1, w.kp, krows, nullptr);
   q.seg[2] = plain_seg(tq + tk + tv, vrows, 2, w.vp, vrows, nullptr);
   q.err = err;
-  if ((e = launch_gemv(1, nt, kEpiStore, q, tq + tk + tv, w.gemv, st)) != cudaSuccess)
+  q.epi = kEpiStore;
+  if (rows) {
+    GemvParams ph[2] = {p, q};
+    const int tl[2] = {tiles_of(H), tq + tk + tv};
+    if ((e = launch_gemv_rows(ph, tl, 2, w.gemv, err, st)) != cudaSuccess)
+      return cuda_fail(e, "eh_proj + qkv launch");
+  } else if ((e = launch_gemv(1, nt, kEpiStore, q, tq + tk + tv, w.gemv, st)) != cudaSuccess) {
     return cuda_fail(e, "qkv launch");
+  }
 
   // 5. attention (norm + rope + append + split-K + sink + gate), packed output
   AttnParams a = make_attn(&g, w.qp, w.kp, w.vp, L->q_norm, L->k_norm, L->rope, L->sinks,
@@ -773,7 +784,9 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     o.out_m = m;
     o.ss_out = w.ss1;
   }
-  if ((e = launch_gemv(1, nt, kEpiStore, o, tiles_of(H), w.gemv, st)) != cudaSuccess)
+  o.epi = kEpiStore;
+  const bool fused_tail = rows && !L->moe;  // o, gate/up, down and lm_head in one launch
+  if (!fused_tail && (e = launch_gemv(1, nt, kEpiStore, o, tiles_of(H), w.gemv, st)) != cudaSuccess)
     return cuda_fail(e, "o_proj launch");
 
   float* u2 = out->d_u2 ? out->d_u2 : w.u2;
@@ -801,7 +814,8 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     gu.out_xs = w.xsa;
     gu.out_m = m;
     gu.err = err;
-    if ((e = launch_gemv(2, nt, kEpiSwiglu, gu, tiles_of(I), w.gemv, st)) != cudaSuccess)
+    gu.epi = kEpiSwiglu;
+    if (!fused_tail && (e = launch_gemv(2, nt, kEpiSwiglu, gu, tiles_of(I), w.gemv, st)) != cudaSuccess)
       return cuda_fail(e, "gate/up launch");
     // 9. u2 = u1 + W_down h
     GemvParams dn = {};
@@ -820,7 +834,8 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     dn.out_xs = w.xsb;
     dn.out_m = 1;
     dn.ss_out = w.ss2;
-    if ((e = launch_gemv(1, nt, kEpiStore, dn, tiles_of(H), w.gemv, st)) != cudaSuccess)
+    dn.epi = kEpiStore;
+    if (!fused_tail && (e = launch_gemv(1, nt, kEpiStore, dn, tiles_of(H), w.gemv, st)) != cudaSuccess)
       return cuda_fail(e, "down launch");
     // 10-11. lm_head + argmax of RMSNorm(u2[m-1]) * final_norm (folded)
     GemvParams hd = {};
@@ -844,8 +859,15 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     hd.am_value = out->d_value;
     hd.logits = out->d_logits;
     hd.err = err;
-    if ((e = launch_gemv(1, 1, kEpiArgmax, hd, tiles_of(L->vocab), w.gemv, st)) != cudaSuccess)
+    hd.epi = kEpiArgmax;
+    if (fused_tail) {
+      GemvParams ph[4] = {o, gu, dn, hd};
+      const int tl[4] = {tiles_of(H), tiles_of(I), tiles_of(H), tiles_of(L->vocab)};
+      if ((e = launch_gemv_rows(ph, tl, 4, w.gemv, err, st)) != cudaSuccess)
+        return cuda_fail(e, "o_proj + gate/up + down + lm head launch");
+    } else if ((e = launch_gemv(1, 1, kEpiArgmax, hd, tiles_of(L->vocab), w.gemv, st)) != cudaSuccess) {
       return cuda_fail(e, "lm head launch");
+    }
     return MTP_OK;
   }
 

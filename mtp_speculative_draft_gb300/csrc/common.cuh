@@ -21,7 +21,13 @@ struct WsHeader {
 };
 static_assert(sizeof(WsHeader) == 1024, "workspace header is 1 KB");
 
-enum DevErr : int { kErrNone = 0, kErrMbarTimeout = 1 };
+// Device error word of a workspace (first error wins).
+enum DevErr : int {
+  kErrNone = 0,
+  kErrMbarTimeout = 1,   // a wait for a TMA copy gave up
+  kErrBadToken = 2,      // a token id outside [0, vocab) (row 0 used instead)
+  kErrPhaseTimeout = 3,  // a wait for the previous phase of a one-row launch gave up
+};
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -141,6 +147,12 @@ __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
   return v;
+}
+
+// Orders this thread's earlier (acquired) view of global memory before its
+// later bulk-copy (async proxy) reads of it.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 __device__ __forceinline__ void set_dev_error(int* err, int code) {

@@ -119,17 +119,16 @@ size_t gemv_scratch_part_bytes() {
   return (size_t)sm_count() * 16 * 32 * 32 * sizeof(float);
 }
 
-// Stage depth of each warp's pipeline and whether m = 1 activations are
-// staged through shared memory (compile-time tuning knobs).
+// Stage depth of each warp's pipeline (compile-time tuning knob).
 #ifndef MTP_GEMV_STAGES
 #define MTP_GEMV_STAGES 2
 #endif
 
-template <int NMAT, int NT, int EPI, int XM, bool C1, bool PAIRED = false>
+template <int NMAT, int NT, int EPI, int XM, bool PAIRED = false>
 static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
                                  cudaStream_t st) {
   constexpr int S = MTP_GEMV_STAGES;
-  auto kern = gemv_tc_kernel<NMAT, NT, EPI, S, XM, C1, PAIRED>;
+  auto kern = gemv_tc_kernel<NMAT, NT, EPI, S, XM, PAIRED>;
   const int smem = gemv_smem_bytes<NMAT, S, XM>();
   static thread_local int configured_dev = -1;
   static thread_local int ctas_per_sm = 1;
@@ -166,29 +165,83 @@ static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
+cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
+                             const GemvScratch& sc, int* err, cudaStream_t st) {
+  constexpr int S = MTP_GEMV_STAGES;
+  auto kern = gemv_row_kernel<S>;
+  const int smem = kGemvWarps * S * (kRowCode + kRowRest) + 2048;  // + barriers, alignment
+  static_assert(sizeof(StreamParams) <= 32764, "kernel parameters fit the 32 KB limit");
+  if (nphase < 1 || nphase > kMaxPhases) return cudaErrorInvalidValue;
+  static thread_local int configured_dev = -1;
+  static thread_local int ctas_per_sm = 1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (configured_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    int nb = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kGemvWarps * 32, smem);
+    if (e != cudaSuccess) return e;
+    ctas_per_sm = nb > 0 ? nb : 1;
+    configured_dev = dev;
+  }
+  // every CTA must be resident at once (phases wait on each other's tiles)
+  const int warps_cap = sm_count() * ctas_per_sm * kGemvWarps;
+  StreamParams sp = {};
+  int max_units = 1;
+  for (int q = 0; q < nphase; ++q) {
+    GemvParams& p = ph[q];
+    if (p.m != 1 || (q + 1 < nphase && p.epi == kEpiArgmax)) return cudaErrorInvalidValue;
+    const int um = p.epi == kEpiSwiglu ? 2 : 1;
+    const int KS = (p.K / kGroup + 7) / 8;
+    const Plan pl = plan_split(tiles[q], KS, warps_cap, 1, um, sc);  // 32 floats per unit
+    if (pl.ksplit == 0) return cudaErrorInvalidValue;  // scratch too small for the split
+    p.um = um;
+    p.ksplit = pl.ksplit;
+    p.spu = pl.spu;
+    p.part = sc.part;
+    p.tile_cnt = sc.cnt;
+    p.err = err;
+    if (pl.units > max_units) max_units = pl.units;
+    sp.ph[q] = p;
+  }
+  sp.nphase = nphase;
+  sp.phase_done = sc.phase_done;
+  sp.err = err;
+  const int warps = max_units < warps_cap ? max_units : warps_cap;
+  const int grid = (warps + kGemvWarps - 1) / kGemvWarps;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kGemvWarps * 32);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr = pdl_attr();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kern, sp);
+}
+
 cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
                         const GemvScratch& sc, cudaStream_t st) {
   const int m = p.m;
-  // activations staged per stage by bulk copy for up to 4 columns
-  const bool c1 = (m == 1);
-  constexpr int X1 = 1;  // one activation row: staged with each weight stage
-  if (epi == kEpiArgmax) {
-    if (m != 1) return cudaErrorInvalidValue;
-    return launch_gemv_t<1, 1, kEpiArgmax, X1, true>(p, tiles, sc, st);
+  if (m == 1) {  // one activation row: the one-row kernel, a single phase
+    if ((epi == kEpiSwiglu) != (nmat == 2) || nt != 1) return cudaErrorInvalidValue;
+    p.epi = epi;
+    return launch_gemv_rows(&p, &tiles, 1, sc, p.err, st);
   }
+  if (epi == kEpiArgmax) return cudaErrorInvalidValue;
+  // activations staged per stage by bulk copy for up to 4 columns
   if (nmat == 1) {
     if (epi != kEpiStore) return cudaErrorInvalidValue;
-    if (nt == 2) return launch_gemv_t<1, 2, kEpiStore, 0, false>(p, tiles, sc, st);
-    if (c1) return launch_gemv_t<1, 1, kEpiStore, X1, true>(p, tiles, sc, st);
-    if (m <= 4) return launch_gemv_t<1, 1, kEpiStore, 4, false>(p, tiles, sc, st);
-    return launch_gemv_t<1, 1, kEpiStore, 0, false>(p, tiles, sc, st);
+    if (nt == 2) return launch_gemv_t<1, 2, kEpiStore, 0>(p, tiles, sc, st);
+    if (m <= 4) return launch_gemv_t<1, 1, kEpiStore, 4>(p, tiles, sc, st);
+    return launch_gemv_t<1, 1, kEpiStore, 0>(p, tiles, sc, st);
   }
   // SwiGLU: gate (slot mat) and up (slot mat + 1) tiles are separate units
   if (epi != kEpiSwiglu) return cudaErrorInvalidValue;
-  if (nt == 2) return launch_gemv_t<1, 2, kEpiSwiglu, 0, false, true>(p, tiles, sc, st);
-  if (c1) return launch_gemv_t<1, 1, kEpiSwiglu, X1, true, true>(p, tiles, sc, st);
-  if (m <= 4) return launch_gemv_t<1, 1, kEpiSwiglu, 4, false, true>(p, tiles, sc, st);
-  return launch_gemv_t<1, 1, kEpiSwiglu, 0, false, true>(p, tiles, sc, st);
+  if (nt == 2) return launch_gemv_t<1, 2, kEpiSwiglu, 0, true>(p, tiles, sc, st);
+  if (m <= 4) return launch_gemv_t<1, 1, kEpiSwiglu, 4, true>(p, tiles, sc, st);
+  return launch_gemv_t<1, 1, kEpiSwiglu, 0, true>(p, tiles, sc, st);
 }
 
 cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float2* xs, cudaStream_t st) {

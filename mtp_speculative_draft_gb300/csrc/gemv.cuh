@@ -127,6 +127,8 @@ struct GemvParams {
   const int* rowsel;     // routed expert ids (device), or null
   const float* segw;     // routed weights (device), or null
   int rowsel_after_wait; // 1: rowsel is produced by the previous kernel
+  int epi;               // one-row kernel: kEpiStore / kEpiSwiglu / kEpiArgmax
+  int um;                // one-row kernel: 2 when gate (mat) and up (mat + 1) are separate units
   // K-segment mode (MoE down projection): K = nkseg * kseg_len
   int kseg_len;          // 0: off
   int nkseg;
@@ -248,11 +250,12 @@ struct Cursor {
     start(p, u + W, units, ksplit, spu, KS, um);
     return true;
   }
-  // weight coordinates of the current stage
+  // weight coordinates of the current stage (GS groups of 32 columns per stage)
+  template <int GS = 8>
   __device__ __forceinline__ void coords(const GemvParams& p, int& m_out, int& r_out, int& kx,
                                          int& sx) const {
     if (p.kseg_len > 0) {
-      const int spk = p.kseg_len / 256;
+      const int spk = p.kseg_len / (GS * kGroup);
       const int kj = ks / spk;
       const int kin = ks - kj * spk;
       const int lt = row;  // row holds lt * 32 in this mode (no sel on the segment)
@@ -263,25 +266,276 @@ struct Cursor {
         m_out = p.kseg_last_mat;
         r_out = lt;
       }
-      kx = kin * 32;
-      sx = kin * 8;
+      kx = kin * GS * 4;
+      sx = kin * GS;
     } else {
       m_out = mat;
       r_out = row;
-      kx = ks * 32;
-      sx = ks * 8;
+      kx = ks * GS * 4;
+      sx = ks * GS;
     }
   }
 };
 
-template <int NMAT, int NT, int EPI, int S, int XM, bool C1, bool PAIRED = false>
+// ------------------------------------------------------------ shared parts
+// Accumulator fragments of one weight matrix: [row tile rt][column tile nt][e],
+// e = 0: (row gid, column 2tq), 1: (gid, 2tq + 1), 2: (gid + 8, 2tq), 3: (gid + 8, 2tq + 1)
+// of the m16n8 tile; rows are output rows, columns activation rows.
+
+// Per-lane output scales of a folded input RMSNorm for the activation rows
+// this lane's fragments hold (column c = nt*8 + 2tq + e); with `one_row`
+// every fragment holds activation row 0.
+template <int NT>
+__device__ __forceinline__ void row_scales(const GemvParams& p, int m, int tq, bool one_row,
+                                           float (&rsc)[NT][2]) {
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) rsc[nt][0] = rsc[nt][1] = 1.f;
+  if (!p.in_ss) return;
+  for (int c = 0; c < m; ++c) {
+    const float ss = warp_col_sum(p.in_ss, p.in_ss_n, m, c);
+    const float r = rsqrtf(ss / (float)p.in_ss_dim + p.in_ss_eps);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e)
+        if (one_row || nt * 8 + 2 * tq + e == c) rsc[nt][e] = r;
+  }
+}
+
+// Deterministic split-K (and SwiGLU gate/up pairing): the unit stores its
+// NACC-float fragment partial and clears `acc`; the last of the tile's
+// um * ksplit units to finish sums the partials in k order into fin[um] and
+// returns true.
+template <int NACC, int UMAX>
+__device__ __forceinline__ bool splitk_finish(const GemvParams& p, int unit, int tile, int um,
+                                              int ksplit, float* acc, float (&fin)[UMAX][NACC],
+                                              int lane) {
+  float4* mine = reinterpret_cast<float4*>(p.part) + ((size_t)unit * 32 + lane) * (NACC / 4);
+#pragma unroll
+  for (int q = 0; q < NACC / 4; ++q)
+    mine[q] = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+  __threadfence();
+  __syncwarp();
+  unsigned prev = 0;
+  if (lane == 0) prev = atomicAdd(p.tile_cnt + tile, 1u);
+  prev = __shfl_sync(0xffffffffu, prev, 0);
+#pragma unroll
+  for (int q = 0; q < NACC; ++q) acc[q] = 0.f;
+  if (prev != (unsigned)(um * ksplit) - 1) return false;
+  __threadfence();
+  // k order is fixed (deterministic); loads of four partials are issued
+  // together so their L2 latencies overlap
+  const size_t pstride = (size_t)32 * (NACC / 4);
+#pragma unroll
+  for (int u2 = 0; u2 < UMAX; ++u2) {
+    if (u2 >= um) break;
+    float* aw = fin[u2];
+#pragma unroll
+    for (int q = 0; q < NACC; ++q) aw[q] = 0.f;
+    const float4* src0 = reinterpret_cast<const float4*>(p.part) +
+                         ((size_t)(tile * um + u2) * ksplit * 32 + lane) * (NACC / 4);
+    int s2 = 0;
+    for (; s2 + 4 <= ksplit; s2 += 4) {
+      float4 v[4][NACC / 4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q = 0; q < NACC / 4; ++q) v[u][q] = __ldcg(src0 + (s2 + u) * pstride + q);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int q = 0; q < NACC / 4; ++q) {
+          aw[4 * q] += v[u][q].x;
+          aw[4 * q + 1] += v[u][q].y;
+          aw[4 * q + 2] += v[u][q].z;
+          aw[4 * q + 3] += v[u][q].w;
+        }
+    }
+    for (; s2 < ksplit; ++s2) {
+#pragma unroll
+      for (int q = 0; q < NACC / 4; ++q) {
+        const float4 v = __ldcg(src0 + s2 * pstride + q);
+        aw[4 * q] += v.x;
+        aw[4 * q + 1] += v.y;
+        aw[4 * q + 2] += v.z;
+        aw[4 * q + 3] += v.w;
+      }
+    }
+  }
+  if (lane == 0) p.tile_cnt[tile] = 0u;  // leave the counter cleared
+  return true;
+}
+
+// Store epilogue: out = f (+ res); optionally packs the stored rows times
+// pack_w into out_xp/out_xs and writes the tile's sums of squares (a folded
+// RMSNorm of the next projection).
+template <int NT>
+__device__ __forceinline__ void epi_store(const GemvParams& p, const GemvSeg& sg, int lt, int m,
+                                          const float (&f)[2][NT][4], int gid, int tq) {
+  const int rbase = lt * 32;
+  const bool packing = p.pack_w != nullptr;  // full tiles, one segment (checked by the host)
+  const int g_out = (sg.out_col0 + rbase) / kGroup;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float ssq[2] = {0.f, 0.f};
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
+        const int row = rbase + rloc;
+        const int c = nt * 8 + 2 * tq + (e & 1);
+        if (row < sg.n && c < m) {
+          const size_t o = (size_t)c * sg.ld + sg.out_col0 + row;
+          float v = f[rt][nt][e];
+          if (sg.res) v += __ldcg(sg.res + o);
+          sg.out[o] = v;
+          if (packing && c >= p.pack_c0) {
+            const float2 hs = xp_store_elem(p.out_xp, p.out_m, g_out, c - p.pack_c0, rloc >> 3,
+                                            rloc & 7, v * p.pack_w[sg.out_col0 + row]);
+            part[e & 1].x += hs.x;
+            part[e & 1].y += hs.y;
+            ssq[e & 1] = fmaf(v, v, ssq[e & 1]);
+          }
+        }
+      }
+    if (packing) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float2 v = part[e];
+        float q2 = ssq[e];
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+          v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+          v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+          q2 += __shfl_xor_sync(0xffffffffu, q2, o);
+        }
+        const int c = nt * 8 + 2 * tq + e;
+        if (gid == 0 && c < m && c >= p.pack_c0) {
+          p.out_xs[g_out * p.out_m + (c - p.pack_c0)] = v;
+          p.ss_out[lt * p.out_m + (c - p.pack_c0)] = q2;
+        }
+      }
+    }
+  }
+}
+
+// SwiGLU epilogue: h = silu(gate) * up (times the routed weight), packed
+// for the next projection (and optionally stored).
+template <int NT>
+__device__ __forceinline__ void epi_swiglu(const GemvParams& p, const GemvSeg& sg, int lt,
+                                           const float (&g)[2][NT][4], const float (&u)[2][NT][4],
+                                           int gid, int tq) {
+  const int rbase = lt * 32;
+  const float scale = sg.w_idx >= 0 ? p.segw[sg.w_idx] : 1.f;
+  const int g_out = (sg.out_col0 + rbase) / kGroup;
+#pragma unroll
+  for (int nt = 0; nt < NT; ++nt) {
+    float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
+        const int c = nt * 8 + 2 * tq + (e & 1);
+        const float gv = g[rt][nt][e], uv = u[rt][nt][e];
+        const float hv = gv / (1.f + __expf(-gv)) * uv * scale;
+        if (c < p.out_m) {
+          const float2 hs = xp_store_elem(p.out_xp, p.out_m, g_out, c, rloc >> 3, rloc & 7, hv);
+          part[e & 1].x += hs.x;
+          part[e & 1].y += hs.y;
+          if (sg.out) sg.out[(size_t)c * sg.ld + sg.out_col0 + rbase + rloc] = hv;
+        }
+      }
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      float2 v = part[e];
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+      }
+      const int c = nt * 8 + 2 * tq + e;
+      if (gid == 0 && c < p.out_m) p.out_xs[g_out * p.out_m + c] = v;
+    }
+  }
+}
+
+// Argmax epilogue over activation row 0: logits (optional) and the lane's best key.
+__device__ __forceinline__ void epi_argmax(const GemvParams& p, const GemvSeg& sg, int lt,
+                                           const float (&f)[2][1][4], int gid, int tq,
+                                           unsigned long long& best) {
+  const int rbase = lt * 32;
+#pragma unroll
+  for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+    for (int e = 0; e < 4; e += 2) {
+      const int row = rbase + rt * 16 + gid + ((e & 2) ? 8 : 0);
+      if (tq == 0 && row < sg.n) {
+        const float v = f[rt][0][e];
+        if (p.logits) p.logits[row] = v;
+        const unsigned long long key = argmax_key(v, row);
+        best = key > best ? key : best;
+      }
+    }
+}
+
+// CTA-wide argmax, then the grid's: the last CTA to finish writes the token
+// and value.  Every thread of every CTA calls this once.
+__device__ __forceinline__ void argmax_finish(const GemvParams& p, unsigned long long best) {
+  __shared__ unsigned long long red[kGemvWarps];
+  __shared__ bool last;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+    best = other > best ? other : best;
+  }
+  if (lane == 0) red[warp] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long b = red[0];
+    for (int w2 = 1; w2 < kGemvWarps; ++w2) b = red[w2] > b ? red[w2] : b;
+    p.am_partial[blockIdx.x] = b;
+    __threadfence();
+    const unsigned prev = atomicAdd(p.am_counter, 1u);
+    last = (prev == gridDim.x - 1);
+  }
+  __syncthreads();
+  if (last) {
+    __threadfence();
+    unsigned long long b = 0ull;
+    for (int i2 = threadIdx.x; i2 < (int)gridDim.x; i2 += blockDim.x) {
+      const unsigned long long v = __ldcg(p.am_partial + i2);
+      b = v > b ? v : b;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long other = __shfl_xor_sync(0xffffffffu, b, o);
+      b = other > b ? other : b;
+    }
+    if (lane == 0) red[warp] = b;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      unsigned long long bb = red[0];
+      for (int w2 = 1; w2 < kGemvWarps; ++w2) bb = red[w2] > bb ? red[w2] : bb;
+      *p.am_token = argmax_key_index(bb);
+      *p.am_value = argmax_key_value(bb);
+      *p.am_counter = 0u;  // leave the workspace cleared for the next call
+    }
+  }
+}
+
+// ------------------------------------------------------- several activation rows
+// m in 2..16: the m16n8 tiles' columns are activation rows (NT tiles of 8).
+template <int NMAT, int NT, int EPI, int S, int XM, bool PAIRED = false>
 __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 2)
     gemv_tc_kernel(const __grid_constant__ GemvParams p) {
   // PAIRED: the SwiGLU gate and up matrices of a tile are separate work
   // units (one matrix in flight per warp); their partial sums meet in the
   // split-K reduction.
   constexpr int UM = PAIRED ? 2 : 1;
-  static_assert(!C1 || (XM == 1 && NMAT == 1 && NT == 1), "one-row layout: staged activations");
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   // 1024-byte alignment of each codes tile is required by the 128B swizzle.
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -307,11 +561,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
   const int total_tiles = p.seg[p.nseg - 1].tile_end;
   const int units = total_tiles * UM * ksplit;
 
-  __shared__ __align__(16) uint4 zero_b[16];  // B fragments of lanes outside their group's column
-  if constexpr (C1) {
-    if (threadIdx.x < 16) zero_b[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
-    __syncthreads();
-  }
   if (lane == 0) {
     for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
     mbar_fence_init();
@@ -377,26 +626,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     }
   }
   // (after the first activation copies are in flight: these loads wait on L2)
-  // per-lane output scales of the activation rows this lane's fragments hold
   float rsc[NT][2];
-#pragma unroll
-  for (int nt = 0; nt < NT; ++nt) rsc[nt][0] = rsc[nt][1] = 1.f;
-  if (p.in_ss) {
-    for (int c = 0; c < m; ++c) {
-      const float ss = warp_col_sum(p.in_ss, p.in_ss_n, m, c);
-      const float r = rsqrtf(ss / (float)p.in_ss_dim + p.in_ss_eps);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int e = 0; e < 2; ++e)
-          if (nt * 8 + 2 * tq + e == c || (C1 && c == 0)) rsc[nt][e] = r;
-    }
-  }
-  if constexpr (EPI == kEpiArgmax) {
-    if (p.normed_out && blockIdx.x == 0)
-      for (int k = threadIdx.x; k < p.K; k += blockDim.x)
-        p.normed_out[k] = p.normed_src[k] * rsc[0][0] * p.normed_w[k];
-  }
+  row_scales<NT>(p, m, tq, false, rsc);
 
   float acc[NMAT][2][NT][4];
 #pragma unroll
@@ -407,7 +638,6 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
         for (int e = 0; e < 4; ++e) acc[mi][rt][nt][e] = 0.f;
-  unsigned long long best = 0ull;  // argmax key (0 < any real key)
 
   // ldmatrix addressing: lane supplies row ri + 8*(mtx&1) of a 16-row tile
   // and group 2*jp + (mtx>>1).  With the 128-byte swizzle that group's chunk
@@ -418,19 +648,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
   const uint32_t ld_c = (uint32_t)(((mtx >> 1) ^ ri) << 4);
   const int sb_lane = gid * 8;  // float offset of row gid in a [32][8] scale tile
 
-  // one-row layout (C1): code chunks of this lane's groups, the B-fragment
-  // source of this lane (its group's hi or lo part, or zeros)
-  const int a_chunk[2] = {((2 * tq) ^ gid) << 4, ((2 * tq + 1) ^ gid) << 4};
-  const bool b_active = (gid >> 1) == tq;
-  const int b_off = (gid >> 1) * 2 * 8 + (gid & 1);
   uint4 bh[2][NT], bl[2][NT];      // activation fragments of the next pair of groups
   float2 xs0[2][NT], xs1[2][NT];
   bool b_ready = false;
   for (int i = 0; cc.u < units; ++i) {
     const int slot = i % S;
     if (!mbar_wait_bounded(&bars[slot], (uint32_t)((i / S) & 1))) {
-      // give up on the remaining work of this warp; the CTA-level epilogue
-      // below still runs so no thread is left waiting at a barrier
+      // give up on the remaining work of this warp
       if (lane == 0) set_dev_error(p.err, kErrMbarTimeout);
       break;
     }
@@ -438,10 +662,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     const uint8_t* rs = rest_base + slot * kRest;
     const int gbase = cc.ks * 8;
 
-    // B fragments (activations) of a pair of groups and their (sum,
-    // correction) pairs.  For one activation row every lane loads column 0:
-    // lanes of the other columns only feed accumulator columns that are
-    // never read, so no predicate is needed.
+    // B fragments (activations) of a pair of groups and their group sums.
     auto load_b_at = [&](int gb, int jp, uint4 (&bh)[2][NT], uint4 (&bl)[2][NT],
                          float2 (&x0)[2][NT], float2 (&x1)[2][NT]) {
       const uint4* xp_st = p.xp + (size_t)(gb * m) * 8;
@@ -451,31 +672,29 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
         const int j = 2 * jp + h;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          {
-            bh[h][nt] = make_uint4(0, 0, 0, 0);
-            bl[h][nt] = make_uint4(0, 0, 0, 0);
-            x0[h][nt] = make_float2(0.f, 0.f);
-            x1[h][nt] = make_float2(0.f, 0.f);
-            const int c = nt * 8 + gid;
-            const int c0 = nt * 8 + 2 * tq;
-            if constexpr (XM > 0) {
-              const uint4* xps = reinterpret_cast<const uint4*>(rs + NMAT * 2048);
-              const float2* xss = reinterpret_cast<const float2*>(rs + NMAT * 2048 + XM * 1024);
-              if (c < m) {
-                bh[h][nt] = xps[xp_index(j, c, tq, 0, m)];
-                bl[h][nt] = xps[xp_index(j, c, tq, 1, m)];
-              }
-              if (c0 < m) x0[h][nt] = xss[j * m + c0];
-              if (c0 + 1 < m) x1[h][nt] = xss[j * m + c0 + 1];
-            } else {
-              if (c < m) {
-                const uint4* src = xp_st + xp_index(j, c, tq, 0, m);
-                bh[h][nt] = __ldg(src);
-                bl[h][nt] = __ldg(src + 1);
-              }
-              if (c0 < m) x0[h][nt] = __ldg(xs_st + j * m + c0);
-              if (c0 + 1 < m) x1[h][nt] = __ldg(xs_st + j * m + c0 + 1);
+          bh[h][nt] = make_uint4(0, 0, 0, 0);
+          bl[h][nt] = make_uint4(0, 0, 0, 0);
+          x0[h][nt] = make_float2(0.f, 0.f);
+          x1[h][nt] = make_float2(0.f, 0.f);
+          const int c = nt * 8 + gid;
+          const int c0 = nt * 8 + 2 * tq;
+          if constexpr (XM > 0) {
+            const uint4* xps = reinterpret_cast<const uint4*>(rs + NMAT * 2048);
+            const float2* xss = reinterpret_cast<const float2*>(rs + NMAT * 2048 + XM * 1024);
+            if (c < m) {
+              bh[h][nt] = xps[xp_index(j, c, tq, 0, m)];
+              bl[h][nt] = xps[xp_index(j, c, tq, 1, m)];
             }
+            if (c0 < m) x0[h][nt] = xss[j * m + c0];
+            if (c0 + 1 < m) x1[h][nt] = xss[j * m + c0 + 1];
+          } else {
+            if (c < m) {
+              const uint4* src = xp_st + xp_index(j, c, tq, 0, m);
+              bh[h][nt] = __ldg(src);
+              bl[h][nt] = __ldg(src + 1);
+            }
+            if (c0 < m) x0[h][nt] = __ldg(xs_st + j * m + c0);
+            if (c0 + 1 < m) x1[h][nt] = __ldg(xs_st + j * m + c0 + 1);
           }
         }
       }
@@ -486,20 +705,389 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     // the next pair's activations into the same registers (their latency
     // overlaps the scale/bias epilogue), then applies scales and biases.  The
     // last pair of a stage loads the first pair of the next stage when it
-    // continues the same unit.  Activations are zero-padded to whole stages
-    // of 8 groups.
-    if constexpr (C1) {
-      // One activation row.  The eight MMA columns carry (group, hi/lo)
-      // pairs instead of activation columns: in set st (0, 1) lane (gid, tq)
-      // feeds k-slots {2tq, 2tq+1, 2tq+8, 2tq+9} with codes of group
-      // 2tq + st of rows gid and gid + 8, and column 2j + h of B holds part h
-      // (hi, lo) of that group's activations in lane j's slots (zeros in the
-      // others).  So D[row][2tq + h] is part h of the row's product with
-      // group 2tq + st, and each lane applies the scales of its own groups.
-      const uint8_t* ct = code_base + slot * kCode;
-      const uint4* xps = reinterpret_cast<const uint4*>(rs + NMAT * 2048);
-      const float4 sxv =
-          *reinterpret_cast<const float4*>(rs + NMAT * 2048 + XM * 1024 + tq * 16);
+    // continues the same unit (global activations only).  Activations are
+    // zero-padded to whole stages of 8 groups.
+    if (!b_ready) load_b(0, bh, bl, xs0, xs1);
+    const bool next_same_unit = XM == 0 && cc.ks + 1 < cc.ke;
+#pragma unroll 1
+    for (int jp = 0; jp < 4; ++jp) {
+      const uint32_t coff = ((uint32_t)jp << 5) ^ ld_c;
+      float d[NMAT][2][2][NT][4];
+      float sx0[2][NT], sx1[2][NT];
+#pragma unroll
+      for (int h = 0; h < 2; ++h)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          sx0[h][nt] = xs0[h][nt].x;
+          sx1[h][nt] = xs1[h][nt].x;
+        }
+#pragma unroll
+      for (int mi = 0; mi < NMAT; ++mi) {
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt) {
+          // (rows 0-7, group 2jp), (rows 8-15, 2jp), (rows 0-7, 2jp+1), (rows 8-15, 2jp+1)
+          uint32_t w[4];
+          ldmatrix_x4(w[0], w[1], w[2], w[3], cd + mi * 4096 + rt * 2048 + coff);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t wa = w[2 * h], wb = w[2 * h + 1];
+            const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+            // exact codes (and 16 * codes) times 2^-24 as f16: the accumulator
+            // only ever holds sums of code * x, so its rounding stays at that scale
+            const uint32_t a0 = codes_lo_f16x2(wa);
+            const uint32_t a1 = codes_lo_f16x2(wb);
+            const uint32_t a2 = codes_hi_f16x2(wa);
+            const uint32_t a3 = codes_hi_f16x2(wb);
+            const uint32_t a4 = codes_lo_f16x2(wa8);
+            const uint32_t a5 = codes_lo_f16x2(wb8);
+            const uint32_t a6 = codes_hi_f16x2(wa8);
+            const uint32_t a7 = codes_hi_f16x2(wb8);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              float* dd = d[mi][rt][h][nt];
+              dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
+              mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bh[h][nt].x, bh[h][nt].y);
+              mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bl[h][nt].x, bl[h][nt].y);
+              mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bh[h][nt].z, bh[h][nt].w);
+              mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bl[h][nt].z, bl[h][nt].w);
+            }
+          }
+        }
+      }
+      if (jp < 3)
+        load_b(jp + 1, bh, bl, xs0, xs1);
+      else if (next_same_unit)
+        load_b_at(gbase + 8, 0, bh, bl, xs0, xs1);
+#pragma unroll
+      for (int mi = 0; mi < NMAT; ++mi) {
+        const float* ssm = reinterpret_cast<const float*>(rs + mi * 2048) + sb_lane + 2 * jp;
+        const float* bsm = ssm + 256;
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt) {
+          const float2 sa = *reinterpret_cast<const float2*>(ssm + rt * 128);
+          const float2 sb = *reinterpret_cast<const float2*>(ssm + rt * 128 + 64);
+          const float2 ba = *reinterpret_cast<const float2*>(bsm + rt * 128);
+          const float2 bb = *reinterpret_cast<const float2*>(bsm + rt * 128 + 64);
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const float s0 = h ? sa.y : sa.x, s1 = h ? sb.y : sb.x;
+            const float b0 = h ? ba.y : ba.x, b1 = h ? bb.y : bb.x;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+              const float* dd = d[mi][rt][h][nt];
+              float* a = acc[mi][rt][nt];
+              a[0] = fmaf(s0, dd[0], fmaf(b0, sx0[h][nt], a[0]));
+              a[2] = fmaf(s1, dd[2], fmaf(b1, sx0[h][nt], a[2]));
+              a[1] = fmaf(s0, dd[1], fmaf(b0, sx1[h][nt], a[1]));
+              a[3] = fmaf(s1, dd[3], fmaf(b1, sx1[h][nt], a[3]));
+            }
+          }
+        }
+      }
+    }
+    b_ready = next_same_unit;
+    __syncwarp();
+    if (lane == 0 && pc.u < units) {
+      issue_w(pc, slot);
+      issue_x(pc, slot);
+      pc.advance(p, W, units, ksplit, spu, KS, UM);
+    }
+
+    const int unit = cc.u;
+    const int tile = cc.tile;
+    const int seg = cc.seg;
+    if (!cc.advance(p, W, units, ksplit, spu, KS, UM)) continue;
+
+    // ------------------------------------------------------------ unit done
+    // fin[um] is the tile's full sum for matrix um of the unit's tile
+    constexpr int NACC = NMAT * 2 * NT * 4;
+    float fin[UM][NACC];
+    float* af = &acc[0][0][0][0];
+    if (ksplit > 1 || PAIRED) {
+      if (!splitk_finish<NACC, UM>(p, unit, tile, UM, ksplit, af, fin, lane)) continue;
+    } else {
+#pragma unroll
+      for (int q = 0; q < NACC; ++q) {
+        fin[0][q] = af[q];
+        af[q] = 0.f;
+      }
+    }
+    // undo the 2^-24 of the subnormal codes (exact) and apply the input-row
+    // scales of a folded RMSNorm; q = ((mi * 2 + rt) * NT + nt) * 4 + e
+#pragma unroll
+    for (int um = 0; um < UM; ++um)
+#pragma unroll
+      for (int q = 0; q < NACC; ++q) fin[um][q] *= kCodeScale * rsc[(q >> 2) % NT][q & 1];
+
+    const GemvSeg& sg = p.seg[seg];
+    const int lt = tile - (seg ? p.seg[seg - 1].tile_end : 0);
+    using Frag = float[2][NT][4];
+    if constexpr (EPI == kEpiStore) {
+      epi_store<NT>(p, sg, lt, m, *reinterpret_cast<const Frag*>(fin[0]), gid, tq);
+    } else if constexpr (EPI == kEpiSwiglu) {
+      const float* gf = fin[0];
+      const float* uf = PAIRED ? fin[UM - 1] : fin[0] + (NMAT - 1) * 2 * NT * 4;
+      epi_swiglu<NT>(p, sg, lt, *reinterpret_cast<const Frag*>(gf),
+                     *reinterpret_cast<const Frag*>(uf), gid, tq);
+    }
+  }
+}
+
+// ------------------------------------------------------------ one activation row
+// m = 1.  One launch streams up to kMaxPhases projections in order (the
+// phases of a layer between two dependencies on other kernels): every warp
+// walks the phases' work units with one continuous TMA pipeline, so the
+// weights of a phase are already streaming while the previous phase
+// finishes.  A phase reads its activation row only after all tiles of the
+// previous phase are written (per-phase tile counters; bounded waits).
+constexpr int kMaxPhases = 4;
+
+struct StreamParams {
+  GemvParams ph[kMaxPhases];  // m = 1; phase epilogues kEpiStore / kEpiSwiglu / kEpiArgmax (last)
+  int nphase;
+  unsigned* phase_done;       // [kMaxPhases] finished tiles per phase; zero at launch, cleared at the end
+  int* err;
+};
+
+constexpr unsigned kPhaseSpinLimit = 4u << 20;  // polls of >= 256 ns each before giving up
+
+// One-row stages: 32 rows x 8 groups, as for several rows (4 KB of codes in a
+// 128B-swizzled tile, 1 KB scales, 1 KB biases) plus the staged activations
+// of the 8 groups (1 KB) and their sums (64 B).
+constexpr int kRowCode = 4096;
+constexpr int kRowRest = 2048 + 1152;  // scales, biases, activations (128-byte multiple)
+constexpr int kRowStageTx = kStageMatBytes + 8 * (128 + 8);
+
+// Waits until *cnt >= target (acquire); false when the wait gives up.
+__device__ __forceinline__ bool wait_count(const unsigned* cnt, unsigned target) {
+  for (unsigned i = 0; i < kPhaseSpinLimit; ++i) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    if (v >= target) return true;
+    __nanosleep(256);
+  }
+  return false;
+}
+
+// Position in the phases' work units (lane 0's producer copy and every
+// lane's consumer copy are advanced identically).
+struct PhaseCursor {
+  Cursor c;
+  int ph;   // kMaxPhases (or nphase) when done
+};
+
+__device__ __forceinline__ int phase_units(const GemvParams& p) {
+  return p.seg[p.nseg - 1].tile_end * p.um * p.ksplit;
+}
+__device__ __forceinline__ int phase_ks(const GemvParams& p) { return (p.K / kGroup + 7) / 8; }
+
+// First unit of this warp in phase `ph` or a later one.
+__device__ __forceinline__ void phase_start(const StreamParams& sp, PhaseCursor& x, int ph, int gw) {
+  for (; ph < sp.nphase; ++ph) {
+    const GemvParams& p = sp.ph[ph];
+    const int units = phase_units(p);
+    if (gw < units) {
+      x.ph = ph;
+      x.c.start(p, gw, units, p.ksplit, p.spu, phase_ks(p), p.um);
+      return;
+    }
+  }
+  x.ph = sp.nphase;
+}
+
+// Advances by one stage; true when a unit just finished.
+__device__ __forceinline__ bool phase_advance(const StreamParams& sp, PhaseCursor& x, int W, int gw) {
+  const GemvParams& p = sp.ph[x.ph];
+  if (++x.c.ks < x.c.ke) return false;
+  const int units = phase_units(p);
+  const int u = x.c.u + W;
+  if (u < units)
+    x.c.start(p, u, units, p.ksplit, p.spu, phase_ks(p), p.um);
+  else
+    phase_start(sp, x, x.ph + 1, gw);
+  return true;
+}
+
+// Sum of src[32 s] for s < n in order s = 0, 1, ... (loads eight at a time).
+__device__ __forceinline__ float sum_rows(const float* src, int n) {
+  float t = 0.f;
+  int s0 = 0;
+  for (; s0 + 8 <= n; s0 += 8) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = __ldcg(src + (size_t)(s0 + j) * 32);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t += v[j];
+  }
+  float v[8];
+#pragma unroll
+  for (int j = 0; j < 8; ++j) v[j] = s0 + j < n ? __ldcg(src + (size_t)(s0 + j) * 32) : 0.f;
+#pragma unroll
+  for (int j = 0; j < 8; ++j)
+    if (s0 + j < n) t += v[j];
+  return t;
+}
+
+template <int S>
+__global__ void __launch_bounds__(kGemvWarps * 32, 3)
+    gemv_row_kernel(const __grid_constant__ StreamParams sp) {
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  // 1024-byte alignment of each codes tile is required by the 128B swizzle
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int gid = lane >> 2;
+  const int tq = lane & 3;
+  uint8_t* code_base = smem + warp * S * kRowCode;
+  uint8_t* rest_base = smem + kGemvWarps * S * kRowCode + warp * S * kRowRest;
+  uint64_t* bars =
+      reinterpret_cast<uint64_t*>(smem + kGemvWarps * S * (kRowCode + kRowRest)) + warp * S;
+  const int W = gridDim.x * kGemvWarps;
+  const int gw = warp * gridDim.x + blockIdx.x;
+
+  __shared__ __align__(16) uint4 zero_b[16];  // B fragments of lanes outside their group's column
+  if (threadIdx.x < 16) zero_b[threadIdx.x] = make_uint4(0u, 0u, 0u, 0u);
+  __syncthreads();
+  if (lane == 0) {
+    for (int i = 0; i < S; ++i) mbar_init(&bars[i], 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+
+  const uint64_t pol_w = l2_policy_evict_first();
+  const uint64_t pol_x = l2_policy_evict_last();
+  auto issue_w = [&](const PhaseCursor& c, int slot) {
+    const GemvParams& p = sp.ph[c.ph];
+    int mat, row, kx, sx;
+    c.c.coords(p, mat, row, kx, sx);
+    uint8_t* cd = code_base + slot * kRowCode;
+    uint8_t* rs = rest_base + slot * kRowRest;
+    mbar_arrive_expect_tx(&bars[slot], (uint32_t)kRowStageTx);
+    const QMat& mt = p.mat[mat];
+    tma_load_2d(cd, &mt.q, &bars[slot], kx, row, pol_w);
+    tma_load_2d(rs, &mt.s, &bars[slot], sx, row, pol_w);
+    tma_load_2d(rs + 1024, &mt.b, &bars[slot], sx, row, pol_w);
+  };
+  auto issue_x = [&](const PhaseCursor& c, int slot) {
+    const GemvParams& p = sp.ph[c.ph];
+    uint8_t* rs = rest_base + slot * kRowRest + 2048;
+    const int g0 = c.c.ks * 8;
+    bulk_load(rs, p.xp + (size_t)g0 * 8, 8 * 128, &bars[slot], pol_x);
+    bulk_load(rs + 1024, p.xs + g0, 8 * 8, &bars[slot], pol_x);
+  };
+
+  // Producer state (lane 0): pc is the next stage to issue; a stage whose
+  // phase's input is not yet complete gets its weights now and its
+  // activations once the consumer has seen that phase's input complete.
+  PhaseCursor pc, cc;
+  PhaseCursor pend_c[S];
+  bool pend[S];
+#pragma unroll
+  for (int i = 0; i < S; ++i) pend[i] = false;
+  // (slots are indexed with unrolled compares so these stay in registers)
+  auto defer_x = [&](const PhaseCursor& c, int slot) {
+#pragma unroll
+    for (int s2 = 0; s2 < S; ++s2)
+      if (s2 == slot) {
+        pend_c[s2] = c;
+        pend[s2] = true;
+      }
+  };
+  int issued = 0;  // stages issued so far (lane 0)
+  int ready = 0;   // phases <= ready have their input complete
+  const bool first_sel = sp.ph[0].rowsel_after_wait != 0;
+  if (!first_sel) {
+    phase_start(sp, pc, 0, gw);
+    cc = pc;
+    if (lane == 0)
+      for (; issued < S && pc.ph < sp.nphase && !sp.ph[pc.ph].rowsel_after_wait; ++issued) {
+        issue_w(pc, issued);
+        defer_x(pc, issued);
+        phase_advance(sp, pc, W, gw);
+      }
+  }
+  // the first phase's input comes from the previous kernel
+  pdl_wait();
+  pdl_launch_dependents();
+  if (first_sel) {
+    phase_start(sp, pc, 0, gw);
+    cc = pc;
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int s2 = 0; s2 < S; ++s2)
+      if (pend[s2] && pend_c[s2].ph == 0) {
+        issue_x(pend_c[s2], s2);
+        pend[s2] = false;
+      }
+    for (; issued < S && pc.ph < sp.nphase; ++issued) {
+      issue_w(pc, issued);
+      if (pc.ph == 0)
+        issue_x(pc, issued);
+      else
+        defer_x(pc, issued);
+      phase_advance(sp, pc, W, gw);
+    }
+  }
+
+  // The eight MMA columns carry (group, hi/lo) pairs instead of activation
+  // rows: in set st (0, 1) lane (gid, tq) feeds k-slots {2tq, 2tq+1, 2tq+8,
+  // 2tq+9} with codes of group 2tq + st of rows gid and gid + 8, and column
+  // 2j + h of B holds part h (hi, lo) of that group's activations in lane j's
+  // slots (zeros in the others).  So D[row][2tq + h] is part h of the row's
+  // product with group 2tq + st, and each lane applies its own groups' scales.
+  const int a_chunk[2] = {((2 * tq) ^ gid) << 4, ((2 * tq + 1) ^ gid) << 4};
+  const bool b_active = (gid >> 1) == tq;
+  const int b_off = (gid >> 1) * 2 * 8 + (gid & 1);
+
+  float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [row tile][row gid, gid + 8]
+  unsigned long long best = 0ull;  // argmax key (0 < any real key)
+  float rsc = 1.f;
+  int cur = -1;
+  unsigned done_here = 0;  // tiles of phase cur finished by this warp
+  bool dead = false;
+  int i = 0;
+  for (; cc.ph < sp.nphase; ++i) {
+    const int slot = i % S;
+    if (cc.ph != cur) {
+      // entering phase cc.ph: its input is the previous phase's output
+      if (cc.ph > 0) {
+        const GemvParams& pp = sp.ph[cc.ph - 1];
+        bool ok = true;
+        if (lane == 0) ok = wait_count(sp.phase_done + cc.ph - 1, (unsigned)pp.seg[pp.nseg - 1].tile_end);
+        ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+        if (!ok) {
+          if (lane == 0) set_dev_error(sp.err, kErrPhaseTimeout);
+          dead = true;
+          break;
+        }
+      }
+      cur = cc.ph;
+      if (lane == 0) {
+        fence_proxy_async_global();  // the copies below read what the wait acquired
+        ready = cur;
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2)
+          if (pend[s2] && pend_c[s2].ph <= ready) {
+            issue_x(pend_c[s2], s2);
+            pend[s2] = false;
+          }
+      }
+      float r[1][2];
+      row_scales<1>(sp.ph[cur], 1, tq, true, r);
+      rsc = r[0][0];
+    }
+    if (!mbar_wait_bounded(&bars[slot], (uint32_t)((i / S) & 1))) {
+      if (lane == 0) set_dev_error(sp.err, kErrMbarTimeout);
+      dead = true;
+      break;
+    }
+    {
+      const uint8_t* ct = code_base + slot * kRowCode;
+      const uint8_t* rs = rest_base + slot * kRowRest;
+      const uint4* xps = reinterpret_cast<const uint4*>(rs + 2048);
+      const float4 sxv = *reinterpret_cast<const float4*>(rs + 2048 + 1024 + tq * 16);
       const uint4* bsrc = b_active ? xps + b_off : zero_b;
       uint4 B[2][4];
 #pragma unroll
@@ -537,356 +1125,146 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
                           codes_hi_f16x2(y1), B[st][w].z, B[st][w].w);
           }
         }
-        float* a = acc[0][rt][0];
-        a[0] = fmaf(s0.x, d[0][0] + d[0][1], fmaf(b0.x, sxv.x, a[0]));
-        a[0] = fmaf(s0.y, d[1][0] + d[1][1], fmaf(b0.y, sxv.z, a[0]));
-        a[2] = fmaf(s1.x, d[0][2] + d[0][3], fmaf(b1.x, sxv.x, a[2]));
-        a[2] = fmaf(s1.y, d[1][2] + d[1][3], fmaf(b1.y, sxv.z, a[2]));
+        acc[rt][0] = fmaf(s0.x, d[0][0] + d[0][1], fmaf(b0.x, sxv.x, acc[rt][0]));
+        acc[rt][0] = fmaf(s0.y, d[1][0] + d[1][1], fmaf(b0.y, sxv.z, acc[rt][0]));
+        acc[rt][1] = fmaf(s1.x, d[0][2] + d[0][3], fmaf(b1.x, sxv.x, acc[rt][1]));
+        acc[rt][1] = fmaf(s1.y, d[1][2] + d[1][3], fmaf(b1.y, sxv.z, acc[rt][1]));
       }
-    } else {
-      if (!b_ready) load_b(0, bh, bl, xs0, xs1);
-      // (staged activations live in the stage's own buffer: no early load then)
-      const bool next_same_unit = XM == 0 && cc.ks + 1 < cc.ke;
-  #pragma unroll 1
-      for (int jp = 0; jp < 4; ++jp) {
-        const uint32_t coff = ((uint32_t)jp << 5) ^ ld_c;
-        float d[NMAT][2][2][NT][4];
-        float sx0[2][NT], sx1[2][NT];
-  #pragma unroll
-        for (int h = 0; h < 2; ++h)
-  #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) {
-            sx0[h][nt] = xs0[h][nt].x;
-            sx1[h][nt] = xs1[h][nt].x;
-          }
-  #pragma unroll
-        for (int mi = 0; mi < NMAT; ++mi) {
-  #pragma unroll
-          for (int rt = 0; rt < 2; ++rt) {
-            // (rows 0-7, group 2jp), (rows 8-15, 2jp), (rows 0-7, 2jp+1), (rows 8-15, 2jp+1)
-            uint32_t w[4];
-            ldmatrix_x4(w[0], w[1], w[2], w[3], cd + mi * 4096 + rt * 2048 + coff);
-  #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const uint32_t wa = w[2 * h], wb = w[2 * h + 1];
-              const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
-              // exact codes (and 16 * codes) times 2^-24 as f16: the accumulator
-              // only ever holds sums of code * x, so its rounding stays at that scale
-              const uint32_t a0 = codes_lo_f16x2(wa);
-              const uint32_t a1 = codes_lo_f16x2(wb);
-              const uint32_t a2 = codes_hi_f16x2(wa);
-              const uint32_t a3 = codes_hi_f16x2(wb);
-              const uint32_t a4 = codes_lo_f16x2(wa8);
-              const uint32_t a5 = codes_lo_f16x2(wb8);
-              const uint32_t a6 = codes_hi_f16x2(wa8);
-              const uint32_t a7 = codes_hi_f16x2(wb8);
-  #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                float* dd = d[mi][rt][h][nt];
-                dd[0] = dd[1] = dd[2] = dd[3] = 0.f;
-                mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bh[h][nt].x, bh[h][nt].y);
-                mma_f16_16816(d[mi][rt][h][nt], a0, a1, a2, a3, bl[h][nt].x, bl[h][nt].y);
-                mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bh[h][nt].z, bh[h][nt].w);
-                mma_f16_16816(d[mi][rt][h][nt], a4, a5, a6, a7, bl[h][nt].z, bl[h][nt].w);
-              }
-            }
-          }
-        }
-        if (jp < 3)
-          load_b(jp + 1, bh, bl, xs0, xs1);
-        else if (next_same_unit)
-          load_b_at(gbase + 8, 0, bh, bl, xs0, xs1);
-  #pragma unroll
-        for (int mi = 0; mi < NMAT; ++mi) {
-          const float* ssm = reinterpret_cast<const float*>(rs + mi * 2048) + sb_lane + 2 * jp;
-          const float* bsm = ssm + 256;
-  #pragma unroll
-          for (int rt = 0; rt < 2; ++rt) {
-            const float2 sa = *reinterpret_cast<const float2*>(ssm + rt * 128);
-            const float2 sb = *reinterpret_cast<const float2*>(ssm + rt * 128 + 64);
-            const float2 ba = *reinterpret_cast<const float2*>(bsm + rt * 128);
-            const float2 bb = *reinterpret_cast<const float2*>(bsm + rt * 128 + 64);
-  #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-              const float s0 = h ? sa.y : sa.x, s1 = h ? sb.y : sb.x;
-              const float b0 = h ? ba.y : ba.x, b1 = h ? bb.y : bb.x;
-  #pragma unroll
-              for (int nt = 0; nt < NT; ++nt) {
-                const float* dd = d[mi][rt][h][nt];
-                float* a = acc[mi][rt][nt];
-                a[0] = fmaf(s0, dd[0], fmaf(b0, sx0[h][nt], a[0]));
-                a[2] = fmaf(s1, dd[2], fmaf(b1, sx0[h][nt], a[2]));
-                if constexpr (!C1) {
-                  a[1] = fmaf(s0, dd[1], fmaf(b0, sx1[h][nt], a[1]));
-                  a[3] = fmaf(s1, dd[3], fmaf(b1, sx1[h][nt], a[3]));
-                }
-              }
-            }
-          }
-        }
-      }
-      b_ready = next_same_unit;
     }
     __syncwarp();
-    if (lane == 0 && pc.u < units) {
+    if (lane == 0 && pc.ph < sp.nphase) {  // refill the slot
       issue_w(pc, slot);
-      issue_x(pc, slot);
-      pc.advance(p, W, units, ksplit, spu, KS, UM);
+      if (pc.ph <= ready)
+        issue_x(pc, slot);
+      else
+        defer_x(pc, slot);
+      ++issued;
+      phase_advance(sp, pc, W, gw);
     }
 
-    const int unit = cc.u;
-    const int tile = cc.tile;
-    const int seg = cc.seg;
-    if (!cc.advance(p, W, units, ksplit, spu, KS, UM)) continue;
-    if constexpr (C1) {
-      // a row's four lanes each hold two groups per stage: sum them (fixed order)
-#pragma unroll
-      for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          float v = acc[0][rt][0][e];
-          v += __shfl_xor_sync(0xffffffffu, v, 1);
-          v += __shfl_xor_sync(0xffffffffu, v, 2);
-          acc[0][rt][0][e] = v;
-        }
-    }
+    const int ph = cc.ph;
+    const int unit = cc.c.u, tile = cc.c.tile, seg = cc.c.seg;
+    if (!phase_advance(sp, cc, W, gw)) continue;
 
     // ------------------------------------------------------------ unit done
-    // fin[um] is the tile's full sum for matrix um of the unit's tile
-    float fin[UM][NMAT][2][NT][4];
-    if (ksplit > 1 || PAIRED) {
-      // Deterministic split-K: every unit stores its fragment partial; the
-      // last unit of a tile to finish sums them in k order.
-      constexpr int NACC = NMAT * 2 * NT * 4;
-      float4* mine = reinterpret_cast<float4*>(p.part) + ((size_t)unit * 32 + lane) * (NACC / 4);
-      const float* af = &acc[0][0][0][0];
+    // a row's four lanes each hold two groups per stage: sum them in a fixed
+    // order; then lane (gid, tq) keeps tile row rr (one row per lane)
 #pragma unroll
-      for (int q = 0; q < NACC / 4; ++q)
-        mine[q] = make_float4(af[4 * q], af[4 * q + 1], af[4 * q + 2], af[4 * q + 3]);
+    for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = acc[rt][e];
+        v += __shfl_xor_sync(0xffffffffu, v, 1);
+        v += __shfl_xor_sync(0xffffffffu, v, 2);
+        acc[rt][e] = v;
+      }
+    const int rr = (tq >> 1) * 16 + (tq & 1) * 8 + gid;
+    float g = (tq & 2) ? ((tq & 1) ? acc[1][1] : acc[1][0]) : ((tq & 1) ? acc[0][1] : acc[0][0]);
+    acc[0][0] = acc[0][1] = acc[1][0] = acc[1][1] = 0.f;
+    const GemvParams& p = sp.ph[ph];
+    const GemvSeg& sg = p.seg[seg];
+    const int lt = tile - (seg ? p.seg[seg - 1].tile_end : 0);
+    const int row = lt * 32 + rr;
+    const bool row_ok = row < sg.n;
+    // what the epilogue reads, loaded before the split-K round trips
+    float resv = 0.f, pw = 0.f;
+    if (p.epi == kEpiStore && row_ok) {
+      if (sg.res) resv = __ldcg(sg.res + sg.out_col0 + row);
+      if (p.pack_w) pw = __ldg(p.pack_w + sg.out_col0 + row);
+    }
+    float u = 0.f;
+    bool fin = true;
+    if (p.ksplit > 1 || p.um > 1) {
+      // deterministic split-K (and gate/up pairing): each unit stores its 32
+      // rows; the last of the tile's units sums them in k order
+      p.part[(size_t)unit * 32 + lane] = g;
       __threadfence();
       __syncwarp();
       unsigned prev = 0;
       if (lane == 0) prev = atomicAdd(p.tile_cnt + tile, 1u);
       prev = __shfl_sync(0xffffffffu, prev, 0);
-#pragma unroll
-      for (int mi = 0; mi < NMAT; ++mi)
-#pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) acc[mi][rt][nt][e] = 0.f;
-      if (prev != (unsigned)(UM * ksplit) - 1) continue;
-      __threadfence();
-      // k order is fixed (deterministic); loads of four partials are issued
-      // together so their L2 latencies overlap
-      const size_t pstride = (size_t)32 * (NACC / 4);
-#pragma unroll
-      for (int um = 0; um < UM; ++um) {
-        float* aw = &fin[um][0][0][0][0];
-#pragma unroll
-        for (int q = 0; q < NACC; ++q) aw[q] = 0.f;
-        const float4* src0 = reinterpret_cast<const float4*>(p.part) +
-                             ((size_t)(tile * UM + um) * ksplit * 32 + lane) * (NACC / 4);
-        int s2 = 0;
-        for (; s2 + 4 <= ksplit; s2 += 4) {
-          float4 v[4][NACC / 4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int q = 0; q < NACC / 4; ++q) v[u][q] = __ldcg(src0 + (s2 + u) * pstride + q);
-#pragma unroll
-          for (int u = 0; u < 4; ++u)
-#pragma unroll
-            for (int q = 0; q < NACC / 4; ++q) {
-              aw[4 * q] += v[u][q].x;
-              aw[4 * q + 1] += v[u][q].y;
-              aw[4 * q + 2] += v[u][q].z;
-              aw[4 * q + 3] += v[u][q].w;
-            }
-        }
-        for (; s2 < ksplit; ++s2) {
-#pragma unroll
-          for (int q = 0; q < NACC / 4; ++q) {
-            const float4 v = __ldcg(src0 + s2 * pstride + q);
-            aw[4 * q] += v.x;
-            aw[4 * q + 1] += v.y;
-            aw[4 * q + 2] += v.z;
-            aw[4 * q + 3] += v.w;
-          }
-        }
+      fin = prev == (unsigned)(p.um * p.ksplit) - 1;
+      if (fin) {
+        __threadfence();
+        const float* src = p.part + (size_t)tile * p.um * p.ksplit * 32 + lane;
+        g = sum_rows(src, p.ksplit);
+        if (p.um > 1) u = sum_rows(src + (size_t)p.ksplit * 32, p.ksplit);
+        if (lane == 0) p.tile_cnt[tile] = 0u;  // leave the counter cleared
       }
-      if (lane == 0) p.tile_cnt[tile] = 0u;  // leave the counter cleared
-    } else {
-#pragma unroll
-      for (int mi = 0; mi < NMAT; ++mi)
-#pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              fin[0][mi][rt][nt][e] = acc[mi][rt][nt][e];
-              acc[mi][rt][nt][e] = 0.f;
-            }
     }
-    // undo the 2^-24 of the subnormal codes (exact) and apply the input-row
-    // scales of a folded RMSNorm
+    if (fin) {
+      // undo the 2^-24 of the subnormal codes (exact), apply a folded RMSNorm
+      g *= kCodeScale * rsc;
+      u *= kCodeScale * rsc;
+      const int g_out = (sg.out_col0 + lt * 32) / kGroup;
+      if (p.epi == kEpiStore) {
+        const float v = g + resv;
+        if (row_ok) sg.out[sg.out_col0 + row] = v;
+        if (p.pack_w) {  // full tiles (checked by the host)
+          float2 hs = xp_store_elem(p.out_xp, 1, g_out, 0, rr >> 3, rr & 7, v * pw);
+          float q2 = v * v;
 #pragma unroll
-    for (int um = 0; um < UM; ++um)
-#pragma unroll
-      for (int mi = 0; mi < NMAT; ++mi)
-#pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) fin[um][mi][rt][nt][e] *= kCodeScale * rsc[nt][e & 1];
-
-    // ---------------------------------------------------------- epilogue
-    const GemvSeg& sg = p.seg[seg];
-    const int lt = tile - (seg ? p.seg[seg - 1].tile_end : 0);
-    const int rbase = lt * 32;
-    if constexpr (EPI == kEpiStore) {
-      const bool packing = p.pack_w != nullptr;  // full tiles, one segment (checked by the host)
-      const int g_out = (sg.out_col0 + rbase) / kGroup;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-        float ssq[2] = {0.f, 0.f};
-#pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
-            const int row = rbase + rloc;
-            const int c = nt * 8 + 2 * tq + (e & 1);
-            if (row < sg.n && c < m) {
-              const size_t o = (size_t)c * sg.ld + sg.out_col0 + row;
-              float v = fin[0][0][rt][nt][e];
-              if (sg.res) v += sg.res[o];
-              sg.out[o] = v;
-              if (packing && c >= p.pack_c0) {
-                const float2 hs = xp_store_elem(p.out_xp, p.out_m, g_out, c - p.pack_c0,
-                                                rloc >> 3, rloc & 7,
-                                                v * p.pack_w[sg.out_col0 + row]);
-                part[e & 1].x += hs.x;
-                part[e & 1].y += hs.y;
-                ssq[e & 1] = fmaf(v, v, ssq[e & 1]);
-              }
-            }
+          for (int o = 1; o < 32; o <<= 1) {
+            hs.x += __shfl_xor_sync(0xffffffffu, hs.x, o);
+            hs.y += __shfl_xor_sync(0xffffffffu, hs.y, o);
+            q2 += __shfl_xor_sync(0xffffffffu, q2, o);
           }
-        if (packing) {
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            float2 v = part[e];
-            float q2 = ssq[e];
-#pragma unroll
-            for (int o = 4; o < 32; o <<= 1) {
-              v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-              v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-              q2 += __shfl_xor_sync(0xffffffffu, q2, o);
-            }
-            const int c = nt * 8 + 2 * tq + e;
-            if (gid == 0 && c < m && c >= p.pack_c0) {
-              p.out_xs[g_out * p.out_m + (c - p.pack_c0)] = v;
-              p.ss_out[lt * p.out_m + (c - p.pack_c0)] = q2;
-            }
+          if (lane == 0) {
+            p.out_xs[g_out] = hs;
+            p.ss_out[lt] = q2;
           }
         }
+      } else if (p.epi == kEpiSwiglu) {
+        const float scale = sg.w_idx >= 0 ? p.segw[sg.w_idx] : 1.f;
+        const float hv = g / (1.f + __expf(-g)) * u * scale;
+        float2 hs = xp_store_elem(p.out_xp, 1, g_out, 0, rr >> 3, rr & 7, hv);
+        if (sg.out) sg.out[sg.out_col0 + lt * 32 + rr] = hv;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          hs.x += __shfl_xor_sync(0xffffffffu, hs.x, o);
+          hs.y += __shfl_xor_sync(0xffffffffu, hs.y, o);
+        }
+        if (lane == 0) p.out_xs[g_out] = hs;
+      } else {
+        if (row_ok) {
+          if (p.logits) p.logits[row] = g;
+          const unsigned long long key = argmax_key(g, row);
+          best = key > best ? key : best;
+        }
+        if (tile == 0 && p.normed_out)
+          for (int k = lane; k < p.K; k += 32)
+            p.normed_out[k] = __ldcg(p.normed_src + k) * rsc * p.normed_w[k];
       }
-    } else if constexpr (EPI == kEpiSwiglu) {
-      const float scale = sg.w_idx >= 0 ? p.segw[sg.w_idx] : 1.f;
-      const int g_out = (sg.out_col0 + rbase) / kGroup;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll
-        for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
-            const int c = nt * 8 + 2 * tq + (e & 1);
-            const float gv = PAIRED ? fin[0][0][rt][nt][e] : fin[0][0][rt][nt][e];
-            const float uv = PAIRED ? fin[UM - 1][0][rt][nt][e] : fin[0][NMAT - 1][rt][nt][e];
-            const float hv = gv / (1.f + __expf(-gv)) * uv * scale;
-            if (c < p.out_m) {
-              const float2 hs = xp_store_elem(p.out_xp, p.out_m, g_out, c, rloc >> 3, rloc & 7, hv);
-              part[e & 1].x += hs.x;
-              part[e & 1].y += hs.y;
-              if (sg.out) sg.out[(size_t)c * sg.ld + sg.out_col0 + rbase + rloc] = hv;
-            }
-          }
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          float2 v = part[e];
-#pragma unroll
-          for (int o = 4; o < 32; o <<= 1) {
-            v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-            v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-          }
-          const int c = nt * 8 + 2 * tq + e;
-          if (gid == 0 && c < p.out_m) p.out_xs[g_out * p.out_m + c] = v;
-        }
+      ++done_here;
+    }
+    if (cc.ph != ph) {
+      // leaving phase ph: publish this warp's finished tiles (one fence and
+      // one atomic per warp and phase); the launch's last tile clears the counters
+      __threadfence();
+      __syncwarp();
+      if (lane == 0 && done_here > 0) {
+        const unsigned tiles = (unsigned)p.seg[p.nseg - 1].tile_end;
+        const unsigned prev = atomicAdd(sp.phase_done + ph, done_here);
+        if (ph == sp.nphase - 1 && prev + done_here == tiles)
+          for (int q = 0; q < sp.nphase; ++q) sp.phase_done[q] = 0u;  // every wait has passed
       }
-    } else {  // argmax over column 0 (one activation row)
-#pragma unroll
-      for (int rt = 0; rt < 2; ++rt)
-#pragma unroll
-        for (int e = 0; e < 4; e += 2) {
-          const int row = rbase + rt * 16 + gid + ((e & 2) ? 8 : 0);
-          if (tq == 0 && row < sg.n) {
-            const float v = fin[0][0][rt][0][e];
-            if (p.logits) p.logits[row] = v;
-            const unsigned long long key = argmax_key(v, row);
-            best = key > best ? key : best;
-          }
-        }
+      done_here = 0;
     }
   }
 
-  if constexpr (EPI == kEpiArgmax) {
-    __shared__ unsigned long long red[kGemvWarps];
-    __shared__ bool last;
+  if (dead) {
+    // make every issued stage complete before the CTA can exit: issue the
+    // activations still pending (their inputs may be incomplete; the results
+    // are discarded), then wait for the stages not yet consumed
+    const int n_issued = __shfl_sync(0xffffffffu, issued, 0);
+    if (lane == 0)
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
-      best = other > best ? other : best;
-    }
-    if (lane == 0) red[warp] = best;
-    __syncthreads();
-    if (threadIdx.x == 0) {
-      unsigned long long b = red[0];
-      for (int w2 = 1; w2 < kGemvWarps; ++w2) b = red[w2] > b ? red[w2] : b;
-      p.am_partial[blockIdx.x] = b;
-      __threadfence();
-      const unsigned prev = atomicAdd(p.am_counter, 1u);
-      last = (prev == gridDim.x - 1);
-    }
-    __syncthreads();
-    if (last) {
-      __threadfence();
-      unsigned long long b = 0ull;
-      for (int i2 = threadIdx.x; i2 < (int)gridDim.x; i2 += blockDim.x) {
-        const unsigned long long v = __ldcg(p.am_partial + i2);
-        b = v > b ? v : b;
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const unsigned long long other = __shfl_xor_sync(0xffffffffu, b, o);
-        b = other > b ? other : b;
-      }
-      if (lane == 0) red[warp] = b;
-      __syncthreads();
-      if (threadIdx.x == 0) {
-        unsigned long long bb = red[0];
-        for (int w2 = 1; w2 < kGemvWarps; ++w2) bb = red[w2] > bb ? red[w2] : bb;
-        *p.am_token = argmax_key_index(bb);
-        *p.am_value = argmax_key_value(bb);
-        *p.am_counter = 0u;  // leave the workspace cleared for the next call
-      }
-    }
+      for (int s2 = 0; s2 < S; ++s2)
+        if (pend[s2]) issue_x(pend_c[s2], s2);
+    __syncwarp();
+    for (int j = i; j < n_issued; ++j) mbar_wait_bounded(&bars[j % S], (uint32_t)((j / S) & 1));
   }
+  if (sp.ph[sp.nphase - 1].epi == kEpiArgmax) argmax_finish(sp.ph[sp.nphase - 1], best);
 }
 
 // Plain CUDA-core fallback for shapes the TMA path cannot describe

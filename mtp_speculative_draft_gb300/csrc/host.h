@@ -30,16 +30,21 @@ mtp_status check_affine(const mtp_affine4* w, int n, int k, const char* name, bo
 
 // Workspace regions a GEMV launch may use for split-K partial sums.
 struct GemvScratch {
-  float* part;       // partial fragments
+  float* part;          // partial fragments
   size_t part_bytes;
-  unsigned* cnt;     // per-tile completion counters (cleared)
+  unsigned* cnt;        // per-tile completion counters (cleared)
   int cnt_len;
+  unsigned* phase_done; // [kMaxPhases] per-phase tile counters of the one-row kernel (cleared)
 };
 size_t gemv_scratch_part_bytes();
 constexpr int kGemvCounters = 4096;
 
 // Launch helpers (programmatic dependent launch on `stream`).  Fills in the
 // split-K plan of `p` (ksplit, spu, part, tile_cnt) from the scratch given.
+// One-row (m = 1) projections in order in one launch: phase q reads its
+// activation row only after every tile of phase q - 1 is written.
+cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
+                             const GemvScratch& sc, int* err, cudaStream_t st);
 cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
                         const GemvScratch& scratch, cudaStream_t stream);
 cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float2* xs, cudaStream_t st);

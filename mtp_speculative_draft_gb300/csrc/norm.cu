@@ -34,7 +34,7 @@ __device__ __forceinline__ const float* seg_row(const NormSeg& s, int c, int* er
   if (s.table) {
     int tok = s.tokens[c];
     if (tok < 0 || tok >= s.vocab) {
-      set_dev_error(err, 2);
+      set_dev_error(err, kErrBadToken);
       tok = 0;
     }
     return s.table + (size_t)tok * s.dim;
