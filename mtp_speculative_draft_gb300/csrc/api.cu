@@ -112,9 +112,9 @@ static GemvScratch carve_scratch(Carve& cv) {
 }
 
 // Counter slots inside WsHeader::counters.
-constexpr int kCntAttn = 0;      // [n_kv] (n_kv <= 64)
-constexpr int kCntArgmax = 64;
-constexpr int kCntRouter = 65;
+constexpr int kCntAttn = 0;      // [2 * n_kv] arrivals and departures (n_kv <= 64)
+constexpr int kCntArgmax = 128;
+constexpr int kCntRouter = 129;
 
 static GemvSeg plain_seg(int tiles_end, int n, int mat, float* out, int ld, const float* res) {
   GemvSeg s = {};
@@ -1002,7 +1002,7 @@ mtp_status attn_decode_sink_noalloc(const mtp_attn_geom* g, const float* d_qp, c
   void* scratch = nullptr;
   s = noalloc_scratch(&scratch);
   if (s != MTP_OK) return s;
-  cudaError_t e = cudaMemsetAsync(header(scratch)->counters + kCntAttn, 0, sizeof(unsigned) * 64,
+  cudaError_t e = cudaMemsetAsync(header(scratch)->counters + kCntAttn, 0, sizeof(unsigned) * 128,
                                   static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attn_decode_sink_noalloc: clearing the counters");
   return attn_decode_sink(g, d_qp, d_kp, d_vp, d_q_norm, d_k_norm, d_rope, d_sinks, d_k_cache,

@@ -7,7 +7,7 @@
 // apply_sigmoid_gate_multiply) and "cortiq-engine 0.8.49 src/mimo_mtp.rs"
 // (sliding window, per-head sinks).
 //
-// Split-K over the cache, about one CTA per SM.  A CTA serves every query
+// Split-K over the cache, at most one CTA per SM.  A CTA serves every query
 // row of its KV head (grouped-query sharing of the K/V stream: G heads x m
 // new rows).  It owns `nbuf` tile buffers of 32 keys; each buffer is read by
 // `qgroups` warps, each of which holds a slice of the query rows.  Warps work
@@ -21,10 +21,10 @@
 //     of shared memory and are read back four keys at a time.
 // The buffers' states meet once in shared memory and the CTA writes one
 // partial.  The m new keys and values are normalised/rotated, appended to the
-// cache by the last split and attended to from shared memory.  The last CTA
-// of a KV head to finish (completion counter, no spinning) merges the
-// partials, adds the sink to the denominator, applies the gate and writes the
-// output as fp32 and packed for the o_proj GEMV.
+// cache by the last split and attended to from shared memory.  The splits of
+// a KV head then wait (bounded) for each other's partials and each merges a
+// slice of whole 32-dim groups: adds the sink to the denominator, applies the
+// gate and writes the output as fp32 and packed for the o_proj GEMV.
 #include "host.h"
 
 namespace mtp {
@@ -113,6 +113,17 @@ __device__ __forceinline__ void warp_norm_rope(float* v, const float* src, int d
   if (post_scale != 1.f)
     for (int i = lane; i < d; i += 32) v[i] *= post_scale;
   __syncwarp();
+}
+
+// Waits (one thread, bounded) until *cnt >= target; acquire.
+__device__ __forceinline__ bool wait_count_cta(const unsigned* cnt, unsigned target) {
+  for (unsigned i = 0; i < (4u << 20); ++i) {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
+    if (v >= target) return true;
+    __nanosleep(128);
+  }
+  return false;
 }
 
 // Named-barrier AND-reduction over `count` threads (all of them arrive).
@@ -272,7 +283,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   float* newv = reinterpret_cast<float*>(smraw + Ly.newv_off);
   float* ps = reinterpret_cast<float*>(smraw + Ly.ps_off) + (size_t)warp * kAttnQMax * kTileKeys;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smraw + Ly.bar_off);
-  __shared__ bool last;
+  __shared__ bool arrived;
 
   // this warp: buffer b, query rows [q0, q0 + nq) in slots [qgi * QM, qgi * QM + QM)
   const int b = warp / qgroups, qgi = warp % qgroups;
@@ -426,136 +437,100 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
       a.part[(pidx + q) * 2 + 1] = l;
     }
   }
+  // ---- all splits of this KV head publish their partials, then each merges
+  // one slice of the head's output (whole 32-dim groups, for the packed copy)
+  const int ns = a.nsplit;
   __threadfence();
   __syncthreads();
   if (tid == 0) {
-    const unsigned prev = atomicAdd(&a.counters[kvh], 1u);
-    last = (prev == (unsigned)a.nsplit - 1);
+    atomicAdd(&a.counters[kvh], 1u);
+    arrived = wait_count_cta(&a.counters[kvh], (unsigned)ns);
+    if (!arrived) set_dev_error(a.err, kErrMbarTimeout);
   }
   __syncthreads();
-  if (!last) return;
-  __threadfence();
-
-  // ---- merge across splits (last CTA of this KV head)
-  const int ns = a.nsplit;
-  float* wsm = reinterpret_cast<float*>(smraw);        // [ns][QG] split weights
-  float* lsm = wsm + ns * QG;                          // [ns][QG] split denominators
-  float* fin = lsm + ns * QG;                          // [QG][dv]
+  if (!arrived) return;
   const size_t base = (size_t)kvh * ns * QG;
-  const int dv4 = dv / 4;
-  const int items = QG * dv4;
-  const size_t sstride = (size_t)QG * dv4;
-  // The first kMergePre partial outputs and the gate of this thread's first
-  // item are loaded together with the (M, l) pairs: one round trip to L2.
-  constexpr int kMergePre = 16;
-  float4 gate = make_float4(0.f, 0.f, 0.f, 0.f);
-  float4 pre[kMergePre];
-  if (tid < items) {
-    const int qi = tid / dv4, d4 = tid - qi * dv4;
-    const float4* po = reinterpret_cast<const float4*>(part_o + (base + qi) * dv) + d4;
-#pragma unroll
-    for (int u = 0; u < kMergePre; ++u)
-      pre[u] = u < ns ? __ldcg(po + (size_t)u * sstride) : make_float4(0.f, 0.f, 0.f, 0.f);
-    if (a.gated) {
-      const int r = qi / G, h = kvh * G + qi % G;
-      gate = *reinterpret_cast<const float4*>(a.qp + (size_t)r * q_rows + (size_t)h * dqk * 2 +
-                                              dqk + d4 * 4);
-    }
+  const int gpq = dv / kGroup;                 // 32-dim groups per query row
+  const int ngroups = QG * gpq;
+  const int g0 = split * ngroups / ns, g1 = (split + 1) * ngroups / ns;
+  const int nit = (g1 - g0) * 8;               // float4 items of the slice
+  // smem: split weights [ns][QG], denominators [ns][QG], partial outputs of
+  // the slice [ns][nit] float4, merged slice [nit] float4 (tile buffers are free)
+  float* wsm = reinterpret_cast<float*>(smraw);
+  float* lsm = wsm + ns * QG;
+  float4* osm = reinterpret_cast<float4*>(smraw + (((size_t)2 * ns * QG * 4 + 15) / 16) * 16);
+  float4* fsm = osm + (size_t)ns * nit;
+  // one round trip: (M, l) pairs and the slice's partials, all loads in flight
+  for (int i2 = tid; i2 < ns * QG; i2 += nthreads) {
+    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part) + base + i2);
+    wsm[i2] = ml.x;
+    lsm[i2] = ml.y;
   }
-  for (int i = tid; i < ns * QG; i += nthreads) {
-    const float2 ml = __ldcg(reinterpret_cast<const float2*>(a.part) + base + i);
-    wsm[i] = ml.x;
-    lsm[i] = ml.y;
+  for (int i2 = tid; i2 < ns * nit; i2 += nthreads) {
+    const int sp2 = i2 / nit, it = i2 - sp2 * nit;
+    const int gg = g0 + it / 8;                // group of the head's output
+    const int qi = gg / gpq, d4 = (gg - qi * gpq) * 8 + (it & 7);
+    osm[i2] = __ldcg(reinterpret_cast<const float4*>(part_o + ((size_t)(kvh * ns + sp2) * QG + qi) * dv) + d4);
   }
   __syncthreads();
-  // one warp per query row: lanes over the splits
-  for (int q = warp; q < QG; q += nw) {
+  // split weights of the slice's rows: one warp per row, lanes over the splits
+  const int q_lo = (g0 * kGroup) / dv, q_hi = g1 > g0 ? ((g1 - 1) * kGroup) / dv : q_lo - 1;
+  for (int q = q_lo + warp; q <= q_hi; q += nw) {
     const int h = kvh * G + q % G;
     const float sinkl2 = a.sinks ? a.sinks[h] * kLog2e : kNegBig;
     float M = sinkl2;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, wsm[s * QG + q]);
+    for (int s2 = lane; s2 < ns; s2 += 32) M = fmaxf(M, wsm[s2 * QG + q]);
     M = warp_max(M);
     float den = 0.f;
-    for (int s = lane; s < ns; s += 32) den += exp2f(wsm[s * QG + q] - M) * lsm[s * QG + q];
+    for (int s2 = lane; s2 < ns; s2 += 32) den += exp2f(wsm[s2 * QG + q] - M) * lsm[s2 * QG + q];
     den = warp_sum(den) + (a.sinks ? exp2f(sinkl2 - M) : 0.f);
     const float inv = den > 0.f ? 1.f / den : 0.f;
     __syncwarp();
-    for (int s = lane; s < ns; s += 32) wsm[s * QG + q] = exp2f(wsm[s * QG + q] - M) * inv;
+    for (int s2 = lane; s2 < ns; s2 += 32) wsm[s2 * QG + q] = exp2f(wsm[s2 * QG + q] - M) * inv;
   }
   __syncthreads();
-  for (int it = tid; it < items; it += nthreads) {
-    const int qi = it / dv4, d4 = it - qi * dv4;
-    const float4* po = reinterpret_cast<const float4*>(part_o + (base + qi) * dv) + d4;
+  for (int it = tid; it < nit; it += nthreads) {
+    const int gg = g0 + it / 8;
+    const int qi = gg / gpq, d4 = (gg - qi * gpq) * 8 + (it & 7);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    int s = 0;
-    if (it == tid) {
-#pragma unroll
-      for (int u = 0; u < kMergePre; ++u) {
-        const float w = u < ns ? wsm[u * QG + qi] : 0.f;
-        acc.x = fmaf(w, pre[u].x, acc.x);
-        acc.y = fmaf(w, pre[u].y, acc.y);
-        acc.z = fmaf(w, pre[u].z, acc.z);
-        acc.w = fmaf(w, pre[u].w, acc.w);
-      }
-      s = ns < kMergePre ? ns : kMergePre;
-    }
-    for (; s + 8 <= ns; s += 8) {  // eight independent loads in flight
-      float4 v[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) v[u] = __ldcg(po + (size_t)(s + u) * sstride);
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float w = wsm[(s + u) * QG + qi];
-        acc.x = fmaf(w, v[u].x, acc.x);
-        acc.y = fmaf(w, v[u].y, acc.y);
-        acc.z = fmaf(w, v[u].z, acc.z);
-        acc.w = fmaf(w, v[u].w, acc.w);
-      }
-    }
-    for (; s < ns; ++s) {
-      const float4 v = __ldcg(po + (size_t)s * sstride);
-      const float w = wsm[s * QG + qi];
+    for (int s2 = 0; s2 < ns; ++s2) {  // k order: deterministic
+      const float w = wsm[s2 * QG + qi];
+      const float4 v = osm[s2 * nit + it];
       acc.x = fmaf(w, v.x, acc.x);
       acc.y = fmaf(w, v.y, acc.y);
       acc.z = fmaf(w, v.z, acc.z);
       acc.w = fmaf(w, v.w, acc.w);
     }
-    float o[4] = {acc.x, acc.y, acc.z, acc.w};
     if (a.gated) {
-      float4 g = gate;
-      if (it != tid) {
-        const int r = qi / G, h = kvh * G + qi % G;
-        g = *reinterpret_cast<const float4*>(a.qp + (size_t)r * q_rows + (size_t)h * dqk * 2 +
-                                             dqk + d4 * 4);
-      }
-      o[0] = o[0] / (1.f + __expf(-g.x));
-      o[1] = o[1] / (1.f + __expf(-g.y));
-      o[2] = o[2] / (1.f + __expf(-g.z));
-      o[3] = o[3] / (1.f + __expf(-g.w));
+      const int r = qi / G, h = kvh * G + qi % G;
+      const float4 g = *reinterpret_cast<const float4*>(a.qp + (size_t)r * q_rows +
+                                                        (size_t)h * dqk * 2 + dqk + d4 * 4);
+      acc.x = acc.x / (1.f + __expf(-g.x));
+      acc.y = acc.y / (1.f + __expf(-g.y));
+      acc.z = acc.z / (1.f + __expf(-g.z));
+      acc.w = acc.w / (1.f + __expf(-g.w));
     }
-#pragma unroll
-    for (int e = 0; e < 4; ++e) fin[qi * dv + d4 * 4 + e] = o[e];
+    fsm[it] = acc;
   }
   __syncthreads();
-  // fp32 output and packed copy: octets of (row, head, dims)
-  const int oct_per_q = dv / 8;
-  const int total_oct = QG * oct_per_q;
-  for (int o0 = 0; o0 < total_oct; o0 += nthreads) {
+  // fp32 output and packed copy: octets (two float4 items) of the slice
+  const int noct = nit / 2;
+  for (int o0 = 0; o0 < noct; o0 += nthreads) {
     const int oi = o0 + tid;
     float2 sum = make_float2(0.f, 0.f);
     int r = 0, k = 0;
-    if (oi < total_oct) {
-      const int qi = oi / oct_per_q, oc = oi - qi * oct_per_q;
+    if (oi < noct) {
+      const int gg = g0 + oi / 4;
+      const int qi = gg / gpq;
       r = qi / G;
       const int h = kvh * G + qi % G;
-      k = h * dv + oc * 8;
-      float v[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) v[i] = fin[qi * dv + oc * 8 + i];
+      k = h * dv + (gg - qi * gpq) * kGroup + (oi & 3) * 8;
+      const float4 v0 = fsm[2 * oi], v1 = fsm[2 * oi + 1];
+      float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
       if (a.out) {
         float4* dst = reinterpret_cast<float4*>(a.out + (size_t)r * a.nh * dv + k);
-        dst[0] = make_float4(v[0], v[1], v[2], v[3]);
-        dst[1] = make_float4(v[4], v[5], v[6], v[7]);
+        dst[0] = v0;
+        dst[1] = v1;
       }
       if (a.out_xp) {
         uint4 hi, lo;
@@ -566,25 +541,34 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
       }
     }
     if (a.out_xp) {
-      // the four octets of a group are adjacent (dv % 32 == 0, blockDim % 32 == 0)
+      // the four octets of a group are adjacent lanes (groups start at multiples of 4)
       sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 1);
       sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
       sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
       sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 2);
-      if (oi < total_oct && (oi & 3) == 0) a.out_xs[(k / kGroup) * a.m + r] = sum;
+      if (oi < noct && (oi & 3) == 0) a.out_xs[(k / kGroup) * a.m + r] = sum;
     }
   }
-  if (tid == 0) a.counters[kvh] = 0u;
+  // leave the counters cleared once every split has read the arrivals
+  __syncthreads();
+  if (tid == 0) {
+    const unsigned prev = atomicAdd(&a.counters[a.nkv + kvh], 1u);
+    if (prev == (unsigned)ns - 1) {
+      a.counters[kvh] = 0u;
+      a.counters[a.nkv + kvh] = 0u;
+    }
+  }
 }
 
 // ------------------------------------------------------------------ host side
 static int ceil_div(int a, int b) { return (a + b - 1) / b; }
 
 // Upper bound of the split count for `cached` keys in the window (sizes the
-// partials); attn_splits never exceeds it and it grows with `cached`.
+// partials); attn_splits never exceeds it and it grows with `cached`.  At
+// most one CTA per SM: the splits of a KV head wait for each other.
 int attn_splits_bound(int nkv, int cached) {
   const int ntiles = ceil_div(cached, kTileKeys);
-  int ns = ceil_div(sm_count(), nkv);  // about one CTA per SM
+  int ns = sm_count() / nkv;
   if (ns > ntiles) ns = ntiles;
   return ns < 1 ? 1 : ns;
 }
@@ -702,7 +686,11 @@ cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
   const AttnLayout Ly = attn_layout(a.dqk, a.dv, qslots, a.m, nbuf, nw);
   // the tile buffers are reused for the buffers' states, then the merge
   const size_t combine = ((size_t)kAttnMaxWarps * kAttnQMax * 2 + (size_t)nw * qm * a.dv) * 4;
-  const size_t merge = (size_t)a.nsplit * QG * 8 + (size_t)QG * a.dv * 4;
+  // the merge of one split: weights and denominators [ns][QG], its slice's
+  // partials [ns][items] and merged items (float4 items, 8 per 32-dim group)
+  const int ngroups = QG * a.dv / kGroup;
+  const size_t items = (size_t)ceil_div(ngroups, a.nsplit) * 8;
+  const size_t merge = ((size_t)2 * a.nsplit * QG * 4 + 15) / 16 * 16 + (a.nsplit + 1) * items * 16;
   size_t smem = Ly.total;
   if (combine > smem) smem = combine;
   if (merge > smem) smem = merge;

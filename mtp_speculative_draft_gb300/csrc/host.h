@@ -84,7 +84,7 @@ struct alignas(64) AttnParams {
   uint4* out_xp;       // packed output for the next projection (may be null)
   float2* out_xs;
   float* part;         // partials
-  unsigned* counters;  // [nkv]
+  unsigned* counters;  // [2 * nkv] arrivals, departures
   int nsplit;
   int nbuf;            // tile buffers per CTA (set by launch_attn)
   int qgroups;         // warps per buffer, each with a slice of the query rows (set by launch_attn)
