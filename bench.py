@@ -440,7 +440,7 @@ def run_ours(args):
                    "parallelism": "replicas" if world > 1 else "single GPU"},
         "algorithmic_bytes_per_step": total_bytes,
         "hbm_gbs_step": total_bytes / (ms * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "gemv_tc_kernel<1,1,argmax> (lm_head)",
+        "roofline": {"bound": "hbm", "kernel": "gemv_row_kernel: lm_head projection + argmax, timed alone",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind, "traffic": traffic,
                      "algorithmic_bytes_per_launch": head_bytes, "launch_ms": head_ms},

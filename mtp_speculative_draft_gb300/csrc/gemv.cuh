@@ -163,7 +163,8 @@ struct GemvParams {
   const float* pack_w;
   int pack_c0;
   float* ss_out;
-  // Argmax epilogue: CTA 0 also writes normed_out[k] = normed_src[k] * r[0] * normed_w[k]
+  // Argmax epilogue: tiles t < K / 32 also write normed_out[k] = normed_src[k] * r[0] * normed_w[k]
+  // for k in [32 t, 32 t + 32)
   const float* normed_src;
   const float* normed_w;
   float* normed_out;
@@ -1231,9 +1232,10 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
           const unsigned long long key = argmax_key(g, row);
           best = key > best ? key : best;
         }
-        if (tile == 0 && p.normed_out)
-          for (int k = lane; k < p.K; k += 32)
-            p.normed_out[k] = __ldcg(p.normed_src + k) * rsc * p.normed_w[k];
+        // the first K / 32 tiles also write the normed input row, 32 values each
+        const int kn = lt * 32 + lane;
+        if (p.normed_out && kn < p.K)
+          p.normed_out[kn] = __ldcg(p.normed_src + kn) * rsc * p.normed_w[kn];
       }
       ++done_here;
     }
