@@ -106,7 +106,7 @@ static GemvScratch carve_scratch(Carve& cv) {
   sc.part_bytes = gemv_scratch_part_bytes();
   sc.part = cv.take<float>(sc.part_bytes);
   sc.cnt = cv.take<unsigned>(sizeof(unsigned) * kGemvCounters);
-  sc.cnt_len = kGemvCounters - kMaxPhases;
+  sc.cnt_len = kGemvCounters - 8;  // the last 8: phase and pre-unit counters
   sc.phase_done = sc.cnt ? sc.cnt + sc.cnt_len : nullptr;
   return sc;
 }
@@ -303,6 +303,7 @@ static AttnParams make_attn(const mtp_attn_geom* g, const float* qp, const float
   a.cap = cap;
   a.m = m;
   a.nsplit = attn_splits(a.nkv, g->window > 0 ? std::min(L, g->window - 1) : L);
+  a.merge_in_kernel = 1;
   return a;
 }
 
@@ -571,6 +572,7 @@ struct LayerWs {
   float* part;
   unsigned long long* am_partial;
   float *ss0, *ss1, *ss2;  // per-tile sums of squares of u, u1, u2 (folded RMSNorms)
+  float* ss_pre;           // per-group raw sums of squares of the embedding and hidden rows
   GemvScratch gemv;
   MoeScratch moe;
 };
@@ -610,6 +612,7 @@ static void carve_layer(Carve& cv, const mtp_layer_desc* L, int m, LayerWs* w) {
   w->ss0 = cv.take<float>(sizeof(float) * m * (H / kGroup));
   w->ss1 = cv.take<float>(sizeof(float) * m * (H / kGroup));
   w->ss2 = cv.take<float>(sizeof(float) * m * (H / kGroup));
+  w->ss_pre = cv.take<float>(sizeof(float) * 2 * (H / kGroup));
   w->gemv = carve_scratch(cv);
   if (L->moe) carve_moe(cv, L->moe, H, &w->moe);
 }
@@ -691,8 +694,29 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   segs[1].eps = 1e-6f;
   segs[1].dim = H;
   segs[1].src_ld = H;
-  if ((e = launch_norm_pack(segs, 2, m, w.xa, w.xsa, err, st)) != cudaSuccess)
+  // one activation row: consecutive projections share one launch (phases), and
+  // the embedding/hidden pack runs inside it (its RMSNorms fold into eh_proj)
+  const bool rows = (m == 1);
+  const bool pre_pack = rows && H % 256 == 0;
+  PreParams pre_a = {};
+  if (pre_pack) {
+    pre_a.kind = kPreEmbedPack;
+    pre_a.units = 2 * H / kGroup;
+    pre_a.xp = w.xa;
+    pre_a.xs = w.xsa;
+    pre_a.table = L->embed;
+    pre_a.tokens = in->d_tokens;
+    pre_a.vocab = L->vocab;
+    pre_a.rows = in->d_embed_rows;
+    pre_a.hidden = in->d_hidden;
+    pre_a.w0 = L->enorm;
+    pre_a.w1 = L->hnorm;
+    pre_a.dim = H;
+    pre_a.eps = 1e-6f;
+    pre_a.ss = w.ss_pre;
+  } else if ((e = launch_norm_pack(segs, 2, m, w.xa, w.xsa, err, st)) != cudaSuccess) {
     return cuda_fail(e, "eh norm launch");
+  }
 
   // 2. u = eh_proj [e_n ; h_n]
   GemvParams p = {};
@@ -715,8 +739,6 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   p.ss_out = w.ss0;
   p.epi = kEpiStore;
   const int nt = m > 8 ? 2 : 1;
-  // one activation row: consecutive projections share one launch (phases)
-  const bool rows = (m == 1);
   if (!rows && (e = launch_gemv(1, nt, kEpiStore, p, tiles_of(H), w.gemv, st)) != cudaSuccess)
     return cuda_fail(e, "eh_proj launch");
 
@@ -747,7 +769,8 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   if (rows) {
     GemvParams ph[2] = {p, q};
     const int tl[2] = {tiles_of(H), tq + tk + tv};
-    if ((e = launch_gemv_rows(ph, tl, 2, w.gemv, err, st)) != cudaSuccess)
+    if ((e = launch_gemv_rows(ph, tl, 2, w.gemv, err, st, pre_pack ? &pre_a : nullptr)) !=
+        cudaSuccess)
       return cuda_fail(e, "eh_proj + qkv launch");
   } else if ((e = launch_gemv(1, nt, kEpiStore, q, tq + tk + tv, w.gemv, st)) != cudaSuccess) {
     return cuda_fail(e, "qkv launch");
@@ -760,6 +783,9 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   a.counters = header(ws)->counters + kCntAttn;
   a.err = err;
   a.prefetch_before_wait = 1;  // the q/k/v projection signals only after its own wait
+  // one row, dense FFN: the next launch merges the splits before o_proj
+  const bool fused_tail = rows && !L->moe;  // o, gate/up, down and lm_head in one launch
+  a.merge_in_kernel = fused_tail ? 0 : 1;
   a.out = nullptr;
   a.out_xp = w.xa;
   a.out_xs = w.xsa;
@@ -785,7 +811,6 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     o.ss_out = w.ss1;
   }
   o.epi = kEpiStore;
-  const bool fused_tail = rows && !L->moe;  // o, gate/up, down and lm_head in one launch
   if (!fused_tail && (e = launch_gemv(1, nt, kEpiStore, o, tiles_of(H), w.gemv, st)) != cudaSuccess)
     return cuda_fail(e, "o_proj launch");
 
@@ -863,7 +888,22 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     if (fused_tail) {
       GemvParams ph[4] = {o, gu, dn, hd};
       const int tl[4] = {tiles_of(H), tiles_of(I), tiles_of(H), tiles_of(L->vocab)};
-      if ((e = launch_gemv_rows(ph, tl, 4, w.gemv, err, st)) != cudaSuccess)
+      PreParams pre_b = {};
+      pre_b.kind = kPreAttnMerge;
+      pre_b.units = g.n_heads * g.head_dim_v / kGroup;
+      pre_b.xp = w.xa;
+      pre_b.xs = w.xsa;
+      pre_b.part = w.part;
+      pre_b.part_o = attn_part_outputs(w.part, g.n_kv_heads, a.nsplit, g.n_heads / g.n_kv_heads);
+      pre_b.nkv = g.n_kv_heads;
+      pre_b.ns = a.nsplit;
+      pre_b.G = g.n_heads / g.n_kv_heads;
+      pre_b.dv = g.head_dim_v;
+      pre_b.dqk = g.head_dim_qk;
+      pre_b.gated = g.gated_q ? 1 : 0;
+      pre_b.sinks = L->sinks;
+      pre_b.qp = w.qp;
+      if ((e = launch_gemv_rows(ph, tl, 4, w.gemv, err, st, &pre_b)) != cudaSuccess)
         return cuda_fail(e, "o_proj + gate/up + down + lm head launch");
     } else if ((e = launch_gemv(1, 1, kEpiArgmax, hd, tiles_of(L->vocab), w.gemv, st)) != cudaSuccess) {
       return cuda_fail(e, "lm head launch");

@@ -440,6 +440,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   // ---- all splits of this KV head publish their partials, then each merges
   // one slice of the head's output (whole 32-dim groups, for the packed copy)
   const int ns = a.nsplit;
+  if (!a.merge_in_kernel) return;  // the next launch merges the partials
   __threadfence();
   __syncthreads();
   if (tid == 0) {
@@ -579,6 +580,10 @@ int attn_splits(int nkv, int cached) {
   if (ntiles == 0) return 1;
   const int tps = ceil_div(ntiles, bound);
   return ceil_div(ntiles, tps);  // no split without cached tiles
+}
+
+const float* attn_part_outputs(const float* part, int nkv, int nsplit, int q_per_kv) {
+  return part + attn_part_o_offset(nkv, nsplit, q_per_kv);
 }
 
 size_t attn_part_bytes(int nkv, int nsplit, int q_per_kv, int dv) {

@@ -91,11 +91,13 @@ static cudaLaunchAttribute pdl_attr() {
 struct Plan {
   int ksplit, spu, units;
 };
+// kalign > 0: units must not straddle a multiple of kalign stages.
 static Plan plan_split(int tiles, int KS, int warps_cap, int nacc, int um,
-                       const GemvScratch& sc) {
+                       const GemvScratch& sc, int kalign = 0) {
   Plan best = {0, 0, 0};
   double best_cost = 1e30;
   for (int spu = KS; spu >= 1; --spu) {
+    if (kalign > 0 && kalign % spu) continue;
     const int ksplit = (KS + spu - 1) / spu;
     if (ksplit > 1 && spu * (ksplit - 1) >= KS) continue;  // same split as a larger spu
     const long long units = (long long)tiles * um * ksplit;
@@ -166,7 +168,8 @@ static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
 }
 
 cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
-                             const GemvScratch& sc, int* err, cudaStream_t st) {
+                             const GemvScratch& sc, int* err, cudaStream_t st,
+                             const PreParams* pre) {
   constexpr int S = MTP_GEMV_STAGES;
   auto kern = gemv_row_kernel<S>;
   const int smem = kGemvWarps * S * (kRowCode + kRowRest) + 2048;  // + barriers, alignment
@@ -194,7 +197,9 @@ cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
     if (p.m != 1 || (q + 1 < nphase && p.epi == kEpiArgmax)) return cudaErrorInvalidValue;
     const int um = p.epi == kEpiSwiglu ? 2 : 1;
     const int KS = (p.K / kGroup + 7) / 8;
-    const Plan pl = plan_split(tiles[q], KS, warps_cap, 1, um, sc);  // 32 floats per unit
+    // with packed halves (kPreEmbedPack) the first phase's units stay in one half
+    const int kalign = (q == 0 && pre && pre->kind == kPreEmbedPack) ? pre->dim / 256 : 0;
+    const Plan pl = plan_split(tiles[q], KS, warps_cap, 1, um, sc, kalign);  // 32 floats per unit
     if (pl.ksplit == 0) return cudaErrorInvalidValue;  // scratch too small for the split
     p.um = um;
     p.ksplit = pl.ksplit;
@@ -208,6 +213,7 @@ cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
   sp.nphase = nphase;
   sp.phase_done = sc.phase_done;
   sp.err = err;
+  if (pre) sp.pre = *pre;
   const int warps = max_units < warps_cap ? max_units : warps_cap;
   const int grid = (warps + kGemvWarps - 1) / kGemvWarps;
   cudaLaunchConfig_t cfg = {};

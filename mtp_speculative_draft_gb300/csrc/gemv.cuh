@@ -843,12 +843,134 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
 // previous phase are written (per-phase tile counters; bounded waits).
 constexpr int kMaxPhases = 4;
 
+// Work a launch does before its first phase: units of one warp each, run
+// right after the wait on the previous kernel; the first phase's activation
+// copies wait for all of them (pre_done).
+enum PreKind : int {
+  kPreNone = 0,
+  // pack [embed(token) * enorm ; hidden * hnorm] unnormalised (one 32-value
+  // group per unit) with each group's sum of squares of the raw values; the
+  // first phase scales the units of each half by rsqrt(mean + eps)
+  kPreEmbedPack = 1,
+  // merge the split-K partials of decode attention (one 32-dim group of the
+  // output per unit): sink in the denominator, sigmoid gate, packed output
+  kPreAttnMerge = 2,
+};
+
+struct PreParams {
+  int kind;
+  int units;
+  uint4* xp;         // packed output row
+  float2* xs;
+  // kPreEmbedPack
+  const float* table;  // [vocab][dim] (or null: rows)
+  const int* tokens;
+  int vocab;
+  const float* rows;   // [dim] embedding row given directly
+  const float* hidden; // [dim]
+  const float* w0;     // enorm
+  const float* w1;     // hnorm
+  int dim;
+  float eps;
+  float* ss;           // [2 * dim / 32] raw sums of squares per group
+  // kPreAttnMerge (m = 1)
+  const float* part;   // (M, l) pairs [nkv][ns][G] then outputs [nkv][ns][G][dv] at part_o
+  const float* part_o;
+  int nkv, ns, G, dv, dqk, gated, q_rows;
+  const float* sinks;  // [nkv * G] or null
+  const float* qp;     // gate source (q projection row)
+};
+
 struct StreamParams {
   GemvParams ph[kMaxPhases];  // m = 1; phase epilogues kEpiStore / kEpiSwiglu / kEpiArgmax (last)
   int nphase;
-  unsigned* phase_done;       // [kMaxPhases] finished tiles per phase; zero at launch, cleared at the end
+  unsigned* phase_done;       // [kMaxPhases + 1] finished tiles per phase, then pre-units;
+                              // zero at launch, cleared at the end
   int* err;
+  PreParams pre;
 };
+
+// One 32-value group of [embed * enorm ; hidden * hnorm], packed unnormalised,
+// with the group's raw sum of squares (one warp).
+__device__ __forceinline__ void pre_embed_pack(const PreParams& q, int u, int* err, int lane) {
+  const int gpr = q.dim / kGroup;
+  const bool first = u < gpr;
+  const int k = (first ? u : u - gpr) * kGroup + lane;
+  const float* row;
+  if (first) {
+    if (q.table) {
+      int tok = q.tokens[0];
+      if (tok < 0 || tok >= q.vocab) {
+        if (lane == 0) set_dev_error(err, kErrBadToken);
+        tok = 0;
+      }
+      row = q.table + (size_t)tok * q.dim;
+    } else {
+      row = q.rows;
+    }
+  } else {
+    row = q.hidden;
+  }
+  const float wv = first ? q.w0[k] : q.w1[k];
+  const float x = __ldcg(row + k);
+  const float v = x * wv;
+  float2 hs = xp_store_elem(q.xp, 1, u, 0, lane >> 3, lane & 7, v);
+  float ss = x * x;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    hs.x += __shfl_xor_sync(0xffffffffu, hs.x, o);
+    hs.y += __shfl_xor_sync(0xffffffffu, hs.y, o);
+    ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  }
+  if (lane == 0) {
+    q.xs[u] = hs;
+    q.ss[u] = ss;
+  }
+}
+
+// One 32-dim group of the attention output (m = 1): merges the splits'
+// partials with weights exp2(M_s - M) / den, den including the head's sink
+// logit, applies the sigmoid gate and packs the group (one warp).  Every
+// load of a chunk of 32 splits is issued before any arithmetic.
+__device__ __forceinline__ void pre_attn_merge(const PreParams& q, int u, int lane) {
+  const int gph = q.dv / kGroup;           // groups per head
+  const int h = u / gph, d0 = (u - h * gph) * kGroup;
+  const int kvh = h / q.G, qi = h - kvh * q.G;
+  const float* ml = q.part + ((size_t)kvh * q.ns * q.G + qi) * 2;  // stride G * 2 per split
+  const float* po = q.part_o + ((size_t)kvh * q.ns * q.G + qi) * q.dv + d0 + lane;
+  const size_t sstride = (size_t)q.G * q.dv;
+  const float g = q.gated ? q.qp[(size_t)h * q.dqk * 2 + q.dqk + d0 + lane] : 0.f;
+  const float sinkl2 = q.sinks ? q.sinks[h] * 1.4426950408889634f : -1e30f;
+  // running merge over chunks of 32 splits (one chunk for up to 32 splits)
+  float Mrun = sinkl2, den = q.sinks ? 1.f : 0.f, acc = 0.f;
+  for (int s0 = 0; s0 < q.ns; s0 += 32) {
+    const int n = min(32, q.ns - s0);
+    const int sl = s0 + lane;
+    const float2 mlv = sl < q.ns ? __ldcg(reinterpret_cast<const float2*>(ml + (size_t)sl * q.G * 2))
+                                 : make_float2(-1e30f, 0.f);
+    float v[32];
+#pragma unroll
+    for (int t = 0; t < 32; ++t) v[t] = t < n ? __ldcg(po + (size_t)(s0 + t) * sstride) : 0.f;
+    const float M = fmaxf(Mrun, warp_max(mlv.x));
+    const float wl = sl < q.ns ? exp2f(mlv.x - M) : 0.f;
+    const float scale = exp2f(Mrun - M);
+    den = den * scale + warp_sum(wl * mlv.y);
+    acc *= scale;
+#pragma unroll
+    for (int t = 0; t < 32; ++t)
+      if (t < n) acc = fmaf(__shfl_sync(0xffffffffu, wl, t), v[t], acc);  // split order
+    Mrun = M;
+  }
+  acc = den > 0.f ? acc / den : 0.f;
+  if (q.gated) acc = acc / (1.f + __expf(-g));
+  float2 hs = xp_store_elem(q.xp, 1, (h * q.dv + d0) / kGroup, 0, lane >> 3, lane & 7, acc);
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    hs.x += __shfl_xor_sync(0xffffffffu, hs.x, o);
+    hs.y += __shfl_xor_sync(0xffffffffu, hs.y, o);
+  }
+  if (lane == 0) q.xs[(h * q.dv + d0) / kGroup] = hs;
+}
 
 constexpr unsigned kPhaseSpinLimit = 4u << 20;  // polls of >= 256 ns each before giving up
 
@@ -996,7 +1118,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       }
   };
   int issued = 0;  // stages issued so far (lane 0)
-  int ready = 0;   // phases <= ready have their input complete
+  // phases <= ready have their input complete (phase 0 after the previous
+  // kernel, or after this launch's pre-units)
+  int ready = sp.pre.kind != kPreNone ? -1 : 0;
   const bool first_sel = sp.ph[0].rowsel_after_wait != 0;
   if (!first_sel) {
     phase_start(sp, pc, 0, gw);
@@ -1018,18 +1142,31 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
   if (lane == 0) {
 #pragma unroll
     for (int s2 = 0; s2 < S; ++s2)
-      if (pend[s2] && pend_c[s2].ph == 0) {
+      if (pend[s2] && pend_c[s2].ph <= ready) {
         issue_x(pend_c[s2], s2);
         pend[s2] = false;
       }
     for (; issued < S && pc.ph < sp.nphase; ++issued) {
       issue_w(pc, issued);
-      if (pc.ph == 0)
+      if (pc.ph <= ready)
         issue_x(pc, issued);
       else
         defer_x(pc, issued);
       phase_advance(sp, pc, W, gw);
     }
+  }
+  // pre-units of this warp (after its first weight copies are in flight)
+  if (sp.pre.kind != kPreNone) {
+    unsigned n_pre = 0;
+    for (int u = gw; u < sp.pre.units; u += W, ++n_pre) {
+      if (sp.pre.kind == kPreEmbedPack)
+        pre_embed_pack(sp.pre, u, sp.err, lane);
+      else
+        pre_attn_merge(sp.pre, u, lane);
+    }
+    __threadfence();
+    __syncwarp();
+    if (lane == 0 && n_pre > 0) atomicAdd(sp.phase_done + kMaxPhases, n_pre);
   }
 
   // The eight MMA columns carry (group, hi/lo) pairs instead of activation
@@ -1045,6 +1182,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
   float acc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};  // [row tile][row gid, gid + 8]
   unsigned long long best = 0ull;  // argmax key (0 < any real key)
   float rsc = 1.f;
+  float seg_r[2] = {1.f, 1.f};  // per-half scales of the first phase (kPreEmbedPack)
   int cur = -1;
   unsigned done_here = 0;  // tiles of phase cur finished by this warp
   bool dead = false;
@@ -1052,11 +1190,18 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
   for (; cc.ph < sp.nphase; ++i) {
     const int slot = i % S;
     if (cc.ph != cur) {
-      // entering phase cc.ph: its input is the previous phase's output
-      if (cc.ph > 0) {
-        const GemvParams& pp = sp.ph[cc.ph - 1];
+      // entering phase cc.ph: its input is the previous phase's output (or
+      // the pre-units' output for phase 0)
+      if (cc.ph > 0 || sp.pre.kind != kPreNone) {
         bool ok = true;
-        if (lane == 0) ok = wait_count(sp.phase_done + cc.ph - 1, (unsigned)pp.seg[pp.nseg - 1].tile_end);
+        if (lane == 0) {
+          if (cc.ph > 0) {
+            const GemvParams& pp = sp.ph[cc.ph - 1];
+            ok = wait_count(sp.phase_done + cc.ph - 1, (unsigned)pp.seg[pp.nseg - 1].tile_end);
+          } else {
+            ok = wait_count(sp.phase_done + kMaxPhases, (unsigned)sp.pre.units);
+          }
+        }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
         if (!ok) {
           if (lane == 0) set_dev_error(sp.err, kErrPhaseTimeout);
@@ -1078,6 +1223,14 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       float r[1][2];
       row_scales<1>(sp.ph[cur], 1, tq, true, r);
       rsc = r[0][0];
+      if (cur == 0 && sp.pre.kind == kPreEmbedPack) {
+        // the two halves' RMSNorm scales, applied per unit (units never straddle)
+        const int gpr = sp.pre.dim / kGroup;
+        const float s0 = warp_col_sum(sp.pre.ss, gpr, 1, 0);
+        const float s1 = warp_col_sum(sp.pre.ss + gpr, gpr, 1, 0);
+        seg_r[0] = rsqrtf(s0 / (float)sp.pre.dim + sp.pre.eps);
+        seg_r[1] = rsqrtf(s1 / (float)sp.pre.dim + sp.pre.eps);
+      }
     }
     if (!mbar_wait_bounded(&bars[slot], (uint32_t)((i / S) & 1))) {
       if (lane == 0) set_dev_error(sp.err, kErrMbarTimeout);
@@ -1145,6 +1298,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
 
     const int ph = cc.ph;
     const int unit = cc.c.u, tile = cc.c.tile, seg = cc.c.seg;
+    const int unit_ks = cc.c.ks;  // a stage of the unit (for the per-half scale)
     if (!phase_advance(sp, cc, W, gw)) continue;
 
     // ------------------------------------------------------------ unit done
@@ -1173,6 +1327,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       if (sg.res) resv = __ldcg(sg.res + sg.out_col0 + row);
       if (p.pack_w) pw = __ldg(p.pack_w + sg.out_col0 + row);
     }
+    if (ph == 0 && sp.pre.kind == kPreEmbedPack)
+      g *= seg_r[unit_ks * 8 >= sp.pre.dim / kGroup ? 1 : 0];
     float u = 0.f;
     bool fin = true;
     if (p.ksplit > 1 || p.um > 1) {
@@ -1248,7 +1404,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
         const unsigned tiles = (unsigned)p.seg[p.nseg - 1].tile_end;
         const unsigned prev = atomicAdd(sp.phase_done + ph, done_here);
         if (ph == sp.nphase - 1 && prev + done_here == tiles)
-          for (int q = 0; q < sp.nphase; ++q) sp.phase_done[q] = 0u;  // every wait has passed
+          for (int q = 0; q <= kMaxPhases; ++q) sp.phase_done[q] = 0u;  // every wait has passed
       }
       done_here = 0;
     }

@@ -34,7 +34,7 @@ struct GemvScratch {
   size_t part_bytes;
   unsigned* cnt;        // per-tile completion counters (cleared)
   int cnt_len;
-  unsigned* phase_done; // [kMaxPhases] per-phase tile counters of the one-row kernel (cleared)
+  unsigned* phase_done; // [kMaxPhases + 1] per-phase tile and pre-unit counters of the one-row kernel (cleared)
 };
 size_t gemv_scratch_part_bytes();
 constexpr int kGemvCounters = 4096;
@@ -44,7 +44,8 @@ constexpr int kGemvCounters = 4096;
 // One-row (m = 1) projections in order in one launch: phase q reads its
 // activation row only after every tile of phase q - 1 is written.
 cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
-                             const GemvScratch& sc, int* err, cudaStream_t st);
+                             const GemvScratch& sc, int* err, cudaStream_t st,
+                             const PreParams* pre = nullptr);
 cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
                         const GemvScratch& scratch, cudaStream_t stream);
 cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float2* xs, cudaStream_t st);
@@ -92,8 +93,13 @@ struct alignas(64) AttnParams {
   // when that kernel signals its dependents after its own wait (so every
   // earlier kernel, including the step that wrote those rows, has finished).
   int prefetch_before_wait;
+  // 1: the splits merge the output in this kernel; 0: they only write their
+  // partials (the next launch merges them, m = 1)
+  int merge_in_kernel;
   int* err;
 };
+// Start of the split outputs inside the partials buffer.
+const float* attn_part_outputs(const float* part, int nkv, int nsplit, int q_per_kv);
 // Split count for `cached` keys inside the window, and an upper bound of it
 // that grows with `cached` (sizes the partials).
 int attn_splits(int nkv, int cached);
