@@ -32,7 +32,19 @@ namespace mtp {
 constexpr int kTileKeys = 32;
 constexpr float kNegBig = -1e30f;
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr int kAttnMaxWarps = 8;
+#ifndef MTP_ATTN_MAX_WARPS
+#define MTP_ATTN_MAX_WARPS 8
+#endif
+// L2 policy of the cached K/V tiles (tuning knob).  Evict-first: keeping
+// the 33.5 MB cache of the 40/8-head, 4096-row layer resident with
+// evict-last measured 10 us slower per draft step (it crowds the weights).
+#ifndef MTP_ATTN_KV_POLICY
+#define MTP_ATTN_KV_POLICY l2_policy_evict_first
+#endif
+#ifndef MTP_ATTN_MIN_QGROUPS
+#define MTP_ATTN_MIN_QGROUPS 1
+#endif
+constexpr int kAttnMaxWarps = MTP_ATTN_MAX_WARPS;  // warps per CTA (tuning knob)
 constexpr int kAttnQMax = 8;                     // query rows per warp (template bound)
 constexpr size_t kAttnSmemLimit = 226 * 1024;     // dynamic shared memory of one CTA (227 KB less static)
 constexpr size_t kAttnSlack = 1024;               // alignment of the swizzled K boxes
@@ -308,7 +320,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
     mbar_fence_init();
   }
   __syncthreads();
-  const uint64_t pol = l2_policy_evict_first();
+  const uint64_t pol = MTP_ATTN_KV_POLICY();
   // the buffer's leader lane fills it with tile t (absolute index)
   auto issue = [&](int t) {
     const int key0 = kbeg + t * kTileKeys;
@@ -599,6 +611,8 @@ static int attn_qmax(int dv) { return dv <= 128 ? kAttnQMax : 4; }
 // smallest instantiated size that holds a group's rows).
 static void attn_groups(int QG, int dv, int* qgroups, int* qm) {
   *qgroups = ceil_div(QG, attn_qmax(dv));
+  // more warps per buffer (fewer rows each) shorten the per-tile chains
+  if (*qgroups < MTP_ATTN_MIN_QGROUPS) *qgroups = MTP_ATTN_MIN_QGROUPS < QG ? MTP_ATTN_MIN_QGROUPS : QG;
   const int qpw = ceil_div(QG, *qgroups);
   *qm = qpw <= 2 ? 2 : qpw <= 4 ? 4 : qpw <= 6 ? 6 : 8;
 }
