@@ -68,10 +68,14 @@ def layer_bytes(cfg):
 
 
 def launches_per_step(cfg):
-    # dense: norm/pack, eh_proj, qkv, attention, o_proj, gate/up, down, lm_head (the other
-    # three RMSNorms are folded into the projections); MoE: norm/pack, eh_proj, qkv,
-    # attention, o_proj, router, expert gate/up, expert down, final norm, lm_head
-    return 8 if not cfg.moe else 10
+    # m = 1 dense: one-row launch A (embedding pack + eh_proj + q/k/v), attention,
+    # one-row launch B (split merge + o_proj + gate/up + down + lm_head).
+    # m > 1 dense: norm/pack, eh_proj, q/k/v, attention, o_proj, gate/up, down, lm_head.
+    # MoE (m = 1): launch A, attention, o_proj, router, expert gate/up, expert down,
+    # final norm, lm_head.
+    if cfg.moe:
+        return 8
+    return 3 if cfg.m == 1 else 8
 
 
 # --------------------------------------------------------------- clocks
