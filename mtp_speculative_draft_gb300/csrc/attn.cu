@@ -211,16 +211,26 @@ __device__ __forceinline__ void warp_tile(const AttnParams& a, WarpState<QM, DV>
 #pragma unroll
   for (int q = 0; q < QM; ++q) acc[q] = 0.f;
   if (lane < nk) {
-#pragma unroll 2
-    for (int f = 0; f < kq4; ++f) {
-      const float4 k = swz ? *reinterpret_cast<const float4*>(Ks + (f >> 3) * 1024 + lane * 32 +
-                                                               (((f & 7) ^ (lane & 7)) << 2))
-                           : *reinterpret_cast<const float4*>(Ks + lane * dqk + 4 * f);
+    // 32-dim blocks: the key's 8 chunks of a block (all loads in flight)
+    const int l7 = lane & 7;
+    for (int bx = 0; bx < kq4 / 8; ++bx) {
+      float4 k[8];
+      if (swz) {  // box bx: row lane, 16-byte chunk c at c ^ (lane & 7)
+        const float* kb = Ks + bx * 1024 + lane * 32;
 #pragma unroll
-      for (int q = 0; q < QM; ++q) {
-        const float4 x = *reinterpret_cast<const float4*>(qrow + q * dqk + 4 * f);
-        acc[q] = fmaf(x.x, k.x, fmaf(x.y, k.y, fmaf(x.z, k.z, fmaf(x.w, k.w, acc[q]))));
+        for (int c = 0; c < 8; ++c) k[c] = *reinterpret_cast<const float4*>(kb + ((c ^ l7) << 2));
+      } else {
+        const float* kb = Ks + lane * dqk + bx * 32;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) k[c] = *reinterpret_cast<const float4*>(kb + 4 * c);
       }
+#pragma unroll
+      for (int c = 0; c < 8; ++c)
+#pragma unroll
+        for (int q = 0; q < QM; ++q) {
+          const float4 x = *reinterpret_cast<const float4*>(qrow + q * dqk + bx * 32 + 4 * c);
+          acc[q] = fmaf(x.x, k[c].x, fmaf(x.y, k[c].y, fmaf(x.z, k[c].z, fmaf(x.w, k[c].w, acc[q]))));
+        }
     }
   }
   // ---- online softmax per query row; probabilities to the warp's rows
