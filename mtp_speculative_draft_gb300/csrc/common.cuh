@@ -155,6 +155,18 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// GPU-scope counters: a barrier (bar.sync / bar.warp.sync) makes the block's
+// or warp's earlier stores precede the releasing thread's operation, whose
+// release then publishes them (the barrier-then-release pattern).
+__device__ __forceinline__ unsigned atom_add_acq_rel_gpu(unsigned* p, unsigned v) {
+  unsigned r;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(r) : "l"(p), "r"(v) : "memory");
+  return r;
+}
+__device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void set_dev_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
 }

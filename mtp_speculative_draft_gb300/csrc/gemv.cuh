@@ -1164,9 +1164,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       else
         pre_attn_merge(sp.pre, u, lane);
     }
-    __threadfence();
-    __syncwarp();
-    if (lane == 0 && n_pre > 0) atomicAdd(sp.phase_done + kMaxPhases, n_pre);
+    __syncwarp();  // the warp's stores, then one release by lane 0
+    if (lane == 0 && n_pre > 0) red_add_release_gpu(sp.phase_done + kMaxPhases, n_pre);
   }
 
   // The eight MMA columns carry (group, hi/lo) pairs instead of activation
@@ -1335,14 +1334,12 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       // deterministic split-K (and gate/up pairing): each unit stores its 32
       // rows; the last of the tile's units sums them in k order
       p.part[(size_t)unit * 32 + lane] = g;
-      __threadfence();
-      __syncwarp();
+      __syncwarp();  // the warp's partial, then one acquire-release count by lane 0
       unsigned prev = 0;
-      if (lane == 0) prev = atomicAdd(p.tile_cnt + tile, 1u);
+      if (lane == 0) prev = atom_add_acq_rel_gpu(p.tile_cnt + tile, 1u);
       prev = __shfl_sync(0xffffffffu, prev, 0);
       fin = prev == (unsigned)(p.um * p.ksplit) - 1;
       if (fin) {
-        __threadfence();
         const float* src = p.part + (size_t)tile * p.um * p.ksplit * 32 + lane;
         g = sum_rows(src, p.ksplit);
         if (p.um > 1) u = sum_rows(src + (size_t)p.ksplit * 32, p.ksplit);
@@ -1396,15 +1393,18 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       ++done_here;
     }
     if (cc.ph != ph) {
-      // leaving phase ph: publish this warp's finished tiles (one fence and
-      // one atomic per warp and phase); the launch's last tile clears the counters
-      __threadfence();
+      // leaving phase ph: publish this warp's finished tiles (one release
+      // per warp and phase); the launch's last tile clears the counters
       __syncwarp();
       if (lane == 0 && done_here > 0) {
         const unsigned tiles = (unsigned)p.seg[p.nseg - 1].tile_end;
-        const unsigned prev = atomicAdd(sp.phase_done + ph, done_here);
-        if (ph == sp.nphase - 1 && prev + done_here == tiles)
-          for (int q = 0; q <= kMaxPhases; ++q) sp.phase_done[q] = 0u;  // every wait has passed
+        if (ph == sp.nphase - 1) {
+          const unsigned prev = atom_add_acq_rel_gpu(sp.phase_done + ph, done_here);
+          if (prev + done_here == tiles)
+            for (int q = 0; q <= kMaxPhases; ++q) sp.phase_done[q] = 0u;  // every wait has passed
+        } else {
+          red_add_release_gpu(sp.phase_done + ph, done_here);
+        }
       }
       done_here = 0;
     }
