@@ -192,6 +192,7 @@ cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
   const int warps_cap = sm_count() * ctas_per_sm * kGemvWarps;
   StreamParams sp = {};
   int max_units = 1;
+  int units_q[kMaxPhases];
   for (int q = 0; q < nphase; ++q) {
     GemvParams& p = ph[q];
     if (p.m != 1 || (q + 1 < nphase && p.epi == kEpiArgmax)) return cudaErrorInvalidValue;
@@ -207,6 +208,7 @@ cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
     p.part = sc.part;
     p.tile_cnt = sc.cnt;
     p.err = err;
+    units_q[q] = pl.units;
     if (pl.units > max_units) max_units = pl.units;
     sp.ph[q] = p;
   }
@@ -215,6 +217,13 @@ cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
   sp.err = err;
   if (pre) sp.pre = *pre;
   const int warps = max_units < warps_cap ? max_units : warps_cap;
+  // each phase spreads its units evenly: ceil(units / warps) rounds on as
+  // few warps as that number of rounds needs (a part-filled last round runs
+  // the stream on fewer warps than it needs for full bandwidth)
+  for (int q = 0; q < nphase; ++q) {
+    const int rounds = (units_q[q] + warps - 1) / warps;
+    sp.ph[q].wq = (units_q[q] + rounds - 1) / rounds;
+  }
   const int grid = (warps + kGemvWarps - 1) / kGemvWarps;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);

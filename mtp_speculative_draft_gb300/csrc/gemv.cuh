@@ -129,6 +129,7 @@ struct GemvParams {
   int rowsel_after_wait; // 1: rowsel is produced by the previous kernel
   int epi;               // one-row kernel: kEpiStore / kEpiSwiglu / kEpiArgmax
   int um;                // one-row kernel: 2 when gate (mat) and up (mat + 1) are separate units
+  int wq;                // one-row kernel: warps gw < wq take units gw, gw + wq, ... (same count each)
   // K-segment mode (MoE down projection): K = nkseg * kseg_len
   int kseg_len;          // 0: off
   int nkseg;
@@ -1008,9 +1009,9 @@ __device__ __forceinline__ int phase_ks(const GemvParams& p) { return (p.K / kGr
 __device__ __forceinline__ void phase_start(const StreamParams& sp, PhaseCursor& x, int ph, int gw) {
   for (; ph < sp.nphase; ++ph) {
     const GemvParams& p = sp.ph[ph];
-    const int units = phase_units(p);
-    if (gw < units) {
+    if (gw < p.wq) {
       x.ph = ph;
+      const int units = phase_units(p);
       x.c.start(p, gw, units, p.ksplit, p.spu, phase_ks(p), p.um);
       return;
     }
@@ -1019,11 +1020,11 @@ __device__ __forceinline__ void phase_start(const StreamParams& sp, PhaseCursor&
 }
 
 // Advances by one stage; true when a unit just finished.
-__device__ __forceinline__ bool phase_advance(const StreamParams& sp, PhaseCursor& x, int W, int gw) {
+__device__ __forceinline__ bool phase_advance(const StreamParams& sp, PhaseCursor& x, int gw) {
   const GemvParams& p = sp.ph[x.ph];
   if (++x.c.ks < x.c.ke) return false;
   const int units = phase_units(p);
-  const int u = x.c.u + W;
+  const int u = x.c.u + p.wq;
   if (u < units)
     x.c.start(p, u, units, p.ksplit, p.spu, phase_ks(p), p.um);
   else
@@ -1129,7 +1130,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       for (; issued < S && pc.ph < sp.nphase && !sp.ph[pc.ph].rowsel_after_wait; ++issued) {
         issue_w(pc, issued);
         defer_x(pc, issued);
-        phase_advance(sp, pc, W, gw);
+        phase_advance(sp, pc, gw);
       }
   }
   // the first phase's input comes from the previous kernel
@@ -1152,7 +1153,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
         issue_x(pc, issued);
       else
         defer_x(pc, issued);
-      phase_advance(sp, pc, W, gw);
+      phase_advance(sp, pc, gw);
     }
   }
   // pre-units of this warp (after its first weight copies are in flight)
@@ -1292,13 +1293,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       else
         defer_x(pc, slot);
       ++issued;
-      phase_advance(sp, pc, W, gw);
+      phase_advance(sp, pc, gw);
     }
 
     const int ph = cc.ph;
     const int unit = cc.c.u, tile = cc.c.tile, seg = cc.c.seg;
     const int unit_ks = cc.c.ks;  // a stage of the unit (for the per-half scale)
-    if (!phase_advance(sp, cc, W, gw)) continue;
+    if (!phase_advance(sp, cc, gw)) continue;
 
     // ------------------------------------------------------------ unit done
     // a row's four lanes each hold two groups per stage: sum them in a fixed
