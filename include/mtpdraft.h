@@ -168,7 +168,7 @@ mtp_status attn_decode_sink(const mtp_attn_geom *g, const float *d_qp, const flo
                             float *d_out, void *d_ws, size_t ws_bytes, void *stream);
 
 /* attn_decode_sink_noalloc: attn_decode_sink with the library's own static
- * device scratch (1 MiB, a file-scope __device__ array) in place of d_ws.
+ * device scratch (2 MiB, a file-scope __device__ array) in place of d_ws.
  * The draft-layer method has no counterpart of this call: it exists for
  * callers that hold no device memory to lend, such as a host runtime whose
  * device memory all sits in its own pools, or a plugin interface whose
@@ -178,7 +178,7 @@ mtp_status attn_decode_sink(const mtp_attn_geom *g, const float *d_qp, const flo
  *    stream capture.  Later calls enqueue a clear of the completion counters
  *    on `stream`, then the same launch as attn_decode_sink.
  *  - Geometries whose scratch (attn_decode_sink_workspace_bytes) exceeds
- *    1 MiB return MTP_ERR_WORKSPACE without launching anything.
+ *    2 MiB return MTP_ERR_WORKSPACE without launching anything.
  *  - Calls that overlap on one device share the scratch and race: order
  *    them (one stream, or events).
  *  - A device-side wait that gives up records its code in the scratch

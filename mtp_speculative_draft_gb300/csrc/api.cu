@@ -981,11 +981,11 @@ mtp_status mtp_draft_chain(const mtp_layer_desc* layers, int32_t n_layers, const
 namespace mtp {
 
 // Scratch of attn_decode_sink_noalloc: the workspace header (device error
-// word + completion counters) followed by the split partials.  1 MiB holds
+// word + completion counters) followed by the split partials.  2 MiB holds
 // the partials of every geometry up to nkv * splits * (G*m) * (dv + 2)
-// floats of about 255 K, e.g. 8 KV heads x 19 splits x 5 rows x 130 floats
+// floats of about 520 K, e.g. 8 KV heads x 19 splits x 5 rows x 130 floats
 // (395 KB) for a 40/8-head, 128-dim cache of 4096 rows.
-constexpr size_t kNoallocScratchBytes = size_t(1) << 20;
+constexpr size_t kNoallocScratchBytes = size_t(2) << 20;
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
 constexpr int kNoallocMaxDevices = 64;
 

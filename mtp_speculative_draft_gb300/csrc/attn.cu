@@ -9,14 +9,15 @@
 //
 // Split-K over the cache, at most one CTA per SM.  A CTA serves every query
 // row of its KV head (grouped-query sharing of the K/V stream: G heads x m
-// new rows).  It owns `nbuf` tile buffers of 32 keys; each buffer is read by
+// new rows).  It owns `nbuf` tile buffers of 16 keys; each buffer is read by
 // `qgroups` warps, each of which holds a slice of the query rows.  Warps work
 // on their buffer's tiles alone, with no CTA-wide barrier in the loop:
-//   * the tile arrives by TMA (K as 128-byte-swizzled boxes of 32 rows x 32
+//   * the tile arrives by TMA (K as 128-byte-swizzled boxes of 16 rows x 32
 //     floats, V as one bulk copy) and completes on the buffer's mbarrier;
-//   * logits with lane = key: a lane reads its key row once and keeps one
-//     accumulator per query row; query chunks are warp-wide broadcasts;
-//   * online softmax per query row in the log2 domain (warp shuffles);
+//   * logits with lane = (key, half of the head dims): a lane reads its half
+//     of the key row once and keeps one accumulator per query row; query
+//     chunks are shared-memory broadcasts; one shuffle adds the halves;
+//   * online softmax per query row in the log2 domain (half-warp shuffles);
 //   * P.V with lane = output dims; probabilities go through a per-warp row
 //     of shared memory and are read back four keys at a time.
 // The buffers' states meet once in shared memory and the CTA writes one
@@ -29,11 +30,11 @@
 
 namespace mtp {
 
-constexpr int kTileKeys = 32;
+constexpr int kTileKeys = 16;  // keys per tile: a half-warp of lanes, one key each
 constexpr float kNegBig = -1e30f;
 constexpr float kLog2e = 1.4426950408889634f;
 #ifndef MTP_ATTN_MAX_WARPS
-#define MTP_ATTN_MAX_WARPS 8
+#define MTP_ATTN_MAX_WARPS 12
 #endif
 // L2 policy of the cached K/V tiles (tuning knob).  Evict-first: keeping
 // the 33.5 MB cache of the 40/8-head, 4096-row layer resident with
@@ -56,7 +57,7 @@ __host__ __device__ inline size_t attn_part_o_offset(int nkv, int nsplit, int QG
 }
 
 __host__ __device__ inline size_t attn_tile_bytes(int dqk, int dv) {
-  return (size_t)kTileKeys * (dqk + dv) * 4;  // a multiple of 4 KB (dims are multiples of 32)
+  return (size_t)kTileKeys * (dqk + dv) * 4;  // a multiple of 2 KB (dims are multiples of 32)
 }
 
 struct AttnLayout {
@@ -206,46 +207,60 @@ __device__ __forceinline__ void warp_tile(const AttnParams& a, WarpState<QM, DV>
                                           int lane) {
   const int dqk = a.dqk, dv = a.dv;
   const int kq4 = dqk / 4;
-  // ---- logits: lane = key
+  // ---- logits: lane = (key, half); half h takes the 16-byte chunks 2i + h
+  // of every 32-dim block (so the two halves' query broadcasts fall in
+  // different banks), and one shuffle adds the halves
+  const int key = lane & (kTileKeys - 1), half = lane >> 4;
   float acc[QM];
 #pragma unroll
   for (int q = 0; q < QM; ++q) acc[q] = 0.f;
-  if (lane < nk) {
-    // 32-dim blocks: the key's 8 chunks of a block (all loads in flight)
-    const int l7 = lane & 7;
+  if (key < nk) {
+    // 32-dim blocks: the key's 4 chunks of a block (all loads in flight)
+    const int l7 = key & 7;
     for (int bx = 0; bx < kq4 / 8; ++bx) {
-      float4 k[8];
-      if (swz) {  // box bx: row lane, 16-byte chunk c at c ^ (lane & 7)
-        const float* kb = Ks + bx * 1024 + lane * 32;
+      float4 k[4];
+      if (swz) {  // box bx: row key, 16-byte chunk c at c ^ (key & 7)
+        const float* kb = Ks + bx * (kTileKeys * 32) + key * 32;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) k[c] = *reinterpret_cast<const float4*>(kb + ((c ^ l7) << 2));
+        for (int i = 0; i < 4; ++i)
+          k[i] = *reinterpret_cast<const float4*>(kb + (((2 * i + half) ^ l7) << 2));
       } else {
-        const float* kb = Ks + lane * dqk + bx * 32;
+        const float* kb = Ks + key * dqk + bx * 32;
 #pragma unroll
-        for (int c = 0; c < 8; ++c) k[c] = *reinterpret_cast<const float4*>(kb + 4 * c);
+        for (int i = 0; i < 4; ++i) k[i] = *reinterpret_cast<const float4*>(kb + 4 * (2 * i + half));
       }
 #pragma unroll
-      for (int c = 0; c < 8; ++c)
+      for (int i = 0; i < 4; ++i)
 #pragma unroll
         for (int q = 0; q < QM; ++q) {
-          const float4 x = *reinterpret_cast<const float4*>(qrow + q * dqk + bx * 32 + 4 * c);
-          acc[q] = fmaf(x.x, k[c].x, fmaf(x.y, k[c].y, fmaf(x.z, k[c].z, fmaf(x.w, k[c].w, acc[q]))));
+          const float4 x =
+              *reinterpret_cast<const float4*>(qrow + q * dqk + bx * 32 + 4 * (2 * i + half));
+          acc[q] = fmaf(x.x, k[i].x, fmaf(x.y, k[i].y, fmaf(x.z, k[i].z, fmaf(x.w, k[i].w, acc[q]))));
         }
     }
   }
-  // ---- online softmax per query row; probabilities to the warp's rows
-  const int j = key0 + lane;
+#pragma unroll
+  for (int q = 0; q < QM; ++q) acc[q] += __shfl_xor_sync(0xffffffffu, acc[q], 16);
+  // ---- online softmax per query row (both halves hold every key's logit:
+  // reductions over 16 lanes); probabilities to the warp's rows
+  const int j = key0 + key;
 #pragma unroll
   for (int q = 0; q < QM; ++q) {
     const int p = a.L + (q0 + q) / G;
-    const bool ok = lane < nk && j <= p && (a.window <= 0 || j > p - a.window);
+    const bool ok = key < nk && j <= p && (a.window <= 0 || j > p - a.window);
     const float l = ok ? acc[q] : kNegBig;
-    const float mnew = fmaxf(st.M[q], warp_max(l));
+    float mx = l;
+#pragma unroll
+    for (int o = kTileKeys / 2; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    const float mnew = fmaxf(st.M[q], mx);
     const float pr = ok ? exp2f(l - mnew) : 0.f;
     const float alpha = exp2f(st.M[q] - mnew);
-    st.l[q] = st.l[q] * alpha + warp_sum(pr);
+    float sm = pr;
+#pragma unroll
+    for (int o = kTileKeys / 2; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+    st.l[q] = st.l[q] * alpha + sm;
     st.M[q] = mnew;
-    ps[q * kTileKeys + lane] = pr;
+    if (half == 0) ps[q * kTileKeys + key] = pr;
 #pragma unroll
     for (int i = 0; i < DV; ++i) st.o[q][i] *= alpha;
   }
@@ -337,7 +352,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
     const int nk = min(kTileKeys, L - key0);
     mbar_arrive_expect_tx(&bars[b], (uint32_t)kTileKeys * dqk * 4 + (uint32_t)nk * dv * 4);
     for (int bx = 0; bx < dqk / 32; ++bx)
-      tma_load_2d(Kb + bx * 1024, &a.kmap, &bars[b], bx * 32, kvh * a.cap + key0, pol);
+      tma_load_2d(Kb + bx * (kTileKeys * 32), &a.kmap, &bars[b], bx * 32, kvh * a.cap + key0, pol);
     bulk_load(Vb, vbase + (size_t)key0 * dv, (uint32_t)nk * dv * 4, &bars[b], pol);
   };
   const int t_first = t_begin + b;
@@ -691,7 +706,8 @@ static cudaError_t launch_attn_dv(const AttnParams& a, int qm, size_t smem, cuda
 
 cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
   AttnParams a = a_in;
-  cudaError_t ke = encode_f32_tile_map(&a.kmap, a.kc, (uint64_t)a.nkv * a.cap, (uint64_t)a.dqk);
+  cudaError_t ke =
+      encode_f32_tile_map(&a.kmap, a.kc, (uint64_t)a.nkv * a.cap, (uint64_t)a.dqk, kTileKeys);
   if (ke != cudaSuccess) return ke;
   const int QG = (a.nh / a.nkv) * a.m;
   // warps per buffer: the fewest that keep each warp within attn_qmax rows

@@ -314,10 +314,11 @@ static CUresult encode2d(CUtensorMap* m, CUtensorMapDataType dt, const void* bas
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
-cudaError_t encode_f32_tile_map(CUtensorMap* out, const float* base, uint64_t rows, uint64_t cols) {
-  // rows of `cols` floats, box 32 rows x 32 floats, 128-byte swizzle
-  CUresult r = encode2d(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, cols, rows, cols * 4, 32, 32,
-                        CU_TENSOR_MAP_SWIZZLE_128B);
+cudaError_t encode_f32_tile_map(CUtensorMap* out, const float* base, uint64_t rows, uint64_t cols,
+                                int box_rows) {
+  // rows of `cols` floats, box box_rows x 32 floats, 128-byte swizzle
+  CUresult r = encode2d(out, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, base, cols, rows, cols * 4, 32,
+                        (uint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 

@@ -71,8 +71,10 @@ struct NormSeg {
 cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, float2* xs,
                              int* err, cudaStream_t st);
 
-// Tensor map over float rows [rows][cols] with 32 x 32 boxes, 128-byte swizzle.
-cudaError_t encode_f32_tile_map(CUtensorMap* out, const float* base, uint64_t rows, uint64_t cols);
+// Tensor map over float rows [rows][cols] with boxes of box_rows x 32 floats,
+// 128-byte swizzle.
+cudaError_t encode_f32_tile_map(CUtensorMap* out, const float* base, uint64_t rows, uint64_t cols,
+                                int box_rows);
 
 struct alignas(64) AttnParams {
   CUtensorMap kmap;     // K cache viewed as [n_kv * cap][dqk]

@@ -81,7 +81,8 @@ def test_noalloc_rejects_oversized_scratch(dev):
     import torch
     from mtp_speculative_draft_gb300 import attn_decode_sink_noalloc, attn_geom
     from mtp_speculative_draft_gb300._lib import MtpError
-    # 64 KV heads x 16 query rows x 256 dims: partials far above 1 MiB
+    # 64 KV heads x 2 splits x 16 query rows x 258 floats: 2.11 MB of
+    # partials, above the 2 MiB scratch
     nh, nkv, d, L, m = 1024, 64, 256, 512, 1
     cap = L + m
     g = attn_geom(nh, nkv, d, d, d, 0, False, 1e-6)
