@@ -40,7 +40,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-kernel", default=None, choices=["lm_head", "ffn_down", "attention"],
+    ap.add_argument("--profile-kernel", default=None, choices=["lm_head", "ffn_down", "attention", "verify_head"],
                     help="run only one entry point of the workload (small device footprint, for ncu)")
     return ap.parse_args()
 
@@ -474,7 +474,25 @@ def run_profile_kernel(args):
     cfg = CONFIGS[args.config]
     dev = torch.device("cuda", 0)
     H = cfg.hidden
-    if args.profile_kernel in ("lm_head", "ffn_down"):
+    extra = {}
+    if args.profile_kernel == "verify_head":
+        # the pending token and three drafts through the final norm and the
+        # lm_head in one pass, softcap 30, argmax per row
+        rows = 4
+        w = DeviceAffine(mtp_synth.affine4_weight(cfg.seed, cfg.name + ".lm_head", cfg.vocab, H), dev)
+        h = torch.from_numpy(mtp_synth.normal_f32(cfg.seed, "profile.verify", (rows, H))).to(dev)
+        nw = torch.ones(H, dtype=torch.float32, device=dev)
+        tok = torch.zeros(rows, dtype=torch.int32, device=dev)
+        val = torch.zeros(rows, dtype=torch.float32, device=dev)
+        logits = torch.zeros((rows, cfg.vocab), dtype=torch.float32, device=dev)
+        ws = A.verify_head_argmax(h, rows, nw, cfg.eps, w.desc, 1.0, 30.0, tok, val, logits)
+        run = lambda: A.verify_head_argmax(h, rows, nw, cfg.eps, w.desc, 1.0, 30.0, tok, val,  # noqa: E731
+                                           logits, ws)
+        # weights once, the rows in, the logits out (read back once by the argmax pass)
+        weight_bytes = cfg.vocab * H // 2 + 2 * cfg.vocab * (H // 32) * 4
+        extra["rows"] = rows
+        extra["algorithmic_bytes_per_call"] = weight_bytes + rows * H * 4 + 2 * rows * cfg.vocab * 4
+    elif args.profile_kernel in ("lm_head", "ffn_down"):
         if args.profile_kernel == "lm_head":
             n, k, name = cfg.vocab, H, cfg.name + ".lm_head"
         else:
@@ -520,8 +538,15 @@ def run_profile_kernel(args):
         run()
     e1.record()
     torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / max(1, args.steps)
+    if "algorithmic_bytes_per_call" in extra:
+        peak, kind = measured_peaks()
+        extra["gbs"] = extra["algorithmic_bytes_per_call"] / (ms * 1e-3) / 1e9
+        extra["frac"] = extra["gbs"] / peak
+        extra["peak_gbs"] = peak
+        extra["peak_kind"] = kind
     print(json.dumps({"profile_kernel": args.profile_kernel, "workload": cfg.name,
-                      "ms_per_call": e0.elapsed_time(e1) / max(1, args.steps)}))
+                      "ms_per_call": ms, **extra}))
 
 
 def main():

@@ -208,6 +208,31 @@ mtp_status lmhead_argmax(const float *d_y, const float *d_norm_w, float eps,
                          float *d_y_normed, void *d_ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
+ * verify_head_argmax: for each of `rows` hidden rows h_r,
+ *   y_r = RMSNorm(h_r)*norm_w (or h_r when norm_w is NULL);
+ *   l_r = W . y_r;  l_r *= logit_multiplier;
+ *   l_r = softcap * tanh(l_r / softcap)   (only when softcap > 0);
+ *   token_r = argmax l_r (lowest index among equal maxima), value_r = l_r[token_r].
+ *
+ * "cortiq-engine 0.8.49 src/mimo_mtp.rs" mimo_verify_head_rows (the final
+ * norm and the lm_head over the pending token and the k drafts in one head
+ * pass, then the optional logit multiplier and final softcap, in that order)
+ * as used by mimo_spec_round, whose greedy verification takes each row's
+ * argmax.  The vocabulary matrix is streamed once for all rows.
+ *   d_h [rows][H] row-major; rows in 1..16 (the pages use 2..4); W [V][H];
+ *   logit_multiplier: 1 for none (any finite value); softcap <= 0 for none;
+ *   d_tokens [rows] (int32) and d_values [rows] receive the result;
+ *   d_logits [rows][V] receives the final logits, or NULL (kept in d_ws).
+ *   H % 128 == 0; pointers 16-byte aligned.  Arithmetic after the projection
+ *   is float32, so ties are decided on the float32 values.
+ * ------------------------------------------------------------------------ */
+size_t verify_head_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab);
+mtp_status verify_head_argmax(const float *d_h, int32_t rows, const float *d_norm_w, float eps,
+                              const mtp_affine4 *W, float logit_multiplier, float softcap,
+                              int32_t *d_tokens, float *d_values, float *d_logits, void *d_ws,
+                              size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
  * MoE feed-forward (router softmax, top-k, renormalised expert SwiGLUs plus a
  * sigmoid-gated shared expert).  "hf2q 0.1.13 ... mtp.rs" MtpFfnWeightsGpu::Moe
  * (router, stacked expert gate/up/down, four shared-expert tensors) and

@@ -80,6 +80,9 @@ EXPORTS = {
                                            vp, i32, i32, i32, vp, vp]),
     "lmhead_argmax_workspace_bytes": (sz, [i32, i32]),
     "lmhead_argmax": (C.c_int, [vp, vp, f32, C.POINTER(Affine4), vp, vp, vp, vp, vp, sz, vp]),
+    "verify_head_workspace_bytes": (sz, [i32, i32, i32]),
+    "verify_head_argmax": (C.c_int, [vp, i32, vp, f32, C.POINTER(Affine4), f32, f32, vp, vp, vp,
+                                     vp, sz, vp]),
     "moe_ffn_workspace_bytes": (sz, [C.POINTER(MoeWeights), i32]),
     "moe_ffn": (C.c_int, [C.POINTER(MoeWeights), vp, vp, f32, i32, vp, vp, vp, vp, sz, vp]),
     "mtp_draft_workspace_bytes": (sz, [C.POINTER(LayerDesc), i32]),

@@ -117,6 +117,17 @@ def lmhead_argmax(y, norm_w, eps, w: Affine4, token, value, logits=None, y_norme
     return ws
 
 
+def verify_head_argmax(h, rows, norm_w, eps, w: Affine4, logit_multiplier, softcap, tokens,
+                       values, logits=None, ws=None, stream=None):
+    lib = L.load()
+    if ws is None:
+        ws = workspace(lib.verify_head_workspace_bytes(rows, w.k, w.n), stream=stream)
+    check(lib.verify_head_argmax(_p(h), rows, _p(norm_w), eps, C.byref(w), logit_multiplier,
+                                 softcap, _p(tokens), _p(values), _p(logits), _p(ws), ws.numel(),
+                                 _stream(stream)), "verify_head_argmax")
+    return ws
+
+
 def moe_ffn(w: MoeWeights, u1, post_norm, eps, hidden, u2, sel=None, weight=None, ws=None,
             stream=None):
     lib = L.load()

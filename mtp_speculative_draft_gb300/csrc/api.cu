@@ -402,6 +402,73 @@ mtp_status lmhead_argmax(const float* d_y, const float* d_norm_w, float eps,
                       partial, sc, d_ws, static_cast<cudaStream_t>(stream));
 }
 
+// ------------------------------------------------------------------ verify head
+size_t verify_head_workspace_bytes(int32_t rows, int32_t hidden, int32_t vocab) {
+  if (rows <= 0 || hidden <= 0 || vocab <= 0) return 0;
+  Carve cv(nullptr);
+  cv.take<uint8_t>(xpack_bytes(rows, hidden));
+  cv.take<float>((size_t)rows * vocab * sizeof(float));
+  cv.take<unsigned long long>(16 * sizeof(unsigned long long));
+  cv.take<unsigned>(16 * sizeof(unsigned));
+  carve_scratch(cv);
+  return cv.off + 256;
+}
+
+mtp_status verify_head_argmax(const float* d_h, int32_t rows, const float* d_norm_w, float eps,
+                              const mtp_affine4* W, float logit_multiplier, float softcap,
+                              int32_t* d_tokens, float* d_values, float* d_logits, void* d_ws,
+                              size_t ws_bytes, void* stream) {
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (!d_h || !d_tokens || !d_values)
+    return fail(MTP_ERR_INVALID_ARG, "verify_head_argmax: null pointer");
+  if (rows < 1 || rows > 16) return fail(MTP_ERR_UNSUPPORTED, "verify_head_argmax: rows must be in 1..16");
+  mtp_status s = check_affine(W, -1, -1, "lm_head", true);
+  if (s != MTP_OK) return s;
+  if (!aligned16(d_h) || (d_norm_w && !aligned16(d_norm_w)) || (d_logits && !aligned16(d_logits)))
+    return fail(MTP_ERR_INVALID_ARG, "verify_head_argmax: pointers must be 16-byte aligned");
+  if (!(eps >= 0.f)) return fail(MTP_ERR_INVALID_ARG, "verify_head_argmax: eps must be >= 0");
+  if (!std::isfinite(logit_multiplier) || std::isnan(softcap) || std::isinf(softcap))
+    return fail(MTP_ERR_INVALID_ARG, "verify_head_argmax: multiplier and softcap must be finite");
+  const int H = W->k, V = W->n;
+  if (!d_ws || ws_bytes < verify_head_workspace_bytes(rows, H, V))
+    return fail(MTP_ERR_WORKSPACE, "verify_head_argmax: workspace too small");
+  Carve cv(d_ws);
+  uint4* xp = cv.take<uint4>(xpack_bytes(rows, H));
+  float2* xs = reinterpret_cast<float2*>(reinterpret_cast<uint8_t*>(xp) + xpack_xs_offset(rows, H));
+  float* own_logits = cv.take<float>((size_t)rows * V * sizeof(float));
+  auto* keys = cv.take<unsigned long long>(16 * sizeof(unsigned long long));
+  auto* cnt = cv.take<unsigned>(16 * sizeof(unsigned));
+  const GemvScratch sc = carve_scratch(cv);
+  float* logits = d_logits ? d_logits : own_logits;
+  // 1. final norm of every row, packed for the projection
+  NormSeg sg = {};
+  sg.src = d_h;
+  sg.w = d_norm_w;
+  sg.eps = eps;
+  sg.dim = H;
+  sg.src_ld = H;
+  cudaError_t e = launch_norm_pack(&sg, 1, rows, xp, xs, &header(d_ws)->err, st);
+  if (e != cudaSuccess) return cuda_fail(e, "verify head norm launch");
+  // 2. logits of all rows in one pass over the vocabulary matrix
+  GemvParams p = {};
+  s = qmat_cached(&p.mat[0], *W, "lm_head");
+  if (s != MTP_OK) return s;
+  p.xp = xp;
+  p.xs = xs;
+  p.m = rows;
+  p.K = H;
+  p.nseg = 1;
+  p.seg[0] = plain_seg(tiles_of(V), V, 0, logits, V, nullptr);
+  p.err = &header(d_ws)->err;
+  e = launch_gemv(1, rows > 8 ? 2 : 1, kEpiStore, p, tiles_of(V), sc, st);
+  if (e != cudaSuccess) return cuda_fail(e, "verify head projection launch");
+  // 3. multiplier, softcap and argmax per row
+  e = launch_rows_argmax(logits, rows, V, logit_multiplier, softcap, d_tokens, d_values, keys, cnt,
+                         st);
+  if (e != cudaSuccess) return cuda_fail(e, "verify head argmax launch");
+  return MTP_OK;
+}
+
 // ------------------------------------------------------------------ MoE
 static mtp_status check_moe(const mtp_moe_weights* w, int H) {
   if (!w || !w->router) return fail(MTP_ERR_INVALID_ARG, "moe: null weights");

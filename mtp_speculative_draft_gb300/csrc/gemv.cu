@@ -285,6 +285,72 @@ cudaError_t launch_gemv_simple(const float* x, int m, int K, const mtp_affine4& 
   return cudaLaunchKernelEx(&cfg, gemv_simple_kernel, x, m, K, w.q, w.s, w.b, (int)w.n, y);
 }
 
+// --------------------------------------------------------------- row argmax
+// Logits of `rows` rows [rows][V], in place: l *= mult, then
+// l = cap * tanh(l / cap) when cap > 0; then each row's argmax (lowest index
+// among equal maxima).  Block (x, r) takes a slice of row r; the last block
+// of a row to finish writes its token and value and clears keys[r], cnt[r].
+constexpr int kRowArgmaxThreads = 256;
+
+__global__ void __launch_bounds__(kRowArgmaxThreads)
+    rows_argmax_kernel(float* __restrict__ logits, int V, float mult, float cap,
+                       int32_t* __restrict__ tok, float* __restrict__ val,
+                       unsigned long long* keys, unsigned* cnt) {
+  pdl_wait();
+  pdl_launch_dependents();
+  __shared__ unsigned long long red[kRowArgmaxThreads / 32];
+  const int r = blockIdx.y;
+  float* row = logits + (size_t)r * V;
+  const int per = (V + gridDim.x - 1) / gridDim.x;
+  const int v0 = blockIdx.x * per, v1 = min(V, v0 + per);
+  unsigned long long best = 0ull;  // below any real key
+  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
+    float l = row[v] * mult;
+    if (cap > 0.f) l = cap * tanhf(l / cap);
+    row[v] = l;
+    const unsigned long long k = argmax_key(l, v);
+    best = k > best ? k : best;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long other = __shfl_xor_sync(0xffffffffu, best, o);
+    best = other > best ? other : best;
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) red[warp] = best;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < kRowArgmaxThreads / 32; ++w) best = red[w] > best ? red[w] : best;
+    if (best) atomicMax(keys + r, best);
+    __threadfence();
+    const unsigned prev = atomicAdd(cnt + r, 1u);
+    if (prev == gridDim.x - 1) {  // every block of the row has merged its key
+      __threadfence();
+      const unsigned long long k = atomicMax(keys + r, 0ull);
+      tok[r] = argmax_key_index(k);
+      val[r] = argmax_key_value(k);
+      keys[r] = 0ull;  // leave the workspace cleared for the next call
+      cnt[r] = 0u;
+    }
+  }
+}
+
+cudaError_t launch_rows_argmax(float* logits, int rows, int V, float mult, float cap, int32_t* tok,
+                               float* val, unsigned long long* keys, unsigned* cnt,
+                               cudaStream_t st) {
+  if (rows < 1 || rows > 65535 || V < 1) return cudaErrorInvalidValue;
+  int blocks = (V + kRowArgmaxThreads * 8 - 1) / (kRowArgmaxThreads * 8);  // >= 8 logits a thread
+  if (blocks > 1024) blocks = 1024;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(blocks, rows);
+  cfg.blockDim = dim3(kRowArgmaxThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr = pdl_attr();
+  cfg.attrs = &attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, rows_argmax_kernel, logits, V, mult, cap, tok, val, keys, cnt);
+}
+
 // --------------------------------------------------------------- tensor maps
 static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

@@ -51,6 +51,11 @@ cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
 cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float2* xs, cudaStream_t st);
 cudaError_t launch_gemv_simple(const float* x, int m, int K, const mtp_affine4& w, float* y,
                                cudaStream_t st);
+// In-place multiplier/softcap of rows x V logits and each row's argmax;
+// keys[rows] and cnt[rows] are zero at rest and left zero.
+cudaError_t launch_rows_argmax(float* logits, int rows, int V, float mult, float cap, int32_t* tok,
+                               float* val, unsigned long long* keys, unsigned* cnt,
+                               cudaStream_t st);
 
 struct NormSeg {
   const float* src;       // row 0 source (row stride = src_ld); null when gathered from `table`

@@ -259,6 +259,30 @@ def argmax_lowest(v: np.ndarray):
     return idx, val, margin
 
 
+def verify_head(hidden_rows, norm_w, eps, lm_head, logit_multiplier=None, final_softcap=None):
+    """Batched verify head: ``(logits [b, V], tokens, values, margins)``.
+
+    [mimo_mtp.rs] ``mimo_verify_head_rows``: every row of ``hidden_rows``
+    (the pending token's and the drafts' hidden rows) goes through the final
+    RMSNorm (skipped when ``norm_w`` is None), the lm_head projection, then
+    the optional logit multiplier (``l * m``) and after it the optional final
+    softcap (``c * tanh(l / c)``).  ``mimo_spec_round`` then samples each
+    row; greedy sampling is the argmax with ties to the lowest index
+    (``argmax_lowest``).
+    """
+    h = np.atleast_2d(np.asarray(hidden_rows, dtype=np.float64))
+    x = h if norm_w is None else np.stack([rmsnorm(row, norm_w, eps) for row in h])
+    logits = qmatmul(x, lm_head)
+    if logit_multiplier is not None:
+        logits = logits * float(logit_multiplier)
+    if final_softcap is not None:
+        c = float(final_softcap)
+        logits = c * np.tanh(logits / c)
+    picks = [argmax_lowest(row) for row in logits]
+    return (logits, [t for t, _, _ in picks], [v for _, v, _ in picks],
+            [mg for _, _, mg in picks])
+
+
 # ---------------------------------------------------------------------------
 # One draft layer
 # ---------------------------------------------------------------------------

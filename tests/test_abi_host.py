@@ -139,3 +139,24 @@ def test_attention_and_head_reject_bad_calls(lib):
     assert lib.attn_decode_sink(C.byref(g), *args, 0, 100, 5, p, p, 1 << 20, None) == 2
     w = _fake_affine(1000, 96)
     assert lib.lmhead_argmax(p, None, 1e-6, C.byref(w), p, p, None, None, p, 1 << 20, None) == 2
+
+
+def test_verify_head_rejects_bad_calls(lib):
+    p = C.c_void_p(0x100000)
+    w = _fake_affine(1000, 256)
+    need = lib.verify_head_workspace_bytes(4, 256, 1000)
+    assert need > 4 * 1000 * 4  # holds the logits of every row
+    assert lib.verify_head_workspace_bytes(0, 256, 1000) == 0
+
+    def call(h=p, rows=4, mult=1.0, cap=0.0, tokens=p, wt=w, ws_bytes=need):
+        return lib.verify_head_argmax(h, rows, None, 1e-6, C.byref(wt), mult, cap, tokens, p, None,
+                                      p, ws_bytes, None)
+
+    assert call(h=None) == 1                       # null input
+    assert call(tokens=None) == 1                  # null output
+    assert call(rows=0) == 2 and call(rows=17) == 2  # rows outside 1..16
+    assert call(mult=float("nan")) == 1            # multiplier must be finite
+    assert call(cap=float("inf")) == 1             # softcap must be finite
+    assert call(wt=_fake_affine(1000, 96)) == 2    # K % 128 != 0
+    assert call(ws_bytes=need - 256) == 4          # workspace too small
+    assert b"workspace" in lib.mtp_last_error()

@@ -265,3 +265,66 @@ def test_lmhead_argmax_ties_lowest_index(dev):
     lmhead_argmax(y, None, 1e-6, desc2, tok, val)
     torch.cuda.synchronize()
     assert int(tok.item()) == 4321 and float(val.item()) == float(H)
+
+
+# ------------------------------------------------------------------ verify head
+@pytest.mark.parametrize("rows,H,V,mult,cap", [
+    (2, 256, 4096, 1.0, 0.0),        # plain logits
+    (3, 512, 6000, 0.5, 30.0),       # ragged vocabulary, multiplier and cap
+    (4, 256, 4096, 80.0, 5.0),       # cap in saturation (near-ties)
+    (1, 256, 4096, 1.0, 30.0),       # one row: the one-row kernel
+    (16, 256, 1000, 1.0, 0.0),       # most rows, vocabulary not a multiple of 32
+    (4, 5120, 151936, 1.0, 30.0),    # the 40/8-head layer's head, 4 rows
+])
+def test_verify_head_argmax(dev, rows, H, V, mult, cap):
+    import torch
+    from mtp_speculative_draft_gb300 import verify_head_argmax
+    rng = np.random.default_rng(V + rows)
+    w = seeded_affine(rng, V, H)
+    h = rng.standard_normal((rows, H)).astype(np.float32)
+    nw = (1 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    keep, desc = _w(w, dev)
+    ref, rtok, _, margin = O.verify_head(h, nw, 1e-6, w, mult if mult != 1.0 else None,
+                                         cap if cap > 0 else None)
+    tok = torch.full((rows,), -1, dtype=torch.int32, device=dev)
+    val = torch.zeros(rows, dtype=torch.float32, device=dev)
+    logits = torch.zeros((rows, V), dtype=torch.float32, device=dev)
+    ws = None
+    for call in range(2):  # the second call reuses the workspace the first left
+        ws = verify_head_argmax(_t(h, dev), rows, _t(nw, dev), 1e-6, desc, mult, cap, tok, val,
+                                logits, ws=ws)
+        torch.cuda.synchronize()
+        lg = logits.cpu().numpy()
+        assert_close(lg, ref, f"verify head logits call {call}")
+        t, v = tok.cpu().numpy(), val.cpu().numpy()
+        for r in range(rows):
+            assert_token(int(t[r]), rtok[r], margin[r], f"row {r}")
+            assert int(t[r]) == int(np.argmax(lg[r]))      # agrees with its own logits
+            assert float(v[r]) == float(lg[r, int(t[r])])
+    # without d_logits the logits stay in the workspace: same tokens
+    tok2 = torch.full((rows,), -1, dtype=torch.int32, device=dev)
+    verify_head_argmax(_t(h, dev), rows, _t(nw, dev), 1e-6, desc, mult, cap, tok2, val, None, ws=ws)
+    torch.cuda.synchronize()
+    assert np.array_equal(tok2.cpu().numpy(), tok.cpu().numpy())
+
+
+def test_verify_head_ties_lowest_index(dev):
+    """Planted equal maxima (bias-only head): each row's lowest index wins."""
+    import torch
+    from mtp_speculative_draft_gb300 import verify_head_argmax
+    H, V, rows = 256, 5000, 3
+    b = np.zeros((V, H // 32), np.float32)
+    b[[4321, 4999], :] = 1.0
+    b[77, :] = 0.5
+    keep, desc = _w((np.zeros((V, H // 8), np.uint32), np.zeros((V, H // 32), np.float32), b), dev)
+    h = np.ones((rows, H), np.float32)
+    h[2] = -1.0                                       # row 2: every planted logit negated
+    tok = torch.full((rows,), -1, dtype=torch.int32, device=dev)
+    val = torch.zeros(rows, dtype=torch.float32, device=dev)
+    verify_head_argmax(_t(h, dev), rows, None, 1e-6, desc, 1.0, 0.0, tok, val)
+    torch.cuda.synchronize()
+    assert tok.cpu().tolist() == [4321, 4321, 0] and val.cpu().tolist()[:2] == [float(H)] * 2
+    # a cap that saturates all three planted logits to 1.0: the lowest index wins
+    verify_head_argmax(_t(h, dev), rows, None, 1e-6, desc, 1.0, 1.0, tok, val)
+    torch.cuda.synchronize()
+    assert tok.cpu().tolist() == [77, 77, 0]

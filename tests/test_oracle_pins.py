@@ -347,6 +347,73 @@ def test_argmax_lowest_index():
 
 
 # ---------------------------------------------------------------------------
+# verify head (final norm, lm_head, multiplier, softcap, argmax per row)
+# ---------------------------------------------------------------------------
+
+def _bias_only_head(vals, H):
+    """lm_head [V, H] with zero codes and scales and per-row bias vals[v] / H,
+    so a row of ones has logit vals[v] (exact: the biases are powers-of-two
+    fractions of the values used below)."""
+    V = len(vals)
+    b = np.repeat((np.asarray(vals, np.float64) / H)[:, None], H // 32, axis=1).astype(np.float32)
+    return np.zeros((V, H // 8), np.uint32), np.zeros((V, H // 32), np.float32), b
+
+
+def test_verify_head_softcap_follows_tanh_series():
+    # c*tanh(l/c) = l - l^3/(3c^2) + 2l^5/(15c^4) - ... for |l| << c
+    H, c = 64, 10.0
+    w = _bias_only_head(np.linspace(-0.0625, 0.0625, 9), H)
+    ones = np.ones((1, H))
+    raw = O.qmatmul(ones, w)[0]
+    lg, _, _, _ = O.verify_head(ones, None, 0.0, w, final_softcap=c)
+    series = raw - raw ** 3 / (3 * c * c) + 2 * raw ** 5 / (15 * c ** 4)
+    assert np.max(np.abs(lg[0] - series)) < 1e-13
+    assert np.max(np.abs(raw - np.linspace(-0.0625, 0.0625, 9))) < 1e-15
+
+
+def test_verify_head_multiplier_comes_before_the_cap():
+    H, c = 64, 10.0
+    vals = np.array([-50.0, -3.0, 0.0, 0.5, 2.0, 40.0])
+    w = _bias_only_head(vals, H)
+    ones = np.ones((1, H))
+    lg, tok, val, _ = O.verify_head(ones, None, 0.0, w, logit_multiplier=2.0, final_softcap=c)
+    # capping last keeps every logit inside (-c, c); capping first and then
+    # doubling would reach 2c
+    assert np.all(np.abs(lg) < c) and np.max(np.abs(lg)) > 0.99 * c
+    assert tok == [5] and val[0] == lg[0, 5]             # monotone map: the largest stays largest
+    lg2, tok2, _, _ = O.verify_head(ones, None, 0.0, w, logit_multiplier=-1.0)
+    assert np.array_equal(lg2[0], -vals) and tok2 == [0]  # a negative multiplier reverses the order
+    lg3, tok3, _, _ = O.verify_head(ones, None, 0.0, w)  # neither: plain logits
+    assert np.array_equal(lg3[0], vals) and tok3 == [5]
+
+
+def test_verify_head_saturated_ties_go_to_lowest_index():
+    H = 64
+    w = _bias_only_head(np.array([1.0, 384.0, 512.0, 3.0]), H)
+    lg, tok, val, margin = O.verify_head(np.ones((1, H)), None, 0.0, w, final_softcap=1.0)
+    assert lg[0, 1] == lg[0, 2] == 1.0                  # tanh(384) and tanh(512) round to 1
+    # the argmax is taken on the capped logits (the raw maximum is index 2)
+    assert tok == [1] and val == [1.0] and margin == [0.0]
+
+
+def test_verify_head_rows_are_independent_and_normed():
+    rng = np.random.default_rng(5)
+    H, V = 128, 300
+    w = (rng.integers(0, 2 ** 32, size=(V, H // 8), dtype=np.uint64).astype(np.uint32),
+         (np.abs(0.02 * rng.standard_normal((V, H // 32))) / 8).astype(np.float32),
+         (1e-3 * rng.standard_normal((V, H // 32))).astype(np.float32))
+    nw = (1 + 0.1 * rng.standard_normal(H)).astype(np.float32)
+    h = rng.standard_normal((3, H))
+    lg, tok, _, _ = O.verify_head(h, nw, 0.0, w, 1.5, 30.0)
+    for r in range(3):
+        one, t1, _, _ = O.verify_head(h[r], nw, 0.0, w, 1.5, 30.0)
+        assert np.allclose(one[0], lg[r], rtol=0, atol=1e-12) and t1[0] == tok[r]
+    # the final RMSNorm makes every row scale-free (eps = 0)
+    scaled, ts, _, _ = O.verify_head(h * np.array([[7.0], [0.01], [-2.0]]), nw, 0.0, w, 1.5, 30.0)
+    assert np.allclose(scaled[[0, 1]], lg[[0, 1]], rtol=0, atol=1e-12) and ts[:2] == tok[:2]
+
+
+# ---------------------------------------------------------------------------
 # whole layer and chain
 # ---------------------------------------------------------------------------
 
