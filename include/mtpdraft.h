@@ -84,7 +84,10 @@ mtp_status mtp_workspace_init(void *d_ws, size_t bytes, void *stream);
  * copy); the first error since mtp_workspace_init is kept:
  *   0 none; 1 a wait for a TMA copy gave up; 2 a token id outside
  *   [0, vocab) (row 0 was used); 3 a wait inside a multi-projection launch
- *   for the previous projection's output gave up. */
+ *   for the previous projection's output gave up.
+ * After code 1 or 3 a launch stopped part-way and may have left completion
+ * counters set: clear the workspace with mtp_workspace_init() before its
+ * next use.  Code 2 leaves the workspace usable. */
 mtp_status mtp_workspace_status(const void *d_ws, int32_t *h_code, void *stream);
 
 /* ------------------------------------------------------------------------
