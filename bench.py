@@ -247,14 +247,20 @@ def dist_setup(args):
     return rank, world, local
 
 
-def barrier_max(world, value):
+def barrier_max(world, value, device="cuda"):
+    """The largest `value` over all ranks (an all-reduce; every rank returns it)."""
     if world == 1:
         return value
     import torch
     import torch.distributed as dist
-    t = torch.tensor([value], dtype=torch.float64, device="cuda")
+    t = torch.tensor([value], dtype=torch.float64, device=device)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
+
+
+def job_value(world, steps, ms_total_max):
+    """Whole-job draft tokens/s: the steps of every rank over the slowest rank's time."""
+    return world * steps / (ms_total_max / 1000.0)
 
 
 def run_reference(args):
@@ -363,7 +369,7 @@ def run_ours(args):
     clocks.stop()
     ms_total = barrier_max(world, ev0.elapsed_time(ev1))
     ms = ms_total / args.steps
-    value = world * args.steps / (ms_total / 1000.0)
+    value = job_value(world, args.steps, ms_total)
 
     # ---------------- per-kernel breakdown (events between launches, same steps)
     # The dominant kernel is the lm_head GEMV; time it alone in the same stream
@@ -423,7 +429,7 @@ def run_ours(args):
             e2e_step()
         t1 = time.perf_counter()
     e2e_s = barrier_max(world, t1 - t0)
-    e2e_val = world * e2e_steps / e2e_s
+    e2e_val = job_value(world, e2e_steps, 1000.0 * e2e_s)
     h2d = h_hidden.numel() * 4 + h_tokens.numel() * 4
     d2h = 8
 
