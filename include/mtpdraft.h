@@ -327,6 +327,52 @@ mtp_status mtp_draft_chain(const mtp_layer_desc *layers, int32_t n_layers,
                            int32_t m, float *d_values, float *d_hidden_out, void *d_ws,
                            size_t ws_bytes, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Speculation bookkeeping of one sequence (host only: no device work, no
+ * stream).  "cortiq-engine 0.8.49 src/mimo_mtp.rs": MtpStats (its counters
+ * and tokens_per_round), the accepted prefix of mimo_spec_round and
+ * mimo_verify_rewind.  A round drafts k tokens, the verifier scores the
+ * pending token and the k drafts in one batch (verify_head_argmax gives its
+ * greedy token per row), the drafts are kept while they equal the
+ * verifier's token at the same depth, and every cache is cut back to the
+ * kept positions.
+ * ------------------------------------------------------------------------ */
+#define MTP_SPEC_MAX_DEPTH 16
+
+/* Counters of one generation; zero-initialise before the first round. */
+typedef struct {
+    uint64_t rounds;                                 /* verify batches */
+    uint64_t drafted;                                /* drafts proposed */
+    uint64_t accepted;                               /* drafts accepted */
+    uint64_t accept_hist[MTP_SPEC_MAX_DEPTH + 1];    /* rounds that accepted exactly a drafts */
+    uint64_t depth_drafted[MTP_SPEC_MAX_DEPTH];      /* rounds that drafted depth d (0-based) */
+    uint64_t depth_accepted[MTP_SPEC_MAX_DEPTH];     /* rounds whose accepted prefix reached depth d */
+    uint64_t draft_ns;                               /* time in the drafts */
+    uint64_t verify_ns;                              /* time in the verify */
+} mtp_spec_stats;
+
+/* The accepted prefix: the largest a <= k with drafts[i] == verify_tokens[i]
+ * for every i < a, where verify_tokens[i] is the verifier's greedy token on
+ * the row after the pending token and drafts[0..i-1] (host arrays; entry k,
+ * the round's own next token, is not read).  Returns -1 when a pointer is
+ * NULL with k > 0 or k is outside 0..MTP_SPEC_MAX_DEPTH. */
+int32_t mtp_spec_accept(const int32_t *drafts, const int32_t *verify_tokens, int32_t k);
+
+/* Adds one round of k drafts with a accepted (0 <= a <= k <= MTP_SPEC_MAX_DEPTH)
+ * and its draft and verify times; MTP_ERR_INVALID_ARG otherwise (s unchanged). */
+mtp_status mtp_spec_note_round(mtp_spec_stats *s, int32_t k, int32_t a, uint64_t draft_ns,
+                               uint64_t verify_ns);
+
+/* Tokens a round emits on average: (accepted + rounds) / rounds (the
+ * accepted drafts plus the verifier's own token); 0 before the first round. */
+double mtp_spec_tokens_per_round(const mtp_spec_stats *s);
+
+/* After a rejected suffix: every cache_len[l] above `keep` becomes `keep`
+ * (an absolute row count, not a step back from a possibly stale cursor);
+ * lengths at or below it are unchanged.  MTP_ERR_INVALID_ARG on a NULL
+ * array with n_layers > 0, n_layers < 0 or keep < 0. */
+mtp_status mtp_spec_rewind(int32_t *cache_len, int32_t n_layers, int32_t keep);
+
 #ifdef __cplusplus
 }
 #endif

@@ -58,6 +58,17 @@ class StepIn(C.Structure):
                 ("m", i32)]
 
 
+SPEC_MAX_DEPTH = 16
+
+
+class SpecStats(C.Structure):
+    _fields_ = [("rounds", C.c_uint64), ("drafted", C.c_uint64), ("accepted", C.c_uint64),
+                ("accept_hist", C.c_uint64 * (SPEC_MAX_DEPTH + 1)),
+                ("depth_drafted", C.c_uint64 * SPEC_MAX_DEPTH),
+                ("depth_accepted", C.c_uint64 * SPEC_MAX_DEPTH),
+                ("draft_ns", C.c_uint64), ("verify_ns", C.c_uint64)]
+
+
 class StepOut(C.Structure):
     _fields_ = [("d_token", vp), ("d_value", vp), ("d_hidden_out", vp), ("d_u2", vp),
                 ("d_logits", vp)]
@@ -81,6 +92,10 @@ EXPORTS = {
     "lmhead_argmax_workspace_bytes": (sz, [i32, i32]),
     "lmhead_argmax": (C.c_int, [vp, vp, f32, C.POINTER(Affine4), vp, vp, vp, vp, vp, sz, vp]),
     "verify_head_workspace_bytes": (sz, [i32, i32, i32]),
+    "mtp_spec_accept": (i32, [C.POINTER(i32), C.POINTER(i32), i32]),
+    "mtp_spec_note_round": (C.c_int, [C.POINTER(SpecStats), i32, i32, C.c_uint64, C.c_uint64]),
+    "mtp_spec_tokens_per_round": (C.c_double, [C.POINTER(SpecStats)]),
+    "mtp_spec_rewind": (C.c_int, [C.POINTER(i32), i32, i32]),
     "verify_head_argmax": (C.c_int, [vp, i32, vp, f32, C.POINTER(Affine4), f32, f32, vp, vp, vp,
                                      vp, sz, vp]),
     "moe_ffn_workspace_bytes": (sz, [C.POINTER(MoeWeights), i32]),

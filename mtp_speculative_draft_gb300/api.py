@@ -7,7 +7,7 @@ import ctypes as C
 import torch
 
 from . import _lib as L
-from ._lib import Affine4, AttnGeom, MoeWeights, check
+from ._lib import Affine4, AttnGeom, MoeWeights, SpecStats, check
 
 
 def _p(t):
@@ -149,3 +149,38 @@ def mtp_draft_chain(descs, hidden, seq, cache_lens, m, values, hidden_out, ws, s
     check(L.load().mtp_draft_chain(arr, len(descs), _p(hidden), _p(seq), lens, m, _p(values),
                                    _p(hidden_out), _p(ws), ws.numel(), _stream(stream)),
           "mtp_draft_chain")
+
+
+# ------------------------------------------------------------- speculation bookkeeping (host)
+def _i32_array(values):
+    vals = [int(v) for v in values]
+    return (C.c_int32 * max(1, len(vals)))(*vals), len(vals)
+
+
+def mtp_spec_accept(drafts, verify_tokens) -> int:
+    """Length of the drafts' prefix that equals the verifier's greedy tokens."""
+    d, k = _i32_array(drafts)
+    v, n = _i32_array(verify_tokens)
+    if n < k:
+        raise ValueError("one verifier token per draft is required")
+    a = L.load().mtp_spec_accept(d, v, k)
+    if a < 0:
+        raise ValueError("mtp_spec_accept: k outside 0..16")
+    return a
+
+
+def mtp_spec_note_round(stats: SpecStats, k: int, a: int, draft_ns: int = 0, verify_ns: int = 0):
+    check(L.load().mtp_spec_note_round(C.byref(stats), k, a, draft_ns, verify_ns),
+          "mtp_spec_note_round")
+
+
+def mtp_spec_tokens_per_round(stats: SpecStats) -> float:
+    return L.load().mtp_spec_tokens_per_round(C.byref(stats))
+
+
+def mtp_spec_rewind(cache_len, keep: int) -> list:
+    """Cache lengths after cutting every one above ``keep`` back to ``keep``."""
+    arr, n = _i32_array(cache_len)
+    check(L.load().mtp_spec_rewind(arr, n, keep), "mtp_spec_rewind")
+    return list(arr[:n])
+

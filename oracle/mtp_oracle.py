@@ -392,3 +392,72 @@ def draft_chain(cfg, layers, lm_head, embed, caches, hidden, tokens, forced=None
         nxt = res["token"] if forced is None or forced[k] is None else int(forced[k])
         seq.append(nxt)
     return results
+
+
+# ---------------------------------------------------------------------------
+# Speculation bookkeeping (host)
+# ---------------------------------------------------------------------------
+
+def spec_accept(drafts, verify_tokens):
+    """Accepted drafts of one round.
+
+    [mimo_mtp.rs] ``mimo_spec_round``: walking the rows ``i = 0..=k`` of the
+    batched verify, the verifier's token at row ``i`` is compared with draft
+    ``i``; an equal token accepts the draft and the walk goes on, the first
+    unequal one (or row ``k``, which has no draft) ends it.
+    """
+    a = 0
+    for i in range(len(drafts) + 1):
+        if i < len(drafts) and int(verify_tokens[i]) == int(drafts[i]):
+            a += 1
+        else:
+            break
+    return a
+
+
+def spec_stats_new():
+    """[mimo_mtp.rs] ``MtpStats`` with every counter at zero."""
+    return {"rounds": 0, "drafted": 0, "accepted": 0, "accept_hist": [], "depth_drafted": [],
+            "depth_accepted": [], "draft_ns": 0, "verify_ns": 0}
+
+
+def spec_note_round(st, k, a, draft_ns=0, verify_ns=0):
+    """Counter updates at the end of [mimo_mtp.rs] ``mimo_spec_round``.
+
+    One more round, ``k`` more drafts, ``a`` more accepted; the histogram
+    grows to ``k + 1`` bins and counts ``a``; the per-depth lists grow to
+    ``k`` entries, every depth below ``k`` was drafted and every depth below
+    ``a`` was accepted.
+    """
+    st["draft_ns"] += draft_ns
+    st["verify_ns"] += verify_ns
+    st["rounds"] += 1
+    st["drafted"] += k
+    st["accepted"] += a
+    if len(st["accept_hist"]) <= k:
+        st["accept_hist"] += [0] * (k + 1 - len(st["accept_hist"]))
+    st["accept_hist"][a] += 1
+    if len(st["depth_drafted"]) < k:
+        st["depth_drafted"] += [0] * (k - len(st["depth_drafted"]))
+        st["depth_accepted"] += [0] * (k - len(st["depth_accepted"]))
+    for d in range(k):
+        st["depth_drafted"][d] += 1
+        if d < a:
+            st["depth_accepted"][d] += 1
+    return st
+
+
+def spec_tokens_per_round(st):
+    """[mimo_mtp.rs] ``MtpStats::tokens_per_round``: accepted drafts plus the
+    verifier's own token, per round (0 before any round)."""
+    if st["rounds"] == 0:
+        return 0.0
+    return (st["accepted"] + st["rounds"]) / st["rounds"]
+
+
+def spec_rewind(cache_len, keep):
+    """[mimo_mtp.rs] ``mimo_verify_rewind``: a layer holding more than ``keep``
+    rows drops the rows past ``keep`` (an absolute position); shorter layers
+    are left as they are."""
+    return [keep if n > keep else n for n in cache_len]
+

@@ -38,6 +38,8 @@ def test_struct_layouts_match_c(lib):
              sizeof(mtp_moe_weights), sizeof(mtp_layer_desc), sizeof(mtp_step_in), sizeof(mtp_step_out));
       printf("%zu %zu %zu\n", offsetof(mtp_layer_desc, lm_head), offsetof(mtp_layer_desc, cache_cap),
              offsetof(mtp_moe_weights, sh_gate_inp));
+      printf("%zu %zu %zu\n", sizeof(mtp_spec_stats), offsetof(mtp_spec_stats, depth_accepted),
+             offsetof(mtp_spec_stats, verify_ns));
       return 0; }
     '''
     with tempfile.TemporaryDirectory() as d:
@@ -50,7 +52,9 @@ def test_struct_layouts_match_c(lib):
     want = [C.sizeof(_lib.Affine4), C.sizeof(_lib.AttnGeom), C.sizeof(_lib.MoeWeights),
             C.sizeof(_lib.LayerDesc), C.sizeof(_lib.StepIn), C.sizeof(_lib.StepOut),
             _lib.LayerDesc.lm_head.offset, _lib.LayerDesc.cache_cap.offset,
-            _lib.MoeWeights.sh_gate_inp.offset]
+            _lib.MoeWeights.sh_gate_inp.offset,
+            C.sizeof(_lib.SpecStats), _lib.SpecStats.depth_accepted.offset,
+            _lib.SpecStats.verify_ns.offset]
     assert got == want
 
 

@@ -507,3 +507,49 @@ def test_chain_rows_take_earlier_drafts():
     res2 = O.draft_chain(cfg, layers, sh["lm_head"], embed, caches, step["hidden"], step["tokens"],
                          forced)
     assert res2[1]["tokens_in"][-1] == 5 and res2[2]["tokens_in"][-2:] == [5, 7]
+
+
+# ---------------------------------------------------------------------------
+# speculation bookkeeping (hand-worked rounds)
+# ---------------------------------------------------------------------------
+
+def test_spec_accept_prefix_by_hand():
+    assert O.spec_accept([5, 7, 9], [5, 7, 1, 3]) == 2   # third draft rejected
+    assert O.spec_accept([5, 7, 9], [4, 7, 9, 3]) == 0   # first draft rejected: nothing later counts
+    assert O.spec_accept([5, 7, 9], [5, 7, 9, 0]) == 3   # all drafts; row k is the bonus token
+    assert O.spec_accept([], [11]) == 0
+
+
+def test_spec_stats_by_hand():
+    st = O.spec_stats_new()
+    for k, a in [(3, 2), (3, 0), (3, 3)]:
+        O.spec_note_round(st, k, a, draft_ns=10, verify_ns=100)
+    assert (st["rounds"], st["drafted"], st["accepted"]) == (3, 9, 5)
+    assert st["accept_hist"] == [1, 0, 1, 1]
+    assert st["depth_drafted"] == [3, 3, 3] and st["depth_accepted"] == [2, 2, 1]
+    assert (st["draft_ns"], st["verify_ns"]) == (30, 300)
+    assert O.spec_tokens_per_round(st) == 8 / 3           # 5 accepted + 3 own tokens over 3 rounds
+    # a deeper round grows the histogram and the depth lists
+    st2 = O.spec_note_round(O.spec_note_round(O.spec_stats_new(), 1, 1), 4, 2)
+    assert st2["accept_hist"] == [0, 1, 1, 0, 0]
+    assert st2["depth_drafted"] == [2, 1, 1, 1] and st2["depth_accepted"] == [2, 1, 0, 0]
+    assert O.spec_tokens_per_round(O.spec_stats_new()) == 0.0
+
+
+def test_spec_stats_invariants():
+    rng = np.random.default_rng(3)
+    st = O.spec_stats_new()
+    for _ in range(200):
+        k = int(rng.integers(0, 6))
+        O.spec_note_round(st, k, int(rng.integers(0, k + 1)))
+    hist = st["accept_hist"]
+    assert sum(hist) == st["rounds"]
+    assert sum(a * n for a, n in enumerate(hist)) == st["accepted"]
+    assert sum(st["depth_accepted"]) == st["accepted"] and sum(st["depth_drafted"]) == st["drafted"]
+    assert 1.0 <= O.spec_tokens_per_round(st) <= 6.0
+
+
+def test_spec_rewind_by_hand():
+    assert O.spec_rewind([10, 12, 7], 9) == [9, 9, 7]
+    assert O.spec_rewind([10, 12, 7], 20) == [10, 12, 7]
+    assert O.spec_rewind([10, 12, 7], 0) == [0, 0, 0]
