@@ -64,6 +64,29 @@ def dequant(w) -> np.ndarray:
     return codes * s64 + b64
 
 
+def bf16_round(x) -> np.ndarray:
+    """float32 values rounded to bfloat16 (kept as float64).
+
+    [shared.rs] ``MlxAffineMoeStack``: the expert stacks hold their scales
+    and biases as BF16, cast from the float32 per-expert values at upload.
+    Reading (the cast itself is not on the pages): round to nearest, ties
+    to even, on the top 16 bits of the float32 pattern.
+    """
+    bits = np.asarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    keep = bits >> np.uint64(16)
+    rest = bits & np.uint64(0xFFFF)
+    up = (rest > np.uint64(0x8000)) | ((rest == np.uint64(0x8000)) & ((keep & np.uint64(1)) == np.uint64(1)))
+    keep = keep + up.astype(np.uint64)
+    return (keep << np.uint64(16)).astype(np.uint32).view(np.float32).astype(np.float64)
+
+
+def moe_stack_bf16(w):
+    """An expert stack ``(q, s, b)`` as [shared.rs] ``MlxAffineMoeStack``
+    stores it: the same codes, scales and biases rounded to BF16."""
+    q, s, b = w
+    return q, bf16_round(s), bf16_round(b)
+
+
 def weight_shape(w):
     q, _, _ = w
     return q.shape[0], q.shape[1] * PACK
@@ -367,6 +390,42 @@ def draft_layer(cfg, w, lm_head, k_cache, v_cache, hidden, embed_rows, pos0=None
         tok, val, margin = argmax_lowest(logits)
         out.update(logits=logits, token=tok, value=val, margin=margin)
     return out
+
+
+def kv_catch_up(cfg, w, embed_rows, target_hidden, pending_hidden=None, pos0=0):
+    """KV catch-up of a target batch: ``(k_new [seq, nkv, dqk], v_new [seq, nkv, dv])``.
+
+    [mtp.rs] ``process_target_batch``: the target's hidden rows are used
+    shifted one row right (row 0 is the pending hidden, or zeros for a cold
+    prompt; row ``i > 0`` is target row ``i - 1``), projected with the
+    embedding rows by ``project_embedding_and_hidden``, then
+    ``append_attention_kv``: attention RMSNorm, the ``W_k`` and ``W_v``
+    projections, per-head k RMSNorm (when the layer has it), RoPE at each
+    row's position, and the rows go to the cache at ``pos0 + i``.  Nothing
+    else runs (no attention, FFN or logits).  Reading: the text rows' four
+    rotary position ids are equal, so the rotation is the 1-D RoPE at
+    ``pos0 + i``, as in the draft step.
+    """
+    eps = cfg.eps
+    nkv, dqk, dv = cfg.n_kv_heads, cfg.head_dim_qk, cfg.head_dim_v
+    e = np.atleast_2d(np.asarray(embed_rows, dtype=np.float64))
+    t = np.atleast_2d(np.asarray(target_hidden, dtype=np.float64))
+    seq = e.shape[0]
+    assert t.shape == e.shape and seq > 0
+    shifted = np.zeros_like(t)
+    if pending_hidden is not None:
+        shifted[0] = np.asarray(pending_hidden, dtype=np.float64)
+    shifted[1:] = t[:-1]
+    e_n = rmsnorm(e, w["enorm"], 1e-6)
+    h_n = rmsnorm(shifted, w["hnorm"], 1e-6)
+    u = qmatmul(np.concatenate([e_n, h_n], axis=1), w["eh_proj"])
+    x = rmsnorm(u, w["attn_norm"], eps)
+    k = qmatmul(x, w["wk"]).reshape(seq, nkv, dqk)
+    v = qmatmul(x, w["wv"]).reshape(seq, nkv, dv)
+    if cfg.qk_norm:
+        k = rmsnorm(k, w["k_norm"], eps)
+    k = np.stack([rope(k[i], pos0 + i, cfg.rope_theta, cfg.rot_dim) for i in range(seq)])
+    return k, v
 
 
 def draft_chain(cfg, layers, lm_head, embed, caches, hidden, tokens, forced=None):

@@ -553,3 +553,88 @@ def test_spec_rewind_by_hand():
     assert O.spec_rewind([10, 12, 7], 9) == [9, 9, 7]
     assert O.spec_rewind([10, 12, 7], 20) == [10, 12, 7]
     assert O.spec_rewind([10, 12, 7], 0) == [0, 0, 0]
+
+
+# ---------------------------------------------------------------------------
+# KV catch-up of a target batch
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("qk_norm", [True, False])
+def test_kv_catch_up_rows_equal_draft_steps(qk_norm):
+    """Row i of the catch-up is the K/V row a one-row draft step appends for
+    the same embedding, the shifted target hidden and position pos0 + i
+    (computed there together with attention, FFN and head)."""
+    cfg = _tiny_cfg(qk_norm=qk_norm)
+    w = make_layer_weights(cfg)
+    rng = np.random.default_rng(21)
+    seq, pos0, H = 4, 6, cfg.hidden
+    e = rng.standard_normal((seq, H))
+    t = rng.standard_normal((seq, H))
+    pend = rng.standard_normal(H)
+    k, v = O.kv_catch_up(cfg, w, e, t, pending_hidden=pend, pos0=pos0)
+    lm = w["eh_proj"]  # any weight serves as a head here; only the K/V rows are compared
+    shifted = [pend] + [t[i - 1] for i in range(1, seq)]
+    for i in range(seq):
+        kc = np.zeros((cfg.n_kv_heads, pos0 + i + 1, cfg.head_dim_qk))
+        vc = np.zeros((cfg.n_kv_heads, pos0 + i + 1, cfg.head_dim_v))
+        one = O.draft_layer(cfg, w, lm, kc, vc, shifted[i], e[i], pos0=pos0 + i, want_logits=False)
+        assert np.allclose(k[i], one["k_new"][0], rtol=0, atol=1e-12)
+        assert np.allclose(v[i], one["v_new"][0], rtol=0, atol=1e-12)
+
+
+def test_kv_catch_up_shift_and_cold_prompt():
+    cfg = _tiny_cfg()
+    w = make_layer_weights(cfg)
+    rng = np.random.default_rng(22)
+    seq, H = 5, cfg.hidden
+    e = rng.standard_normal((seq, H))
+    t = rng.standard_normal((seq, H))
+    # a cold prompt's first row reads a zero hidden
+    k0, v0 = O.kv_catch_up(cfg, w, e, t)
+    kz, vz = O.kv_catch_up(cfg, w, e, t, pending_hidden=np.zeros(H))
+    assert np.array_equal(k0, kz) and np.array_equal(v0, vz)
+    # splitting the batch: the second part's pending hidden is the last target row of the first
+    k1, v1 = O.kv_catch_up(cfg, w, e[:2], t[:2], pos0=0)
+    k2, v2 = O.kv_catch_up(cfg, w, e[2:], t[2:], pending_hidden=t[1], pos0=2)
+    assert np.allclose(np.concatenate([k1, k2]), k0, rtol=0, atol=1e-12)
+    assert np.allclose(np.concatenate([v1, v2]), v0, rtol=0, atol=1e-12)
+    # the last target row is never read (it belongs to the next batch)
+    t2 = t.copy()
+    t2[-1] += 100.0
+    k3, _ = O.kv_catch_up(cfg, w, e, t2)
+    assert np.array_equal(k3, k0)
+
+
+# ---------------------------------------------------------------------------
+# BF16 scales and biases of the expert stacks
+# ---------------------------------------------------------------------------
+
+def test_bf16_round_halfway_cases_by_hand():
+    u = 2.0 ** -7  # spacing of bfloat16 at 1.0 (7 stored mantissa bits)
+    assert O.bf16_round([1.0, -3.0, 0.5, 2.0 ** -10, 0.0])[:4].tolist() == [1.0, -3.0, 0.5, 2.0 ** -10]
+    assert O.bf16_round(1 + u / 2)[()] == 1.0                 # halfway, 1.0 is even: down
+    assert O.bf16_round(1 + 3 * u / 2)[()] == 1 + 2 * u       # halfway, 1 + u is odd: up
+    assert O.bf16_round(1 + u / 2 + 2.0 ** -20)[()] == 1 + u  # just above halfway: up
+    assert O.bf16_round(-(1 + u / 2 + 2.0 ** -20))[()] == -(1 + u)
+
+
+def test_bf16_round_matches_library_conversion_and_bound():
+    torch = pytest.importorskip("torch")
+    rng = np.random.default_rng(31)
+    x = (rng.standard_normal(20000) * np.exp(rng.uniform(-20, 20, 20000))).astype(np.float32)
+    ours = O.bf16_round(x)
+    lib = torch.from_numpy(x).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(ours, lib)
+    assert np.max(np.abs(ours - x) / np.abs(x.astype(np.float64))) <= 2.0 ** -8
+
+
+def test_moe_stack_bf16_keeps_codes_and_rounds_only_scales():
+    rng = np.random.default_rng(32)
+    q = rng.integers(0, 2 ** 32, size=(6, 8), dtype=np.uint64).astype(np.uint32)
+    s = (np.abs(0.02 * rng.standard_normal((6, 2))) / 8).astype(np.float32)
+    b = (-8 * s + 1e-3 * rng.standard_normal((6, 2))).astype(np.float32)
+    q2, s2, b2 = O.moe_stack_bf16((q, s, b))
+    assert q2 is q and np.array_equal(s2, O.bf16_round(s)) and np.array_equal(b2, O.bf16_round(b))
+    # exactly representable scales and biases: the dequantised matrix is unchanged
+    se, be = O.bf16_round(s).astype(np.float32), O.bf16_round(b).astype(np.float32)
+    assert np.array_equal(O.dequant(O.moe_stack_bf16((q, se, be))), O.dequant((q, se, be)))
