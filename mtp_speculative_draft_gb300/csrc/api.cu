@@ -307,22 +307,34 @@ static AttnParams make_attn(const mtp_attn_geom* g, const float* qp, const float
   return a;
 }
 
+// Every check of attn_decode_sink's arguments except the workspace (shared
+// with attn_decode_sink_noalloc, which runs it before touching its scratch).
+static mtp_status check_attn_args(const mtp_attn_geom* g, const float* d_qp, const float* d_kp,
+                                  const float* d_vp, const float* d_rope, const float* d_k_cache,
+                                  const float* d_v_cache, int32_t cache_len, int32_t cache_cap,
+                                  int32_t m, const float* d_out, const char* who) {
+  mtp_status s = check_geom(g, m);
+  if (s != MTP_OK) return s;
+  const std::string w(who);
+  if (!d_qp || !d_kp || !d_vp || !d_rope || !d_k_cache || !d_v_cache || !d_out)
+    return fail(MTP_ERR_INVALID_ARG, w + ": null pointer");
+  if (!aligned16(d_qp) || !aligned16(d_kp) || !aligned16(d_vp) || !aligned16(d_k_cache) ||
+      !aligned16(d_v_cache) || !aligned16(d_out))
+    return fail(MTP_ERR_INVALID_ARG, w + ": pointers must be 16-byte aligned");
+  if (cache_len < 0 || cache_cap <= 0) return fail(MTP_ERR_INVALID_ARG, w + ": bad cache length");
+  if (cache_len + m > cache_cap)
+    return fail(MTP_ERR_CAPACITY, w + ": cache_len + m exceeds the cache capacity");
+  return MTP_OK;
+}
+
 mtp_status attn_decode_sink(const mtp_attn_geom* g, const float* d_qp, const float* d_kp,
                             const float* d_vp, const float* d_q_norm, const float* d_k_norm,
                             const float* d_rope, const float* d_sinks, float* d_k_cache,
                             float* d_v_cache, int32_t cache_len, int32_t cache_cap, int32_t m,
                             float* d_out, void* d_ws, size_t ws_bytes, void* stream) {
-  mtp_status s = check_geom(g, m);
+  mtp_status s = check_attn_args(g, d_qp, d_kp, d_vp, d_rope, d_k_cache, d_v_cache, cache_len,
+                                 cache_cap, m, d_out, "attn_decode_sink");
   if (s != MTP_OK) return s;
-  if (!d_qp || !d_kp || !d_vp || !d_rope || !d_k_cache || !d_v_cache || !d_out)
-    return fail(MTP_ERR_INVALID_ARG, "attn_decode_sink: null pointer");
-  if (!aligned16(d_qp) || !aligned16(d_kp) || !aligned16(d_vp) || !aligned16(d_k_cache) ||
-      !aligned16(d_v_cache) || !aligned16(d_out))
-    return fail(MTP_ERR_INVALID_ARG, "attn_decode_sink: pointers must be 16-byte aligned");
-  if (cache_len < 0 || cache_cap <= 0)
-    return fail(MTP_ERR_INVALID_ARG, "attn_decode_sink: bad cache length");
-  if (cache_len + m > cache_cap)
-    return fail(MTP_ERR_CAPACITY, "attn_decode_sink: cache_len + m exceeds the cache capacity");
   if (!d_ws || ws_bytes < attn_decode_sink_workspace_bytes(g, m, cache_len))
     return fail(MTP_ERR_WORKSPACE, "attn_decode_sink: workspace too small");
   AttnParams a = make_attn(g, d_qp, d_kp, d_vp, d_q_norm, d_k_norm, d_rope, d_sinks, d_k_cache,
@@ -1097,9 +1109,11 @@ mtp_status attn_decode_sink_noalloc(const mtp_attn_geom* g, const float* d_qp, c
                                     const float* d_sinks, float* d_k_cache, float* d_v_cache,
                                     int32_t cache_len, int32_t cache_cap, int32_t m,
                                     float* d_out, void* stream) {
-  mtp_status s = check_geom(g, m);
+  // every argument is checked before the scratch is set up or cleared, so an
+  // invalid call does no device work
+  mtp_status s = check_attn_args(g, d_qp, d_kp, d_vp, d_rope, d_k_cache, d_v_cache, cache_len,
+                                 cache_cap, m, d_out, "attn_decode_sink_noalloc");
   if (s != MTP_OK) return s;
-  if (cache_len < 0) return fail(MTP_ERR_INVALID_ARG, "attn_decode_sink_noalloc: bad cache length");
   const size_t need = attn_decode_sink_workspace_bytes(g, m, cache_len);
   if (need > kNoallocScratchBytes)
     return fail(MTP_ERR_WORKSPACE,

@@ -164,3 +164,24 @@ def test_verify_head_rejects_bad_calls(lib):
     assert call(wt=_fake_affine(1000, 96)) == 2    # K % 128 != 0
     assert call(ws_bytes=need - 256) == 4          # workspace too small
     assert b"workspace" in lib.mtp_last_error()
+
+
+def test_noalloc_attention_rejects_before_touching_its_scratch(lib):
+    # Every argument is checked before the static scratch is looked up or
+    # cleared: without a GPU an invalid call still returns its own code (a
+    # CUDA call would have failed with MTP_ERR_CUDA = 5 instead).
+    from mtp_speculative_draft_gb300 import _lib
+    g = _lib.AttnGeom(8, 2, 128, 128, 128, 0, 0, 1e-6, 0.0)
+    p = C.c_void_p(0x100000)
+    full = [p] * 9
+    assert lib.attn_decode_sink_noalloc(C.byref(g), None, *full[1:], 0, 10, 1, p, None) == 1
+    odd = [p] * 7 + [C.c_void_p(0x100004), p]      # misaligned K cache
+    assert lib.attn_decode_sink_noalloc(C.byref(g), *odd, 0, 10, 1, p, None) == 1
+    assert lib.attn_decode_sink_noalloc(C.byref(g), *full, 10, 10, 1, p, None) == 3
+    assert lib.attn_decode_sink_noalloc(C.byref(g), *full, 0, 10, 1, None, None) == 1
+    # a geometry whose scratch exceeds the static array is refused too
+    # (one KV head of 16 query heads, 256-dim heads, 4096 cached rows: about
+    # 148 splits x 16 rows x 258 floats of partials)
+    big = _lib.AttnGeom(16, 1, 256, 256, 256, 0, 0, 1e-6, 0.0)
+    assert lib.attn_decode_sink_workspace_bytes(C.byref(big), 1, 4096) > 2 << 20
+    assert lib.attn_decode_sink_noalloc(C.byref(big), *full, 4096, 4104, 1, p, None) == 4

@@ -7,6 +7,7 @@ quantised-matmul sweep are checked on sampled output rows.
 import numpy as np
 import pytest
 
+from golden.fixtures import affine_fixture, affine_fixtures
 from helpers import assert_close, assert_token, seeded_affine
 from oracle import mtp_oracle as O
 
@@ -52,22 +53,23 @@ def test_qmatmul_tma_path(dev, m, n, k):
     assert_close(y.cpu().numpy(), O.qmatmul(x, w), f"qmatmul m={m} n={n} k={k}")
 
 
-def test_qmatmul_page_fixtures(dev):
+@pytest.mark.parametrize("fx", affine_fixtures(include_derived=True), ids=lambda f: f.name)
+def test_qmatmul_page_fixtures(dev, fx):
+    """The pages' three qmatmul fixtures (K 96, 64, 32: the plain path) and the
+    first one's formulas at K = 256 (the tensor-map path)."""
     import torch
     import mtp_synth
-    from golden.fixtures import affine_fixture, affine_fixture_shapes
     from mtp_speculative_draft_gb300 import qmatmul_affine4
-    for m, n, k, tol in affine_fixture_shapes():
-        codes, s, b, x = affine_fixture(m, n, k)
-        w = (mtp_synth.pack_codes(codes), s, b)
-        keep, desc = _w(w, dev)
-        y = torch.zeros((m, n), dtype=torch.float32, device=dev)
-        qmatmul_affine4(_t(x, dev), desc, y, m)
-        torch.cuda.synchronize()
-        ref = O.qmatmul(x, w)
-        got = y.cpu().numpy()
-        assert np.max(np.abs(got - ref)) < tol        # the page's own criterion
-        assert_close(got, ref, f"fixture m={m} n={n} k={k}")
+    codes, s, b, x = affine_fixture(fx)
+    w = (mtp_synth.pack_codes(codes), s, b)
+    keep, desc = _w(w, dev)
+    y = torch.zeros((fx.m, fx.n), dtype=torch.float32, device=dev)
+    qmatmul_affine4(_t(x, dev), desc, y, fx.m)
+    torch.cuda.synchronize()
+    ref = O.qmatmul(x, w)
+    got = y.cpu().numpy()
+    assert np.max(np.abs(got - ref)) < fx.tol        # the page's own criterion
+    assert_close(got, ref, f"fixture {fx.name}")
 
 
 def test_qmatmul_repeatable_bitwise(dev):

@@ -13,7 +13,7 @@ import numpy as np
 import pytest
 
 import mtp_synth
-from golden.fixtures import affine_fixture, affine_fixture_shapes
+from golden.fixtures import affine_fixture, affine_fixtures
 from oracle import mtp_oracle as O
 from mtp_synth.configs import CONFIGS, make_layer_weights, make_shared, make_state, make_step
 
@@ -60,9 +60,37 @@ def test_unpack_low_nibble_first():
 
 
 def test_pack_unpack_roundtrip_page_fixture():
-    for m, n, k, _ in affine_fixture_shapes():
-        codes, _, _, _ = affine_fixture(m, n, k)
+    for fx in affine_fixtures(include_derived=True):
+        codes, _, _, _ = affine_fixture(fx)
         assert np.array_equal(O.unpack_codes(mtp_synth.pack_codes(codes)), codes)
+
+
+def test_page_fixture_formulas_by_hand():
+    # The reader against the formulas of each page test, element by element
+    # for the first entries (hand-evaluated): "hf2q 0.1.1 ... forward_mlx_shared.rs",
+    # from_mlx_affine_linear_roundtrips_through_packed_kernel,
+    # dispatch_qmatmul_routes_affine_weight_to_packed_kernel,
+    # dispatch_qmatmul_affine_equals_direct_kernel.
+    fx = {f.name: f for f in affine_fixtures()}
+    assert [(f.m, f.n, f.k) for f in fx.values()] == [(16, 64, 96), (8, 32, 64), (4, 32, 32)]
+    c, s, b, x = affine_fixture(fx["roundtrips_through_packed_kernel"])
+    assert c.ravel()[:4].tolist() == [5, 0, 11, 6]          # (11i + 5) % 16
+    assert s.ravel()[2] == np.float32(0.05) + np.float32(2.0) * np.float32(0.0017)
+    assert b.ravel()[3] == np.float32(-0.13) + np.float32(3.0) * np.float32(0.0023)
+    assert abs(float(x.ravel()[0]) - 0.6 * math.sin(-0.4)) < 1e-6
+    assert abs(float(x.ravel()[100]) - 0.6 * math.sin(1.3 - 0.4)) < 1e-6
+    c, s, b, x = affine_fixture(fx["routes_affine_weight_to_packed"])
+    assert c.ravel()[:4].tolist() == [3, 10, 1, 8]           # (7i + 3) % 16
+    assert s.ravel()[1] == np.float32(0.07) + np.float32(0.0011)
+    assert b.ravel()[1] == np.float32(-0.09) + np.float32(0.0027)
+    assert abs(float(x.ravel()[0]) - 0.5 * math.cos(-0.3)) < 1e-6
+    assert abs(float(x.ravel()[50]) - 0.5 * math.cos(0.55 - 0.3)) < 1e-6
+    c, s, b, x = affine_fixture(fx["affine_equals_direct_kernel"])
+    assert c.ravel()[:4].tolist() == [1, 6, 11, 0]           # (5i + 1) % 16
+    assert s.ravel()[5] == np.float32(0.05) + np.float32(5.0) * np.float32(0.001)
+    assert b.ravel()[5] == np.float32(-0.1) + np.float32(5.0) * np.float32(0.002)
+    assert abs(float(x.ravel()[0]) - 0.4 * math.sin(0.2)) < 1e-6
+    assert abs(float(x.ravel()[10]) - 0.4 * math.sin(0.17 + 0.2)) < 1e-6
 
 
 def test_dequant_single_word():
@@ -92,10 +120,10 @@ def _brute_qmatmul(codes, scales, biases, x, group=32):
     return np.array(y)
 
 
-@pytest.mark.parametrize("shape", affine_fixture_shapes())
-def test_qmatmul_page_fixtures_brute_force(shape):
-    m, n, k, tol = shape
-    codes, s, b, x = affine_fixture(m, n, k)
+@pytest.mark.parametrize("fx", affine_fixtures(include_derived=True), ids=lambda f: f.name)
+def test_qmatmul_page_fixtures_brute_force(fx):
+    m, n, tol = fx.m, fx.n, fx.tol
+    codes, s, b, x = affine_fixture(fx)
     w = (mtp_synth.pack_codes(codes), s, b)
     got = O.qmatmul(x, w)
     ref = _brute_qmatmul(codes, s, b, x)
@@ -486,6 +514,48 @@ def test_layer_attention_single_key_and_gate():
     # the appended key is normed then rotated at position 0 (identity)
     k = (x @ O.dequant(w["wk"]).T).reshape(cfg.n_kv_heads, cfg.head_dim_qk)
     assert np.allclose(res["k_new"][0], O.rmsnorm(k, w["k_norm"], cfg.eps))
+
+
+def _hand_rmsnorm(v, w, eps):
+    # x / sqrt(mean(x^2) + eps) * w, element by element
+    ms = sum(float(t) * float(t) for t in v) / len(v)
+    return [float(t) / math.sqrt(ms + eps) * float(wi) for t, wi in zip(v, w)]
+
+
+def _hand_rope(v, pos, theta, rot):
+    # pairs (i, i + rot/2) rotated by pos * theta^(-2i/rot)
+    out = [float(t) for t in v]
+    half = rot // 2
+    for i in range(half):
+        ang = pos * theta ** (-2.0 * i / rot)
+        a, b = float(v[i]), float(v[i + half])
+        out[i] = a * math.cos(ang) - b * math.sin(ang)
+        out[i + half] = a * math.sin(ang) + b * math.cos(ang)
+    return out
+
+
+def test_layer_head_norm_comes_before_rope():
+    """"hf2q 0.1.13 ... mtp.rs" forward_full_attention: the per-head q/k
+    RMSNorm runs first, RoPE on the normed vector after it.  At a position
+    p > 0 with a non-uniform norm weight the two orders differ, so the
+    appended key pins the order (the query enters the attention the same way)."""
+    cfg = _tiny_cfg(cache_len=7)
+    w = make_layer_weights(cfg)
+    kn = np.asarray(w["k_norm"], np.float64)
+    assert np.ptp(kn) > 0.05                      # the weight is not uniform
+    sh = make_shared(cfg)
+    st = make_state(cfg)
+    step = make_step(cfg)
+    e = sh["embed"][step["tokens"]]
+    res = O.draft_layer(cfg, w, sh["lm_head"], st["k_cache"], st["v_cache"], step["hidden"], e)
+    x = O.rmsnorm(res["u"], w["attn_norm"], cfg.eps)
+    k = (x @ O.dequant(w["wk"]).T).reshape(cfg.n_kv_heads, cfg.head_dim_qk)
+    p = cfg.cache_len
+    for h in range(cfg.n_kv_heads):
+        norm_then_rope = _hand_rope(_hand_rmsnorm(k[h], kn, cfg.eps), p, cfg.rope_theta, cfg.rot_dim)
+        rope_then_norm = _hand_rmsnorm(_hand_rope(k[h], p, cfg.rope_theta, cfg.rot_dim), kn, cfg.eps)
+        assert np.allclose(res["k_new"][0, h], norm_then_rope, rtol=1e-12, atol=1e-12)
+        assert np.max(np.abs(np.subtract(norm_then_rope, rope_then_norm))) > 1e-3
 
 
 def test_chain_rows_take_earlier_drafts():
