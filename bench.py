@@ -1,10 +1,20 @@
 """Benchmark of the MTP draft-layer forward on one GB300 (or N replicas).
 
-Workload: the Qwen-style dense draft layer (hidden 5120, 40/8 heads, head 128,
-sigmoid-gated q, per-head q/k norm, 4096-token cache, SwiGLU 17408, vocab
-151936, affine 4-bit group-32 weights) at m = 1: one step = one full draft
-forward (embedding gather through lm_head argmax).  Weights are 0.92 GB, far
-above the 129 MB L2, so every step streams them from HBM.
+Default workload: the Qwen-style dense draft layer (hidden 5120, 40/8 heads,
+head 128, sigmoid-gated q, per-head q/k norm, 4096-token cache, SwiGLU 17408,
+vocab 151936, affine 4-bit group-32 weights) at m = 1: one step = one full
+draft forward (embedding gather through lm_head argmax).  Weights are 0.92 GB,
+far above the 129 MB L2, so every step streams them from HBM.
+
+``--config`` selects another workload: ``tiny_dense`` (microseconds per
+draft; the 1.4 MB layer stays in L2, so it is latency-bound),
+``mimo_chain`` (three chained layers of 4 rows each), ``moe`` (256 experts,
+top 8 + shared; L2 flushed between steps) or ``qmatmul_sweep`` (the bare
+projection at m in {1, 2, 4, 8, 16} over four shapes).
+
+Each launch of a step is also timed alone (CUDA events recorded between the
+library's launches on its stream, mtp_timing_begin/end), which gives the
+roofline of the step's dominant launch.
 
 Prints one JSON line.  ``--impl reference`` times the CPU oracle instead (the
 pages publish no runnable implementation of this path).
@@ -30,6 +40,9 @@ if ROOT not in sys.path:
 METRIC = "MTP draft tokens/sec per layer (m=1) and HBM GB/s vs ~8 TB/s roofline"
 UNIT = "draft tokens/s"
 WORKLOAD = "qwen_dense"
+CONFIG_CHOICES = ["tiny_dense", "qwen_dense", "mimo_chain", "moe", "qmatmul_sweep"]
+DTYPE = ("int4-affine weights (f32 scales/biases); f32 activations split into f16 hi+lo parts "
+         "for the tensor-core products; f32 accumulate")
 
 
 def parse():
@@ -38,44 +51,58 @@ def parse():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", default=WORKLOAD)
+    ap.add_argument("--config", default=WORKLOAD, choices=CONFIG_CHOICES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--profile-kernel", default=None, choices=["lm_head", "ffn_down", "attention", "verify_head"],
+    ap.add_argument("--profile-kernel", default=None,
+                    choices=["lm_head", "ffn_down", "attention", "verify_head", "step"],
                     help="run only one entry point of the workload (small device footprint, for ncu)")
     return ap.parse_args()
 
 
 # --------------------------------------------------------------- accounting
-def layer_bytes(cfg):
-    """Algorithmic HBM bytes of one draft step, by sub-step (weights at 0.75 B/element)."""
+def aff(n, k):
+    """Algorithmic bytes of an affine 4-bit group-32 weight [n, k]: 0.75 B per element."""
+    return n * k * 3 // 4
+
+
+def attn_keys(cfg):
+    cached = min(cfg.cache_len, cfg.window - 1) if cfg.window > 0 else cfg.cache_len
+    return cached + cfg.m
+
+
+def launch_plan(cfg):
+    """(name, algorithmic HBM bytes) of each launch of one draft step, in the
+    order the library enqueues them (weights at 0.75 B per element, the KV
+    rows the attention reads, the activation rows read from memory)."""
     H, m = cfg.hidden, cfg.m
-    aff = lambda n, k: n * k * 3 // 4  # noqa: E731
     nh, nkv, dq, dv = cfg.n_heads, cfg.n_kv_heads, cfg.head_dim_qk, cfg.head_dim_v
-    keys = (min(cfg.cache_len, cfg.window - 1) if cfg.window > 0 else cfg.cache_len) + m
-    b = {
-        "eh_proj": aff(H, 2 * H) + 4 * (H + 2 * H * m),
-        "qkv": aff(cfg.q_rows + nkv * (dq + dv), H) + 4 * H * m,
-        "attention": 4 * keys * nkv * (dq + dv),
-        "o_proj": aff(H, nh * dv),
-    }
+    eh = aff(H, 2 * H) + 4 * (H + 2 * H * m)
+    qkv = aff(cfg.q_rows + nkv * (dq + dv), H) + 4 * H * m
+    attn = 4 * attn_keys(cfg) * nkv * (dq + dv)
+    o = aff(H, nh * dv)
+    lm = aff(cfg.vocab, H) + 4 * H
     if cfg.moe:
-        E, I = cfg.n_experts, cfg.expert_intermediate
-        b["ffn"] = 4 * E * H + (cfg.top_k + 1) * 3 * aff(I, H)
-    else:
-        b["ffn"] = 3 * aff(cfg.intermediate, H)
-    b["lm_head"] = aff(cfg.vocab, H) + 4 * H
-    return b
+        E, Ie, k = cfg.n_experts, cfg.expert_intermediate, cfg.top_k
+        return [("launch A: embedding pack + eh_proj + q/k/v", eh + qkv), ("attention", attn),
+                ("o_proj", o), ("router", 4 * E * H),
+                ("expert gate/up", (k + 1) * 2 * aff(Ie, H)),
+                ("expert down", (k + 1) * aff(H, Ie)), ("final norm", 4 * H),
+                ("lm_head + argmax", lm)]
+    I = cfg.intermediate
+    gu, dn = 2 * aff(I, H), aff(H, I)
+    if m == 1:
+        plan = [("launch A: embedding pack + eh_proj + q/k/v", eh + qkv), ("attention", attn),
+                ("launch B: split merge + o_proj + gate/up + down + lm_head", o + gu + dn + lm)]
+        if H % 256:
+            plan.insert(0, ("embedding/hidden norm pack", 4 * 2 * H))
+        return plan
+    return [("embedding/hidden norm pack", 4 * 2 * H * m), ("eh_proj", eh), ("q/k/v", qkv),
+            ("attention", attn), ("o_proj", o), ("gate/up", gu), ("down", dn),
+            ("lm_head + argmax", lm)]
 
 
-def launches_per_step(cfg):
-    # m = 1 dense: one-row launch A (embedding pack + eh_proj + q/k/v), attention,
-    # one-row launch B (split merge + o_proj + gate/up + down + lm_head).
-    # m > 1 dense: norm/pack, eh_proj, q/k/v, attention, o_proj, gate/up, down, lm_head.
-    # MoE (m = 1): launch A, attention, o_proj, router, expert gate/up, expert down,
-    # final norm, lm_head.
-    if cfg.moe:
-        return 8
-    return 3 if cfg.m == 1 else 8
+def step_bytes(cfg):
+    return sum(b for _, b in launch_plan(cfg)) * max(1, cfg.n_layers)
 
 
 # --------------------------------------------------------------- clocks
@@ -128,7 +155,11 @@ class ClockSampler:
                 "samples": len(rows)}
 
 
+
+
 def measured_peaks():
+    """(HBM GB/s, kind): the measured burst copy bandwidth of the GB300s
+    (a kernel timed alone), else the fallback figure."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as fh:
@@ -140,30 +171,24 @@ def measured_peaks():
 
 def gemv_source_hash():
     h = hashlib.sha256()
-    for f in ("gemv.cuh", "gemv.cu", "common.cuh"):
+    for f in ("gemv.cuh", "gemv.cu", "common.cuh", "attn.cu"):
         with open(os.path.join(ROOT, "mtp_speculative_draft_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kernel_tag):
-    """DRAM bytes per launch from the committed ncu summary, if it matches this source."""
-    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+def profiled_traffic(key):
+    """DRAM bytes per launch from profiles/traffic.json (ncu dram__bytes_read +
+    write of one capture), or None when absent or taken on other sources."""
     try:
-        lines = open(path).read().splitlines()
-    except OSError:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as fh:
+            d = json.load(fh)
+        e = d[key]
+    except (OSError, KeyError, ValueError):
         return None
-    vals = {}
-    for ln in lines:
-        if ":" in ln and ln.strip().startswith("- "):
-            k, v = ln.strip()[2:].split(":", 1)
-            vals[k.strip()] = v.strip().strip("`")
-    if vals.get("source_hash") != gemv_source_hash():
+    if e.get("source_hash") != gemv_source_hash():
         return None
-    try:
-        return float(vals["dram_bytes_per_launch"])
-    except (KeyError, ValueError):
-        return None
+    return float(e["dram_bytes_per_launch"])
 
 
 # --------------------------------------------------------------- CPU oracle
@@ -235,18 +260,6 @@ def oracle_sampled_step(cfg, host, frac, rng):
 
 
 # --------------------------------------------------------------- main arms
-def dist_setup(args):
-    import torch
-    rank = int(os.environ.get("RANK", 0))
-    world = int(os.environ.get("WORLD_SIZE", 1))
-    local = int(os.environ.get("LOCAL_RANK", 0))
-    if world > 1:
-        import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-    return rank, world, local
-
-
 def barrier_max(world, value, device="cuda"):
     """The largest `value` over all ranks (an all-reduce; every rank returns it)."""
     if world == 1:
@@ -274,6 +287,10 @@ def run_reference(args):
     from mtp_synth.configs import CONFIGS, make_layer_weights, make_shared, make_state, make_step
     rank = int(os.environ.get("RANK", 0))
     if rank != 0:
+        return
+    if args.config == "qmatmul_sweep":
+        print(json.dumps({"impl": "reference", "unavailable": "the oracle arm times the draft-layer "
+                          "workloads; the sweep has no step of its own"}))
         return
     cfg = CONFIGS[args.config]
     step = make_step(cfg)
@@ -307,48 +324,101 @@ def run_reference(args):
     print(json.dumps(out))
 
 
-def run_ours(args):
-    import numpy as np
+
+# --------------------------------------------------------------- device helpers
+def _dev():
     import torch
     from mtp_speculative_draft_gb300 import build as B
     B.build()
-    from mtp_speculative_draft_gb300 import _lib as L
-    from mtp_speculative_draft_gb300.layer import DraftLayer, SharedHead
-    from mtp_synth.configs import CONFIGS, make_layer_weights, make_shared, make_state, make_step
-
-    rank, world, local = dist_setup(args)
+    rank, world, local = dist_setup_env()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    cfg = CONFIGS[args.config]
-    step = make_step(cfg)
-    w = make_layer_weights(cfg)
-    shared = make_shared(cfg)
-    st = make_state(cfg)
-    lyr = DraftLayer(cfg, w, SharedHead(shared, dev), st, device=dev)
-    H, m = cfg.hidden, cfg.m
-    hidden = torch.from_numpy(step["hidden"]).to(dev)
-    tokens = torch.from_numpy(step["tokens"]).to(dev)
-    tok = torch.zeros(1, dtype=torch.int32, device=dev)
-    val = torch.zeros(1, dtype=torch.float32, device=dev)
-    hid = torch.zeros(H, dtype=torch.float32, device=dev)
-    stream = torch.cuda.Stream(device=dev)
+    return rank, world, local, dev
 
-    def fwd():
-        lyr.forward(hidden, cfg.cache_len, tokens=tokens, token=tok, value=val, hidden_out=hid,
-                    stream=stream)
 
+def dist_setup_env():
+    import torch
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local = int(os.environ.get("LOCAL_RANK", 0))
+    if world > 1 and not __import__("torch.distributed", fromlist=["x"]).is_initialized():
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    return rank, world, local
+
+
+class L2Flush:
+    """Writes a buffer of twice the L2 size (between timed steps, untimed)."""
+
+    def __init__(self, dev):
+        import torch
+        l2 = torch.cuda.get_device_properties(dev).L2_cache_size or (128 << 20)
+        self.buf = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+
+    def __call__(self):
+        self.buf.zero_()
+
+
+def timed_launches(run_step, n_marks, steps, flush=None):
+    """Each launch of ``run_step`` alone: a timing session per step records an
+    event before every library launch and after the last; returns the mean
+    duration of each launch (ms) over ``steps`` steps and the launch count."""
+    import torch
+    from mtp_speculative_draft_gb300.api import launch_timing
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n_marks + 4)]
+    for e in evs:            # create the events (torch makes them on first record)
+        e.record()
+    torch.cuda.synchronize()
+    sums, n_launch = None, None
+    for _ in range(steps):
+        if flush:
+            flush()
+        with launch_timing(evs) as t:
+            run_step()
+        d = t.durations_ms()
+        n_launch = len(d)
+        sums = d if sums is None else [a + b for a, b in zip(sums, d)]
+    return [v / steps for v in sums], n_launch
+
+
+def roofline_of(plan, launch_ms, peak, peak_kind, traffic_key=None, traffic_scale=1):
+    """Per-launch bandwidth and the dominant launch's roofline object."""
+    rows = []
+    for (name, nbytes), ms in zip(plan, launch_ms):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rows.append({"launch": name, "ms": ms, "algorithmic_bytes": nbytes, "gbs": gbs,
+                     "frac": gbs / peak})
+    dom = max(range(len(plan)), key=lambda i: plan[i][1])
+    traffic = profiled_traffic(traffic_key) if traffic_key else None
+    r = rows[dom]
+    roof = {"bound": "hbm", "kernel": r["launch"], "achieved": r["gbs"], "peak": peak,
+            "unit": "GB/s", "frac": r["frac"], "traffic": traffic,
+            "peak_kind": f"{peak_kind} burst copy bandwidth (kernel timed alone)",
+            "algorithmic_bytes_per_launch": r["algorithmic_bytes"], "launch_ms": r["ms"]}
+    return roof, rows
+
+
+def graph_of(fn, stream):
+    import torch
     with torch.cuda.stream(stream):
         for _ in range(3):
-            fwd()
+            fn()
         stream.synchronize()
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph, stream=stream):
-            fwd()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
     stream.synchronize()
+    return g
 
-    # ---------------- timed region: graph replays, inputs resident in HBM
-    with torch.cuda.stream(stream):   # replay() launches on the current stream
-        for _ in range(args.warmup):
+
+def time_replays(graph, stream, steps, warmup, world, flush=None):
+    """Device time of ``steps`` graph replays (ms total, max over ranks), with a
+    barrier and synchronize on both sides; with ``flush``, each replay is timed
+    alone between its own events and the L2 is flushed between replays."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
             graph.replay()
     stream.synchronize()
     clocks = ClockSampler()
@@ -357,71 +427,103 @@ def run_ours(args):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
-    ev0 = torch.cuda.Event(enable_timing=True)
-    ev1 = torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for _ in range(args.steps):
-            graph.replay()
-        ev1.record(stream)
-    ev1.synchronize()
+        if flush is None:
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                graph.replay()
+            e1.record(stream)
+            e1.synchronize()
+            total = e0.elapsed_time(e1)
+        else:
+            pairs = []
+            for _ in range(steps):
+                flush()
+                a = torch.cuda.Event(enable_timing=True)
+                b = torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                graph.replay()
+                b.record(stream)
+                pairs.append((a, b))
+            pairs[-1][1].synchronize()
+            total = sum(a.elapsed_time(b) for a, b in pairs)
     torch.cuda.synchronize()
     clocks.stop()
-    ms_total = barrier_max(world, ev0.elapsed_time(ev1))
-    ms = ms_total / args.steps
-    value = job_value(world, args.steps, ms_total)
+    return barrier_max(world, total), clocks
 
-    # ---------------- per-kernel breakdown (events between launches, same steps)
-    # The dominant kernel is the lm_head GEMV; time it alone in the same stream
-    # with the same inputs (normalised hidden already packed by the step).
+
+# --------------------------------------------------------------- layer workloads
+def run_layer_bench(args, cfg):
+    import torch
     from mtp_speculative_draft_gb300 import api as A
-    y_dev = hid.clone()
-    logits = None
-    lm_ws = A.workspace(L.load().lmhead_argmax_workspace_bytes(H, cfg.vocab))
-    lm_desc = lyr.shared.lm_head.desc
-    with torch.cuda.stream(stream):
-        for _ in range(5):
-            A.lmhead_argmax(y_dev, None, cfg.eps, lm_desc, tok, val, logits, None, lm_ws, stream)
-        e_norm0 = torch.cuda.Event(enable_timing=True)
-        e_norm1 = torch.cuda.Event(enable_timing=True)
-        # norm-only cost (same launch with no weights streamed is not available):
-        # time lm_head (norm + GEMV) and a norm-only rmsnorm of the same row.
-        ta = torch.cuda.Event(enable_timing=True)
-        tb = torch.cuda.Event(enable_timing=True)
-        ta.record(stream)
-        for _ in range(args.steps):
-            A.lmhead_argmax(y_dev, None, cfg.eps, lm_desc, tok, val, logits, None, lm_ws, stream)
-        tb.record(stream)
-        e_norm0.record(stream)
-        nw = torch.ones(H, device=dev)
-        tmp = torch.empty(H, device=dev)
-        for _ in range(args.steps):
-            A.rmsnorm_residual(y_dev, None, nw, tmp, None, 1, H, cfg.eps, stream)
-        e_norm1.record(stream)
-    stream.synchronize()
-    head_ms = (ta.elapsed_time(tb) - e_norm0.elapsed_time(e_norm1)) / args.steps
-    bytes_map = layer_bytes(cfg)
-    head_bytes = bytes_map["lm_head"]
-    peak, peak_kind = measured_peaks()
-    achieved = head_bytes / (head_ms * 1e-3) / 1e9
-    traffic = profiled_traffic("gemv_lm_head_qwen_dense")
-    total_bytes = sum(bytes_map.values())
+    from mtp_speculative_draft_gb300.layer import DraftChain, DraftLayer, SharedHead
+    from mtp_synth.configs import make_layer_weights, make_shared, make_state, make_step
 
-    # ---------------- end to end through the C ABI with host buffers
+    rank, world, local, dev = _dev()
+    nl, m, H = max(1, cfg.n_layers), cfg.m, cfg.hidden
+    step = make_step(cfg)
+    shared = make_shared(cfg)
+    sh = SharedHead(shared, dev)
+    ws_l = [make_layer_weights(cfg, k) for k in range(nl)]
+    sts = [make_state(cfg, k) for k in range(nl)]
+    layers = [DraftLayer(cfg, ws_l[k], sh, sts[k], device=dev) for k in range(nl)]
+    hidden = torch.from_numpy(step["hidden"]).to(dev)
+    tokens = torch.from_numpy(step["tokens"]).to(dev)
+    tok = torch.zeros(1, dtype=torch.int32, device=dev)
+    val = torch.zeros(nl, dtype=torch.float32, device=dev)
+    hid = torch.zeros((nl, H), dtype=torch.float32, device=dev)
+    seq = torch.zeros(m + nl, dtype=torch.int32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    if nl > 1:
+        chain = DraftChain(layers)
+
+        def fwd():
+            seq[:m].copy_(tokens)   # the known tokens; the chain appends its drafts
+            chain.forward(hidden, seq, [cfg.cache_len] * nl, val, hid, stream=stream)
+    else:
+        lyr = layers[0]
+
+        def fwd():
+            lyr.forward(hidden, cfg.cache_len, tokens=tokens, token=tok, value=val, hidden_out=hid,
+                        stream=stream)
+
+    flush = L2Flush(dev) if cfg.moe else None   # the MoE step reads less than it could cache
+    graph = graph_of(fwd, stream)
+    ms_total, clocks = time_replays(graph, stream, args.steps, args.warmup, world, flush)
+    ms = ms_total / args.steps
+    value = nl * job_value(world, args.steps, ms_total)   # draft tokens (one per layer step)
+
+    # each launch alone (eager, same inputs)
+    plan = launch_plan(cfg) * nl
+    with torch.cuda.stream(stream):
+        launch_ms, n_launch = timed_launches(fwd, len(plan) + 1, max(5, min(args.steps, 50)), flush)
+    stream.synchronize()
+    if n_launch != len(plan):
+        raise RuntimeError(f"expected {len(plan)} launches per step, the library made {n_launch}")
+    peak, peak_kind = measured_peaks()
+    if nl > 1:  # average the chain's layers launch by launch
+        per = len(plan) // nl
+        launch_ms = [sum(launch_ms[i + k * per] for k in range(nl)) / nl for i in range(per)]
+        plan = plan[:per]
+    roof, rows = roofline_of(plan, launch_ms, peak, peak_kind, traffic_key=f"{cfg.name}.dominant")
+    total_bytes = step_bytes(cfg)
+
+    # end to end through the C ABI with pinned host buffers
     h_hidden = torch.from_numpy(step["hidden"]).pin_memory()
     h_tokens = torch.from_numpy(step["tokens"]).pin_memory()
-    h_out_tok = torch.zeros(1, dtype=torch.int32).pin_memory()
-    h_out_val = torch.zeros(1, dtype=torch.float32).pin_memory()
+    h_out_tok = torch.zeros(m + nl if nl > 1 else 1, dtype=torch.int32).pin_memory()
+    h_out_val = torch.zeros(nl, dtype=torch.float32).pin_memory()
     e2e_steps = max(10, args.steps // 2)
     with torch.cuda.stream(stream):
         def e2e_step():
             hidden.copy_(h_hidden, non_blocking=True)
             tokens.copy_(h_tokens, non_blocking=True)
             fwd()
-            h_out_tok.copy_(tok, non_blocking=True)
+            h_out_tok.copy_(seq if nl > 1 else tok, non_blocking=True)
             h_out_val.copy_(val, non_blocking=True)
             stream.synchronize()
-            return int(h_out_tok[0])
         for _ in range(3):
             e2e_step()
         t0 = time.perf_counter()
@@ -429,42 +531,129 @@ def run_ours(args):
             e2e_step()
         t1 = time.perf_counter()
     e2e_s = barrier_max(world, t1 - t0)
-    e2e_val = job_value(world, e2e_steps, 1000.0 * e2e_s)
+    e2e_val = nl * job_value(world, e2e_steps, 1000.0 * e2e_s)
     h2d = h_hidden.numel() * 4 + h_tokens.numel() * 4
-    d2h = 8
+    d2h = h_out_tok.numel() * 4 + h_out_val.numel() * 4
+    status = A.mtp_workspace_status(layers[0].ws)
 
-    # ---------------- check the result once against itself (token = argmax)
-    status = A.mtp_workspace_status(lyr.ws)
-
+    l2 = ("flushed between timed steps (a 2x L2 write, untimed)" if flush is not None else
+          ("inputs larger than L2" if total_bytes > (256 << 20) else
+           f"L2-resident ({total_bytes / 1e6:.1f} MB per step): latency-bound, roofline not meaningful"))
     out = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int4-affine weights, f32 activations, bf16x2-split tensor-core products, f32 accumulate",
+        "vs_baseline": None, "dtype": DTYPE,
         "data": "synthetic (seeded SplitMix64; value distributions of the workload)",
-        "config": {"workload": cfg.name, "m": m, "hidden": H, "n_heads": cfg.n_heads,
-                   "n_kv_heads": cfg.n_kv_heads, "head_dim": cfg.head_dim_qk,
-                   "intermediate": cfg.intermediate, "vocab": cfg.vocab,
-                   "cache_len": cfg.cache_len, "gated_q": cfg.gated_q,
-                   "weights": "affine 4-bit g32", "l2": "inputs larger than L2 (0.92 GB of weights per step)",
-                   "timing": "CUDA graph of one draft step, replayed; CUDA events on the launch stream",
+        "config": {"workload": cfg.name, "m": m, "layers": nl, "hidden": H, "n_heads": cfg.n_heads,
+                   "n_kv_heads": cfg.n_kv_heads, "head_dim_qk": cfg.head_dim_qk,
+                   "head_dim_v": cfg.head_dim_v, "intermediate": cfg.intermediate,
+                   "vocab": cfg.vocab, "cache_len": cfg.cache_len, "window": cfg.window,
+                   "gated_q": cfg.gated_q, "experts": cfg.n_experts, "top_k": cfg.top_k,
+                   "weights": "affine 4-bit g32", "l2": l2,
+                   "timing": ("CUDA graph of one step, replayed; CUDA events on the launch "
+                              "stream" + ("; each step between its own events" if flush else "")),
                    "parallelism": "replicas" if world > 1 else "single GPU"},
+        "us_per_draft_token": 1000.0 * ms / nl,
         "algorithmic_bytes_per_step": total_bytes,
         "hbm_gbs_step": total_bytes / (ms * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "kernel": "gemv_row_kernel: lm_head projection + argmax, timed alone",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_kind": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": head_bytes, "launch_ms": head_ms},
+        "step_frac_of_peak": total_bytes / (ms * 1e-3) / 1e9 / peak,
+        "roofline": roof,
+        "launches": rows,
         "e2e": {"value": e2e_val, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_step(cfg) * args.steps,
+        "gpu_launches": len(plan) * nl * args.steps,
         "clocks": clocks.summary(local),
         "device_error_word": status,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_oracle_full_step(cfg, (w, shared, st, step))
+    if (rank == 0 and world == 1 and not args.no_cpu_baseline and cfg.name == WORKLOAD):
+        out["cpu_baseline"] = cpu_oracle_full_step(cfg, (ws_l[0], shared, sts[0], step))
     if rank == 0:
         print(json.dumps(out))
     if world > 1:
         torch.distributed.destroy_process_group()
+
+
+# --------------------------------------------------------------- qmatmul sweep
+def run_sweep(args, sc):
+    import torch
+    import mtp_synth
+    from mtp_speculative_draft_gb300 import api as A
+    from mtp_speculative_draft_gb300 import _lib as L
+    from mtp_speculative_draft_gb300.layer import DeviceAffine
+
+    rank, world, local, dev = _dev()
+    peak, peak_kind = measured_peaks()
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size or (128 << 20)
+    stream = torch.cuda.Stream(device=dev)
+    results = []
+    clock_all = []
+    for (n, k) in sc.shapes:
+        w = mtp_synth.affine4_weight(sc.seed, f"sweep.{n}x{k}", n, k)
+        wbytes = aff(n, k)
+        copies = max(1, -(-2 * l2 // wbytes))      # rotate copies so the L2 never serves weights
+        devw = [DeviceAffine(w, dev)]
+        for _ in range(copies - 1):
+            d0 = devw[0]
+            c = DeviceAffine.__new__(DeviceAffine)
+            c.q, c.s, c.b = d0.q.clone(), d0.s.clone(), d0.b.clone()
+            c.desc = A.affine4(c.q, c.s, c.b)
+            devw.append(c)
+        del w
+        xall = torch.from_numpy(mtp_synth.normal_f32(sc.seed, f"sweep.x.{k}", (16, k))).to(dev)
+        for m in sc.ms:
+            x = xall[:m].contiguous()
+            y = torch.zeros((m, n), dtype=torch.float32, device=dev)
+            ws = A.workspace(L.load().qmatmul_affine4_workspace_bytes(m, k))
+
+            def calls():
+                for c in devw:
+                    A.qmatmul_affine4(x, c.desc, y, m, ws, stream)
+            g = graph_of(calls, stream)
+            reps = max(3, args.steps // (4 * copies))
+            total, clocks = time_replays(g, stream, reps, max(3, args.warmup // 4), world)
+            clock_all.append(clocks.summary(local))
+            call_ms = total / (reps * copies)
+            with torch.cuda.stream(stream):
+                lms, nl_ = timed_launches(calls, 2 * copies + 1, max(3, reps // 2))
+            stream.synchronize()
+            gemv = [lms[2 * i + 1] for i in range(copies)]   # launch 0 packs x, launch 1 is the GEMV
+            gemv_ms = sum(gemv) / len(gemv)
+            nbytes = wbytes + 4 * m * (k + n)
+            gbs = nbytes / (gemv_ms * 1e-3) / 1e9
+            results.append({"n": n, "k": k, "m": m, "call_ms": call_ms, "gemv_ms": gemv_ms,
+                            "algorithmic_bytes": nbytes, "gbs": gbs, "frac": gbs / peak,
+                            "weight_copies": copies})
+        del devw
+        torch.cuda.empty_cache()
+    big = [r for r in results if r["n"] * r["k"] > 5120 * 5120]
+    mean_gbs = statistics.mean(r["gbs"] for r in results)
+    worst = min(results, key=lambda r: r["frac"])
+    sms = [c["sm_mhz"] for c in clock_all if c["sm_mhz"]]
+    out = {"metric": "qmatmul_affine4 HBM GB/s per (N x K, m)", "value": mean_gbs, "unit": "GB/s",
+           "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "data": "synthetic (seeded SplitMix64)",
+           "config": {"workload": sc.name, "ms": list(sc.ms), "shapes": [list(s) for s in sc.shapes],
+                      "l2": "weights rotated over copies totalling at least 2x L2",
+                      "timing": "CUDA graph of the calls on every copy; the GEMV launch alone "
+                                "from events between the library's launches"},
+           "roofline": {"bound": "hbm", "kernel": "qmatmul_affine4 GEMV (worst case)",
+                        "achieved": worst["gbs"], "peak": peak, "unit": "GB/s",
+                        "frac": worst["frac"], "traffic": None, "peak_kind": peak_kind},
+           "min_frac_large_shapes": min(r["frac"] for r in big) if big else None,
+           "sweep": results,
+           "clocks": {"sm_mhz": statistics.median(sms) if sms else None,
+                      "sm_max_mhz": max((c["sm_max_mhz"] or 0) for c in clock_all) or None,
+                      "reasons": sorted({x for c in clock_all for x in c["reasons"]})}}
+    if rank == 0:
+        print(json.dumps(out))
+
+
+def run_ours(args):
+    from mtp_synth.configs import CONFIGS
+    cfg = CONFIGS[args.config]
+    if args.config == "qmatmul_sweep":
+        run_sweep(args, cfg)
+    else:
+        run_layer_bench(args, cfg)
 
 
 def run_profile_kernel(args):
@@ -516,6 +705,22 @@ def run_profile_kernel(args):
             ws = None
             run = lambda: A.qmatmul_affine4(x, w.desc, y, 1, ws)  # noqa: E731
             ws = A.qmatmul_affine4(x, w.desc, y, 1)
+    elif args.profile_kernel == "step":
+        # one whole draft step, embedding rows passed directly (no 3 GB table
+        # on the device), for launch lists and captures of the step's launches
+        from mtp_speculative_draft_gb300.layer import DraftLayer, SharedHead
+        from mtp_synth.configs import make_layer_weights, make_shared, make_state, make_step
+        step = make_step(cfg)
+        shared = make_shared(cfg, embed_rows=step["tokens"])
+        lyr = DraftLayer(cfg, make_layer_weights(cfg), SharedHead(shared, dev), make_state(cfg),
+                         device=dev)
+        hidden = torch.from_numpy(step["hidden"]).to(dev)
+        rows = torch.from_numpy(shared["embed_rows"]).to(dev)
+        tok = torch.zeros(1, dtype=torch.int32, device=dev)
+        val = torch.zeros(1, dtype=torch.float32, device=dev)
+        run = lambda: lyr.forward(hidden, cfg.cache_len, embed_rows=rows, token=tok,  # noqa: E731
+                                  value=val)
+        extra["algorithmic_bytes_per_call"] = step_bytes(cfg)
     else:
         from mtp_synth.configs import make_state
         g = A.attn_geom(cfg.n_heads, cfg.n_kv_heads, cfg.head_dim_qk, cfg.head_dim_v, cfg.rot_dim,

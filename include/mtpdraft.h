@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define MTPDRAFT_VERSION 1
+#define MTPDRAFT_VERSION 2
 
 typedef enum {
     MTP_OK = 0,
@@ -84,11 +84,37 @@ mtp_status mtp_workspace_init(void *d_ws, size_t bytes, void *stream);
  * copy); the first error since mtp_workspace_init is kept:
  *   0 none; 1 a wait for a TMA copy gave up; 2 a token id outside
  *   [0, vocab) (row 0 was used); 3 a wait inside a multi-projection launch
- *   for the previous projection's output gave up.
- * After code 1 or 3 a launch stopped part-way and may have left completion
- * counters set: clear the workspace with mtp_workspace_init() before its
- * next use.  Code 2 leaves the workspace usable. */
+ *   for the previous projection's output gave up; 4 a wait of the attention
+ *   splits of a KV head for each other's partials gave up.
+ * After code 1, 3 or 4 a launch stopped part-way (its outputs are not
+ * valid) and may have left completion counters set: clear the workspace
+ * with mtp_workspace_init() before its next use.  Code 2 leaves the
+ * workspace usable.  The waits behind codes 3 and 4 need every CTA of the
+ * launch resident at once (the launches size their grids for that); a
+ * device shared with other work at the same time can make them give up, so
+ * check the status after steps whose results matter. */
 mtp_status mtp_workspace_status(const void *d_ws, int32_t *h_code, void *stream);
+
+/* Diagnostic hook: the cross-CTA waits of later launches on this workspace
+ * (codes 3 and 4 above) give up after `polls` polls (0 restores the compiled
+ * limit of about two seconds).  With a limit of one poll, waits that are not
+ * already satisfied give up at once, which exercises the error path on a
+ * healthy device.  Enqueued on `stream`; mtp_workspace_init() also resets
+ * it to 0. */
+mtp_status mtp_workspace_set_wait_limit(void *d_ws, int32_t polls, void *stream);
+
+/* Diagnostics (per calling thread): between mtp_timing_begin and
+ * mtp_timing_end every kernel launch the library enqueues from this thread
+ * is preceded by a record of the next of `events` (cudaEvent_t handles the
+ * caller created) on the launch's stream; mtp_timing_end records one more
+ * event after the last launch and stores how many marks were made (launches
+ * + 1).  The interval between events i and i + 1 is launch i alone: a record
+ * between two launches removes their programmatic overlap.  Sessions do not
+ * nest; more launches than events are counted but not recorded
+ * (mtp_timing_end then returns MTP_ERR_INVALID_ARG).  Not for use inside
+ * stream capture. */
+mtp_status mtp_timing_begin(void *const *events, int32_t n_events);
+mtp_status mtp_timing_end(int32_t *n_recorded);
 
 /* ------------------------------------------------------------------------
  * qmatmul_affine4: y[r][n] = sum_k x[r][k] * (s[n][k/32]*code[n][k] + b[n][k/32])
@@ -321,11 +347,14 @@ mtp_status mtp_draft_forward(const mtp_layer_desc *L, const mtp_step_in *in,
  * next layer's embedding gather on the device, with no host round trip.
  * All layers need an embedding table.  d_values [n_layers] receives the
  * drafts' logits; d_hidden_out [n_layers][hidden] (or NULL) each layer's
- * normed last row.  cache_lens[k] is layer k's cache length (host array). */
+ * normed last row; d_u2 [n_layers][m][hidden] (or NULL) each layer's output
+ * rows before the final norm; d_logits [n_layers][vocab] (or NULL) each
+ * layer's last-row logits (layers must then share the vocabulary size).
+ * cache_lens[k] is layer k's cache length (host array). */
 mtp_status mtp_draft_chain(const mtp_layer_desc *layers, int32_t n_layers,
                            const float *d_hidden, int32_t *d_seq, const int32_t *cache_lens,
-                           int32_t m, float *d_values, float *d_hidden_out, void *d_ws,
-                           size_t ws_bytes, void *stream);
+                           int32_t m, float *d_values, float *d_hidden_out, float *d_u2,
+                           float *d_logits, void *d_ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
  * Speculation bookkeeping of one sequence (host only: no device work, no

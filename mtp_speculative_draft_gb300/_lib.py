@@ -80,6 +80,9 @@ EXPORTS = {
     "mtp_version": (C.c_int, []),
     "mtp_workspace_init": (C.c_int, [vp, sz, vp]),
     "mtp_workspace_status": (C.c_int, [vp, C.POINTER(i32), vp]),
+    "mtp_workspace_set_wait_limit": (C.c_int, [vp, i32, vp]),
+    "mtp_timing_begin": (C.c_int, [C.POINTER(vp), i32]),
+    "mtp_timing_end": (C.c_int, [C.POINTER(i32)]),
     "qmatmul_affine4_workspace_bytes": (sz, [i32, i32]),
     "qmatmul_affine4": (C.c_int, [vp, C.POINTER(Affine4), vp, i32, vp, sz, vp]),
     "rmsnorm_residual": (C.c_int, [vp, vp, vp, vp, vp, i32, i32, f32, vp]),
@@ -104,7 +107,7 @@ EXPORTS = {
     "mtp_draft_forward": (C.c_int, [C.POINTER(LayerDesc), C.POINTER(StepIn), C.POINTER(StepOut),
                                     vp, sz, vp]),
     "mtp_draft_chain": (C.c_int, [C.POINTER(LayerDesc), i32, vp, vp, C.POINTER(i32), i32, vp, vp,
-                                  vp, sz, vp]),
+                                  vp, vp, vp, sz, vp]),
 }
 
 

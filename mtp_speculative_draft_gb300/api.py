@@ -66,6 +66,38 @@ def mtp_workspace_status(ws: torch.Tensor, stream=None) -> int:
     return code.value
 
 
+class launch_timing:
+    """Context manager around mtp_timing_begin / mtp_timing_end: ``events`` are
+    torch.cuda.Event(enable_timing=True) objects; after the block,
+    ``durations_ms()`` gives each launch's time (events i -> i + 1)."""
+
+    def __init__(self, events):
+        self.events = events
+        self._handles = (C.c_void_p * len(events))(*[e.cuda_event for e in events])
+        self.n = 0
+
+    def __enter__(self):
+        check(L.load().mtp_timing_begin(self._handles, len(self.events)), "mtp_timing_begin")
+        return self
+
+    def __exit__(self, *exc):
+        n = C.c_int32(0)
+        st = L.load().mtp_timing_end(C.byref(n))
+        self.n = n.value
+        if exc[0] is None:
+            check(st, "mtp_timing_end")
+        return False
+
+    def durations_ms(self):
+        self.events[self.n - 1].synchronize()
+        return [self.events[i].elapsed_time(self.events[i + 1]) for i in range(self.n - 1)]
+
+
+def mtp_workspace_set_wait_limit(ws: torch.Tensor, polls: int, stream=None):
+    check(L.load().mtp_workspace_set_wait_limit(_p(ws), int(polls), _stream(stream)),
+          "mtp_workspace_set_wait_limit")
+
+
 def mtp_rope_table(table: torch.Tensor, max_pos: int, rot_dim: int, theta: float, stream=None):
     check(L.load().mtp_rope_table(_p(table), max_pos, rot_dim, float(theta), _stream(stream)),
           "mtp_rope_table")
@@ -143,11 +175,13 @@ def mtp_draft_forward(desc, step_in, step_out, ws, stream=None):
                                      ws.numel(), _stream(stream)), "mtp_draft_forward")
 
 
-def mtp_draft_chain(descs, hidden, seq, cache_lens, m, values, hidden_out, ws, stream=None):
+def mtp_draft_chain(descs, hidden, seq, cache_lens, m, values, hidden_out, ws, stream=None,
+                    u2=None, logits=None):
     arr = (L.LayerDesc * len(descs))(*descs)
     lens = (C.c_int32 * len(descs))(*cache_lens)
     check(L.load().mtp_draft_chain(arr, len(descs), _p(hidden), _p(seq), lens, m, _p(values),
-                                   _p(hidden_out), _p(ws), ws.numel(), _stream(stream)),
+                                   _p(hidden_out), _p(u2), _p(logits), _p(ws), ws.numel(),
+                                   _stream(stream)),
           "mtp_draft_chain")
 
 

@@ -83,6 +83,27 @@ static mtp_status qmat_cached(QMat* out, const mtp_affine4& w, const char* name)
   return MTP_OK;
 }
 
+// Launch-timing session of this thread (mtp_timing_begin / mtp_timing_end).
+struct TimingSession {
+  void* const* events = nullptr;
+  int n_events = 0;
+  int recorded = 0;
+  cudaStream_t last = nullptr;
+  cudaError_t err = cudaSuccess;
+};
+static thread_local TimingSession g_timing;
+
+void launch_mark(cudaStream_t st) {
+  TimingSession& t = g_timing;
+  if (!t.events) return;
+  if (t.recorded < t.n_events) {
+    cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(t.events[t.recorded]), st);
+    if (e != cudaSuccess && t.err == cudaSuccess) t.err = e;
+  }
+  ++t.recorded;
+  t.last = st;
+}
+
 static size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
 // Bump allocator over a caller workspace.
@@ -156,6 +177,45 @@ mtp_status mtp_workspace_status(const void* d_ws, int32_t* h_code, void* stream)
   cudaError_t e = cudaMemcpyAsync(h_code, d_ws, sizeof(int32_t), cudaMemcpyDeviceToHost, st);
   if (e == cudaSuccess) e = cudaStreamSynchronize(st);
   if (e != cudaSuccess) return cuda_fail(e, "workspace status");
+  return MTP_OK;
+}
+
+mtp_status mtp_timing_begin(void* const* events, int32_t n_events) {
+  if (!events || n_events < 2) return fail(MTP_ERR_INVALID_ARG, "timing: need at least two events");
+  if (g_timing.events) return fail(MTP_ERR_INVALID_ARG, "timing: a session is already open on this thread");
+  g_timing = TimingSession{};
+  g_timing.events = events;
+  g_timing.n_events = n_events;
+  return MTP_OK;
+}
+
+mtp_status mtp_timing_end(int32_t* n_recorded) {
+  TimingSession t = g_timing;
+  g_timing = TimingSession{};
+  if (!t.events) return fail(MTP_ERR_INVALID_ARG, "timing: no session is open on this thread");
+  if (t.recorded > 0) {  // the closing event, after the last launch
+    if (t.recorded < t.n_events) {
+      cudaError_t e = cudaEventRecord(static_cast<cudaEvent_t>(t.events[t.recorded]), t.last);
+      if (e != cudaSuccess && t.err == cudaSuccess) t.err = e;
+    }
+    ++t.recorded;
+  }
+  if (n_recorded) *n_recorded = t.recorded;
+  if (t.err != cudaSuccess) return cuda_fail(t.err, "timing: event record");
+  if (t.recorded > t.n_events)
+    return fail(MTP_ERR_INVALID_ARG, "timing: more launches than events (" +
+                                         std::to_string(t.recorded) + " marks)");
+  return MTP_OK;
+}
+
+mtp_status mtp_workspace_set_wait_limit(void* d_ws, int32_t polls, void* stream) {
+  if (!d_ws) return fail(MTP_ERR_INVALID_ARG, "null workspace");
+  if (polls < 0) return fail(MTP_ERR_INVALID_ARG, "polls must be >= 0");
+  // pageable source: the copy has read `polls` when the call returns
+  const int32_t v = polls;
+  cudaError_t e = cudaMemcpyAsync(&header(d_ws)->wait_limit, &v, sizeof(v), cudaMemcpyHostToDevice,
+                                  static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "workspace wait limit");
   return MTP_OK;
 }
 
@@ -1021,8 +1081,8 @@ mtp_status mtp_draft_forward(const mtp_layer_desc* L, const mtp_step_in* in,
 
 mtp_status mtp_draft_chain(const mtp_layer_desc* layers, int32_t n_layers, const float* d_hidden,
                            int32_t* d_seq, const int32_t* cache_lens, int32_t m,
-                           float* d_values, float* d_hidden_out, void* d_ws, size_t ws_bytes,
-                           void* stream) {
+                           float* d_values, float* d_hidden_out, float* d_u2, float* d_logits,
+                           void* d_ws, size_t ws_bytes, void* stream) {
   if (!layers || n_layers <= 0 || !d_hidden || !d_seq || !cache_lens || !d_values)
     return fail(MTP_ERR_INVALID_ARG, "mtp_draft_chain: null argument");
   size_t need = 0;
@@ -1032,10 +1092,15 @@ mtp_status mtp_draft_chain(const mtp_layer_desc* layers, int32_t n_layers, const
     if (!layers[k].embed) return fail(MTP_ERR_INVALID_ARG, "mtp_draft_chain: layers need an embedding table");
     if (layers[k].hidden != layers[0].hidden)
       return fail(MTP_ERR_INVALID_ARG, "mtp_draft_chain: layers must share the hidden size");
+    if (d_logits && layers[k].vocab != layers[0].vocab)
+      return fail(MTP_ERR_INVALID_ARG, "mtp_draft_chain: per-layer logits need one vocabulary size");
     if (cache_lens[k] < 0 || cache_lens[k] + m > layers[k].cache_cap)
       return fail(MTP_ERR_CAPACITY, "mtp_draft_chain: cache_len + m exceeds a cache capacity");
     need = std::max(need, mtp_draft_workspace_bytes(&layers[k], m));
   }
+  if ((d_hidden_out && !aligned16(d_hidden_out)) || (d_u2 && !aligned16(d_u2)) ||
+      (d_logits && !aligned16(d_logits)))
+    return fail(MTP_ERR_INVALID_ARG, "mtp_draft_chain: outputs must be 16-byte aligned");
   if (!d_ws || ws_bytes < need) return fail(MTP_ERR_WORKSPACE, "mtp_draft_chain: workspace too small");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   for (int k = 0; k < n_layers; ++k) {
@@ -1048,6 +1113,8 @@ mtp_status mtp_draft_chain(const mtp_layer_desc* layers, int32_t n_layers, const
     out.d_token = d_seq + m + k;
     out.d_value = d_values + k;
     out.d_hidden_out = d_hidden_out ? d_hidden_out + (size_t)k * layers[k].hidden : nullptr;
+    out.d_u2 = d_u2 ? d_u2 + (size_t)k * m * layers[k].hidden : nullptr;
+    out.d_logits = d_logits ? d_logits + (size_t)k * layers[k].vocab : nullptr;
     mtp_status s = enqueue_layer(&layers[k], &in, &out, d_ws, st);
     if (s != MTP_OK) return s;
   }

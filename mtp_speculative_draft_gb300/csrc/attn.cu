@@ -129,8 +129,9 @@ __device__ __forceinline__ void warp_norm_rope(float* v, const float* src, int d
 }
 
 // Waits (one thread, bounded) until *cnt >= target; acquire.
-__device__ __forceinline__ bool wait_count_cta(const unsigned* cnt, unsigned target) {
-  for (unsigned i = 0; i < (4u << 20); ++i) {
+__device__ __forceinline__ bool wait_count_cta(const unsigned* cnt, unsigned target,
+                                               unsigned polls) {
+  for (unsigned i = 0; i < polls; ++i) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
     if (v >= target) return true;
@@ -482,8 +483,8 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   __syncthreads();
   if (tid == 0) {
     atomicAdd(&a.counters[kvh], 1u);
-    arrived = wait_count_cta(&a.counters[kvh], (unsigned)ns);
-    if (!arrived) set_dev_error(a.err, kErrMbarTimeout);
+    arrived = wait_count_cta(&a.counters[kvh], (unsigned)ns, wait_polls(a.err, 4u << 20));
+    if (!arrived) set_dev_error(a.err, kErrSplitTimeout);
   }
   __syncthreads();
   if (!arrived) return;
@@ -673,6 +674,7 @@ static cudaError_t launch_attn_t(const AttnParams& a, size_t smem, cudaStream_t 
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
+  launch_mark(cfg.stream);
   return cudaLaunchKernelEx(&cfg, attn_decode_kernel<QM, DV>, a);
 }
 

@@ -13,10 +13,13 @@ constexpr int kGroup = 32;               // affine quantisation group
 constexpr unsigned kWaitLimit = 2000;     // bounded device-side waits (polls of at most 1 ms)
 
 // Workspace header shared by every entry point that takes a workspace.
-// word 0: device error code; words 1..: completion counters.
+// word 0: device error code; word 1: poll limit of the cross-CTA waits (0:
+// the compiled default; set by mtp_workspace_set_wait_limit); then the
+// completion counters.
 struct WsHeader {
   int err;
-  int pad[31];
+  int wait_limit;
+  int pad[30];
   unsigned counters[224];
 };
 static_assert(sizeof(WsHeader) == 1024, "workspace header is 1 KB");
@@ -27,6 +30,7 @@ enum DevErr : int {
   kErrMbarTimeout = 1,   // a wait for a TMA copy gave up
   kErrBadToken = 2,      // a token id outside [0, vocab) (row 0 used instead)
   kErrPhaseTimeout = 3,  // a wait for the previous phase of a one-row launch gave up
+  kErrSplitTimeout = 4,  // a wait of the attention splits of a KV head for each other gave up
 };
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -169,6 +173,13 @@ __device__ __forceinline__ void red_add_release_gpu(unsigned* p, unsigned v) {
 
 __device__ __forceinline__ void set_dev_error(int* err, int code) {
   if (err) atomicCAS(err, 0, code);
+}
+
+// Poll limit of a cross-CTA wait: the workspace header's override (the word
+// after the error word) when it is positive, else `dflt`.
+__device__ __forceinline__ unsigned wait_polls(const int* err, unsigned dflt) {
+  const int v = err ? __ldcg(err + 1) : 0;
+  return v > 0 ? (unsigned)v : dflt;
 }
 
 }  // namespace mtp

@@ -164,6 +164,7 @@ static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
   cudaLaunchAttribute attr = pdl_attr();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
+  launch_mark(cfg.stream);
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
@@ -233,6 +234,7 @@ cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
   cudaLaunchAttribute attr = pdl_attr();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
+  launch_mark(cfg.stream);
   return cudaLaunchKernelEx(&cfg, kern, sp);
 }
 
@@ -268,6 +270,7 @@ cudaError_t launch_pack(const float* x, int m, int K, uint4* xp, float2* xs, cud
   cudaLaunchAttribute attr = pdl_attr();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
+  launch_mark(cfg.stream);
   return cudaLaunchKernelEx(&cfg, pack_x_kernel, x, m, K, xp, xs);
 }
 
@@ -282,6 +285,7 @@ cudaError_t launch_gemv_simple(const float* x, int m, int K, const mtp_affine4& 
   cudaLaunchAttribute attr = pdl_attr();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
+  launch_mark(cfg.stream);
   return cudaLaunchKernelEx(&cfg, gemv_simple_kernel, x, m, K, w.q, w.s, w.b, (int)w.n, y);
 }
 
@@ -348,6 +352,7 @@ cudaError_t launch_rows_argmax(float* logits, int rows, int V, float mult, float
   cudaLaunchAttribute attr = pdl_attr();
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
+  launch_mark(cfg.stream);
   return cudaLaunchKernelEx(&cfg, rows_argmax_kernel, logits, V, mult, cap, tok, val, keys, cnt);
 }
 

@@ -986,8 +986,8 @@ constexpr int kRowStageTx = kStageMatBytes + 8 * (128 + 8);
 // Every warp of a launch polls the same counter: sleeps of 512 ns keep the
 // polls from slowing the publishers' atomics on it (measured on the draft
 // step: 32 or 64 ns cost 6 us, 256 ns 1.4 us, 1024 ns 1.6 us over 512 ns).
-__device__ __forceinline__ bool wait_count(const unsigned* cnt, unsigned target) {
-  for (unsigned i = 0; i < kPhaseSpinLimit; ++i) {
+__device__ __forceinline__ bool wait_count(const unsigned* cnt, unsigned target, unsigned polls) {
+  for (unsigned i = 0; i < polls; ++i) {
     unsigned v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(cnt) : "memory");
     if (v >= target) return true;
@@ -1198,11 +1198,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       if (cc.ph > 0 || sp.pre.kind != kPreNone) {
         bool ok = true;
         if (lane == 0) {
+          const unsigned polls = wait_polls(sp.err, kPhaseSpinLimit);
           if (cc.ph > 0) {
             const GemvParams& pp = sp.ph[cc.ph - 1];
-            ok = wait_count(sp.phase_done + cc.ph - 1, (unsigned)pp.seg[pp.nseg - 1].tile_end);
+            ok = wait_count(sp.phase_done + cc.ph - 1, (unsigned)pp.seg[pp.nseg - 1].tile_end,
+                            polls);
           } else {
-            ok = wait_count(sp.phase_done + kMaxPhases, (unsigned)sp.pre.units);
+            ok = wait_count(sp.phase_done + kMaxPhases, (unsigned)sp.pre.units, polls);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;

@@ -17,6 +17,10 @@ mtp_status cuda_fail(cudaError_t e, const char* what);
 
 bool aligned16(const void* p);
 
+// Records the next event of this thread's launch-timing session (if one is
+// open) on `st`; every launcher calls it right before its kernel launch.
+void launch_mark(cudaStream_t st);
+
 // Number of SMs of the current device (cached per device).
 int sm_count();
 

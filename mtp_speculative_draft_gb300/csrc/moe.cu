@@ -161,6 +161,7 @@ cudaError_t launch_router(const RouterParams& r, cudaStream_t st) {
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
+  launch_mark(cfg.stream);
   return cudaLaunchKernelEx(&cfg, router_kernel, r);
 }
 

@@ -163,6 +163,7 @@ cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, fl
   attr.val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
+  launch_mark(cfg.stream);
   return cudaLaunchKernelEx(&cfg, norm_pack_kernel, a);
 }
 

@@ -122,7 +122,9 @@ class DraftChain:
         self.layers = layers
         self.ws = max((lyr.ws for lyr in layers), key=lambda t: t.numel())
 
-    def forward(self, hidden, seq, cache_lens, values, hidden_out=None, stream=None):
+    def forward(self, hidden, seq, cache_lens, values, hidden_out=None, stream=None, u2=None,
+                logits=None):
         from .api import mtp_draft_chain
         mtp_draft_chain([lyr.desc for lyr in self.layers], hidden, seq, cache_lens,
-                        int(hidden.shape[0]), values, hidden_out, self.ws, stream)
+                        int(hidden.shape[0]), values, hidden_out, self.ws, stream, u2=u2,
+                        logits=logits)

@@ -185,3 +185,24 @@ def test_noalloc_attention_rejects_before_touching_its_scratch(lib):
     big = _lib.AttnGeom(16, 1, 256, 256, 256, 0, 0, 1e-6, 0.0)
     assert lib.attn_decode_sink_workspace_bytes(C.byref(big), 1, 4096) > 2 << 20
     assert lib.attn_decode_sink_noalloc(C.byref(big), *full, 4096, 4104, 1, p, None) == 4
+
+
+def test_timing_session_host_rules(lib):
+    # sessions need two or more events, do not nest, and count marks; with no
+    # launch in between nothing is recorded (no CUDA call is made here)
+    evs = (C.c_void_p * 4)(0x10, 0x20, 0x30, 0x40)
+    n = C.c_int32(-1)
+    assert lib.mtp_timing_begin(None, 4) == 1
+    assert lib.mtp_timing_begin(evs, 1) == 1
+    assert lib.mtp_timing_end(C.byref(n)) == 1            # no session open
+    assert lib.mtp_timing_begin(evs, 4) == 0
+    assert lib.mtp_timing_begin(evs, 4) == 1              # already open
+    assert lib.mtp_timing_end(C.byref(n)) == 0 and n.value == 0
+    # a rejected call launches nothing, so it makes no mark either
+    assert lib.mtp_timing_begin(evs, 4) == 0
+    w = _fake_affine(64, 100)
+    p = C.c_void_p(0x1000)
+    assert lib.qmatmul_affine4(p, C.byref(w), p, 1, p, 1 << 20, None) == 2
+    assert lib.mtp_timing_end(C.byref(n)) == 0 and n.value == 0
+    assert lib.mtp_workspace_set_wait_limit(None, 1, None) == 1
+    assert lib.mtp_workspace_set_wait_limit(p, -1, None) == 1
