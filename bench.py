@@ -53,8 +53,9 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=WORKLOAD, choices=CONFIG_CHOICES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--seq", type=int, default=512, help="rows of the catch-up batch (--profile-kernel catch_up)")
     ap.add_argument("--profile-kernel", default=None,
-                    choices=["lm_head", "ffn_down", "attention", "verify_head", "step"],
+                    choices=["lm_head", "ffn_down", "attention", "verify_head", "step", "catch_up"],
                     help="run only one entry point of the workload (small device footprint, for ncu)")
     return ap.parse_args()
 
@@ -705,6 +706,22 @@ def run_profile_kernel(args):
             ws = None
             run = lambda: A.qmatmul_affine4(x, w.desc, y, 1, ws)  # noqa: E731
             ws = A.qmatmul_affine4(x, w.desc, y, 1)
+    elif args.profile_kernel == "catch_up":
+        # KV catch-up of a target batch of --seq rows (tcgen05 projections)
+        from mtp_speculative_draft_gb300.layer import DraftLayer, SharedHead
+        from mtp_synth.configs import make_layer_weights, make_shared, make_state
+        seq = args.seq
+        c2 = cfg.with_(cache_len=0, m=seq)
+        shared = make_shared(c2, embed_rows=np.arange(seq) % cfg.vocab)
+        lyr = DraftLayer(cfg, make_layer_weights(cfg), SharedHead(shared, dev), make_state(c2),
+                         device=dev)
+        rows = torch.from_numpy(shared["embed_rows"]).to(dev)
+        target = torch.from_numpy(mtp_synth.normal_f32(cfg.seed, "profile.target", (seq, H))).to(dev)
+        run = lambda: lyr.catch_up(target, seq, 0, embed_rows=rows, pending=target[0])  # noqa: E731
+        nkv, dq, dv = cfg.n_kv_heads, cfg.head_dim_qk, cfg.head_dim_v
+        flop = 2 * seq * (H * 2 * H + H * nkv * (dq + dv))
+        extra.update(seq=seq, algorithmic_flop_per_call=flop,
+                     weight_bytes=aff(H, 2 * H) + aff(nkv * (dq + dv), H))
     elif args.profile_kernel == "step":
         # one whole draft step, embedding rows passed directly (no 3 GB table
         # on the device), for launch lists and captures of the step's launches
@@ -750,6 +767,18 @@ def run_profile_kernel(args):
     e1.record()
     torch.cuda.synchronize()
     ms = e0.elapsed_time(e1) / max(1, args.steps)
+    if args.profile_kernel == "catch_up":
+        from mtp_speculative_draft_gb300.api import launch_timing
+        lms, nl_ = timed_launches(run, 8, 10)
+        extra["launch_ms"] = lms
+        gemm_ms = lms[1] + lms[3]
+        extra["gemm_tflops"] = extra["algorithmic_flop_per_call"] / (gemm_ms * 1e-3) / 1e12
+        extra["call_tflops"] = extra["algorithmic_flop_per_call"] / (ms * 1e-3) / 1e12
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            pk = json.load(fh)
+        # three bf16 products per K16 step (hi*hi, hi*lo, lo*hi): the tensor pipe
+        # issues 3x the algorithmic flops
+        extra["tensor_frac_of_bf16_peak"] = 3 * extra["gemm_tflops"] / float(pk["bf16_tflops"])
     if "algorithmic_bytes_per_call" in extra:
         peak, kind = measured_peaks()
         extra["gbs"] = extra["algorithmic_bytes_per_call"] / (ms * 1e-3) / 1e9

@@ -311,7 +311,7 @@ typedef struct {
     const float *final_norm;         /* [hidden] */
     mtp_affine4 lm_head;             /* [vocab][hidden] */
     const float *embed;              /* [vocab][hidden] float32, or NULL (caller passes rows) */
-    const float *rope;               /* mtp_rope_table with max_pos >= cache_cap */
+    const float *rope;               /* mtp_rope_table with max_pos >= pos_base + cache_cap */
     float *k_cache, *v_cache;        /* [n_kv][cache_cap][d] */
     int32_t cache_cap;
 } mtp_layer_desc;
@@ -322,6 +322,9 @@ typedef struct {
     const float *d_hidden;           /* [m][hidden] target hidden states */
     int32_t cache_len;               /* rows already in the layer's cache */
     int32_t m;                       /* new rows, 1..16 */
+    int32_t pos_base;                /* rotary position of cache row 0 (0 unless the cache
+                                        was restarted part-way); row r rotates at
+                                        pos_base + cache_len + r */
 } mtp_step_in;
 
 typedef struct {
@@ -355,6 +358,31 @@ mtp_status mtp_draft_chain(const mtp_layer_desc *layers, int32_t n_layers,
                            const float *d_hidden, int32_t *d_seq, const int32_t *cache_lens,
                            int32_t m, float *d_values, float *d_hidden_out, float *d_u2,
                            float *d_logits, void *d_ws, size_t ws_bytes, void *stream);
+
+/* ------------------------------------------------------------------------
+ * mtp_kv_catch_up: the K/V rows of a target batch of seq tokens, written to
+ * the layer's cache ("hf2q 0.1.13 ... mtp.rs", process_target_batch and
+ * append_attention_kv).  Row i embeds d_tokens[i] (or d_embed_rows[i]) and
+ * reads the target hidden shifted one row right: row 0 reads d_pending (the
+ * target hidden of the token before the batch; NULL for a cold prompt reads
+ * zeros), row i > 0 reads d_target[i - 1] (the last target row is not read).
+ *   u = eh_proj [RMSNorm(e)*enorm ; RMSNorm(h)*hnorm]  (eps 1e-6)
+ *   x = RMSNorm(u)*attn_norm;  k = W_k x, per-head RMSNorm by k_norm (if
+ *   given), rotated at pos_base + cache_len + i;  v = W_v x.
+ * Rows go to cache rows cache_len .. cache_len + seq - 1.  No attention, FFN
+ * or head runs.  The projections run on the tensor cores (tcgen05) with bf16
+ * hi + lo parts of the dequantised weights and of the activations.
+ *   d_target [seq][hidden] (may be NULL when seq == 1); d_pending [hidden].
+ *   1 <= seq <= 65535; 1..32 KV heads; the layer's q/o/FFN/head weights are
+ *   not read.  Token ids outside [0, vocab) set device error code 2 (row 0
+ *   is used).  The workspace (mtp_kv_catch_up_workspace_bytes) is about
+ *   12 * seq * hidden bytes plus split-K partials.
+ * ------------------------------------------------------------------------ */
+size_t mtp_kv_catch_up_workspace_bytes(const mtp_layer_desc *L, int32_t seq);
+mtp_status mtp_kv_catch_up(const mtp_layer_desc *L, const int32_t *d_tokens,
+                           const float *d_embed_rows, const float *d_target,
+                           const float *d_pending, int32_t seq, int32_t cache_len,
+                           int32_t pos_base, void *d_ws, size_t ws_bytes, void *stream);
 
 /* ------------------------------------------------------------------------
  * Speculation bookkeeping of one sequence (host only: no device work, no

@@ -55,7 +55,7 @@ class LayerDesc(C.Structure):
 
 class StepIn(C.Structure):
     _fields_ = [("d_tokens", vp), ("d_embed_rows", vp), ("d_hidden", vp), ("cache_len", i32),
-                ("m", i32)]
+                ("m", i32), ("pos_base", i32)]
 
 
 SPEC_MAX_DEPTH = 16
@@ -108,6 +108,8 @@ EXPORTS = {
                                     vp, sz, vp]),
     "mtp_draft_chain": (C.c_int, [C.POINTER(LayerDesc), i32, vp, vp, C.POINTER(i32), i32, vp, vp,
                                   vp, vp, vp, sz, vp]),
+    "mtp_kv_catch_up_workspace_bytes": (sz, [C.POINTER(LayerDesc), i32]),
+    "mtp_kv_catch_up": (C.c_int, [C.POINTER(LayerDesc), vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
 }
 
 

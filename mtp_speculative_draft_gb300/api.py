@@ -185,6 +185,17 @@ def mtp_draft_chain(descs, hidden, seq, cache_lens, m, values, hidden_out, ws, s
           "mtp_draft_chain")
 
 
+def mtp_kv_catch_up(desc, tokens, embed_rows, target, pending, seq, cache_len, pos_base=0, ws=None,
+                    stream=None):
+    lib = L.load()
+    if ws is None:
+        ws = workspace(lib.mtp_kv_catch_up_workspace_bytes(C.byref(desc), seq), stream=stream)
+    check(lib.mtp_kv_catch_up(C.byref(desc), _p(tokens), _p(embed_rows), _p(target), _p(pending),
+                              int(seq), int(cache_len), int(pos_base), _p(ws), ws.numel(),
+                              _stream(stream)), "mtp_kv_catch_up")
+    return ws
+
+
 # ------------------------------------------------------------- speculation bookkeeping (host)
 def _i32_array(values):
     vals = [int(v) for v in values]

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmtpdraft.so")
-SOURCES = ["api.cu", "gemv.cu", "norm.cu", "attn.cu", "moe.cu", "spec.cu"]
+SOURCES = ["api.cu", "gemv.cu", "norm.cu", "attn.cu", "moe.cu", "spec.cu", "catchup.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -918,6 +918,7 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   // 5. attention (norm + rope + append + split-K + sink + gate), packed output
   AttnParams a = make_attn(&g, w.qp, w.kp, w.vp, L->q_norm, L->k_norm, L->rope, L->sinks,
                            L->k_cache, L->v_cache, in->cache_len, L->cache_cap, m);
+  a.pos_base = in->pos_base;
   a.part = w.part;
   a.counters = header(ws)->counters + kCntAttn;
   a.err = err;
@@ -1066,7 +1067,8 @@ mtp_status mtp_draft_forward(const mtp_layer_desc* L, const mtp_step_in* in,
   if (L->embed ? !in->d_tokens : (!in->d_embed_rows || !aligned16(in->d_embed_rows)))
     return fail(MTP_ERR_INVALID_ARG,
                 "mtp_draft_forward: tokens (with a table) or embedding rows are required");
-  if (in->cache_len < 0) return fail(MTP_ERR_INVALID_ARG, "mtp_draft_forward: negative cache_len");
+  if (in->cache_len < 0 || in->pos_base < 0)
+    return fail(MTP_ERR_INVALID_ARG, "mtp_draft_forward: negative cache_len or pos_base");
   if (in->cache_len + in->m > L->cache_cap)
     return fail(MTP_ERR_CAPACITY, "mtp_draft_forward: cache_len + m exceeds the cache capacity");
   if (!out->d_token || !out->d_value)

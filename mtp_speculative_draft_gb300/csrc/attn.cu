@@ -79,55 +79,6 @@ __host__ __device__ inline AttnLayout attn_layout(int dqk, int dv, int qslots, i
   return L;
 }
 
-// One head vector (d <= 256) read from global memory by one warp: per-head
-// RMSNorm (when nw is given), rotary embedding of the first rot dims (pairs
-// i, i + rot/2), times post_scale; the result goes to v in shared memory.
-// All global loads are issued before any arithmetic.
-__device__ __forceinline__ void warp_norm_rope(float* v, const float* src, int d, const float* nw,
-                                               float eps, const float* rope_row, int rot,
-                                               float post_scale, int lane) {
-  float x[8], w[8], cs[4], sn[4];
-  const int half = rot / 2;
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int i = lane + 32 * j;
-    x[j] = i < d ? src[i] : 0.f;
-    w[j] = (nw && i < d) ? nw[i] : 1.f;
-  }
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int i = lane + 32 * j;
-    cs[j] = i < half ? rope_row[2 * i] : 1.f;
-    sn[j] = i < half ? rope_row[2 * i + 1] : 0.f;
-  }
-  float inv = 1.f;
-  if (nw) {
-    float ss = 0.f;
-#pragma unroll
-    for (int j = 0; j < 8; ++j) ss += x[j] * x[j];
-    inv = rsqrtf(warp_sum(ss) / (float)d + eps);
-  }
-#pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    const int i = lane + 32 * j;
-    if (i < d) v[i] = x[j] * inv * w[j];
-  }
-  __syncwarp();
-#pragma unroll
-  for (int j = 0; j < 4; ++j) {
-    const int i = lane + 32 * j;
-    if (i < half) {
-      const float a = v[i], b = v[i + half];
-      v[i] = a * cs[j] - b * sn[j];
-      v[i + half] = a * sn[j] + b * cs[j];
-    }
-  }
-  __syncwarp();
-  if (post_scale != 1.f)
-    for (int i = lane; i < d; i += 32) v[i] *= post_scale;
-  __syncwarp();
-}
-
 // Waits (one thread, bounded) until *cnt >= target; acquire.
 __device__ __forceinline__ bool wait_count_cta(const unsigned* cnt, unsigned target,
                                                unsigned polls) {
@@ -372,7 +323,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
     if (l < qpw && qi < QG) {
       const int r = qi / G, h = kvh * G + qi % G;
       const float* src = a.qp + (size_t)r * q_rows + (size_t)h * dqk * (a.gated ? 2 : 1);
-      warp_norm_rope(dst, src, dqk, a.qn, a.eps, a.rope + (size_t)(L + r) * a.rot, a.rot, qscale,
+      warp_norm_rope(dst, src, dqk, a.qn, a.eps, a.rope + (size_t)(a.pos_base + L + r) * a.rot, a.rot, qscale,
                      lane);
     } else {
       for (int i = lane; i < dqk; i += 32) dst[i] = 0.f;
@@ -386,7 +337,8 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
       const int pos = L + r;
       float* kn = newk + r * dqk;
       const float* ksrc = a.kp + (size_t)r * a.nkv * dqk + (size_t)kvh * dqk;
-      warp_norm_rope(kn, ksrc, dqk, a.kn, a.eps, a.rope + (size_t)pos * a.rot, a.rot, 1.f, lane);
+      warp_norm_rope(kn, ksrc, dqk, a.kn, a.eps, a.rope + (size_t)(a.pos_base + pos) * a.rot, a.rot,
+                     1.f, lane);
       float* kdst = a.kc + ((size_t)kvh * a.cap + pos) * dqk;
       for (int i = lane; i < dqk; i += 32) kdst[i] = kn[i];
       float* vn = newv + r * dv;

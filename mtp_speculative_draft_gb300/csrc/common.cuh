@@ -182,4 +182,53 @@ __device__ __forceinline__ unsigned wait_polls(const int* err, unsigned dflt) {
   return v > 0 ? (unsigned)v : dflt;
 }
 
+// One head vector (d <= 256) read by one warp (global or shared memory): per-head
+// RMSNorm (when nw is given), rotary embedding of the first rot dims (pairs
+// i, i + rot/2), times post_scale; the result goes to v in shared memory.
+// All global loads are issued before any arithmetic.
+__device__ __forceinline__ void warp_norm_rope(float* v, const float* src, int d, const float* nw,
+                                               float eps, const float* rope_row, int rot,
+                                               float post_scale, int lane) {
+  float x[8], w[8], cs[4], sn[4];
+  const int half = rot / 2;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = lane + 32 * j;
+    x[j] = i < d ? src[i] : 0.f;
+    w[j] = (nw && i < d) ? nw[i] : 1.f;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = lane + 32 * j;
+    cs[j] = i < half ? rope_row[2 * i] : 1.f;
+    sn[j] = i < half ? rope_row[2 * i + 1] : 0.f;
+  }
+  float inv = 1.f;
+  if (nw) {
+    float ss = 0.f;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) ss += x[j] * x[j];
+    inv = rsqrtf(warp_sum(ss) / (float)d + eps);
+  }
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const int i = lane + 32 * j;
+    if (i < d) v[i] = x[j] * inv * w[j];
+  }
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const int i = lane + 32 * j;
+    if (i < half) {
+      const float a = v[i], b = v[i + half];
+      v[i] = a * cs[j] - b * sn[j];
+      v[i + half] = a * sn[j] + b * cs[j];
+    }
+  }
+  __syncwarp();
+  if (post_scale != 1.f)
+    for (int i = lane; i < d; i += 32) v[i] *= post_scale;
+  __syncwarp();
+}
+
 }  // namespace mtp

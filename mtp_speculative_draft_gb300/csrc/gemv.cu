@@ -393,6 +393,15 @@ cudaError_t encode_f32_tile_map(CUtensorMap* out, const float* base, uint64_t ro
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+cudaError_t encode_bf16_rows_map(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols,
+                                 int box_rows) {
+  // rows of `cols` bf16, box box_rows x 64 (128 bytes), 128-byte swizzle;
+  // rows past `rows` read as zeros
+  CUresult r = encode2d(out, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, cols, rows, cols * 2, 64,
+                        (uint32_t)box_rows, CU_TENSOR_MAP_SWIZZLE_128B);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 mtp_status encode_qmat(QMat* out, const mtp_affine4& w, const char* name) {
   const uint64_t kw = (uint64_t)w.k / 8, kg = (uint64_t)w.k / kGroup;
   CUresult r = encode2d(&out->q, CU_TENSOR_MAP_DATA_TYPE_UINT32, w.q, kw, (uint64_t)w.n, kw * 4,

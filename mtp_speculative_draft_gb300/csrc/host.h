@@ -80,6 +80,11 @@ struct NormSeg {
 cudaError_t launch_norm_pack(const NormSeg* segs, int nseg, int m, uint4* xp, float2* xs,
                              int* err, cudaStream_t st);
 
+// Tensor map over bf16 rows [rows][cols] with boxes of box_rows x 64 values
+// (128 bytes), 128-byte swizzle (the tcgen05 K-major operand layout).
+cudaError_t encode_bf16_rows_map(CUtensorMap* out, const void* base, uint64_t rows, uint64_t cols,
+                                 int box_rows);
+
 // Tensor map over float rows [rows][cols] with boxes of box_rows x 32 floats,
 // 128-byte swizzle.
 cudaError_t encode_f32_tile_map(CUtensorMap* out, const float* base, uint64_t rows, uint64_t cols,
@@ -92,6 +97,7 @@ struct alignas(64) AttnParams {
   const float *qp, *kp, *vp, *qn, *kn, *rope, *sinks;
   float *kc, *vc;
   int L, cap, m;
+  int pos_base;        // rotary position of cache row 0
   float* out;          // [m][nh*dv] fp32 (may be null)
   uint4* out_xp;       // packed output for the next projection (may be null)
   float2* out_xs;

@@ -107,12 +107,24 @@ class DraftLayer:
         self.ws = workspace(L.load().mtp_draft_workspace_bytes(C.byref(d), self.m_max))
 
     def forward(self, hidden, cache_len, tokens=None, embed_rows=None, token=None, value=None,
-                hidden_out=None, u2=None, logits=None, stream=None):
+                hidden_out=None, u2=None, logits=None, stream=None, pos_base=0):
         """Enqueues one draft step; outputs are written into the given device tensors."""
         from .api import mtp_draft_forward
-        si = L.StepIn(_p(tokens), _p(embed_rows), _p(hidden), int(cache_len), int(hidden.shape[0]))
+        si = L.StepIn(_p(tokens), _p(embed_rows), _p(hidden), int(cache_len), int(hidden.shape[0]),
+                      int(pos_base))
         so = L.StepOut(_p(token), _p(value), _p(hidden_out), _p(u2), _p(logits))
         mtp_draft_forward(self.desc, si, so, self.ws, stream)
+
+
+    def catch_up(self, target, seq, cache_len, tokens=None, embed_rows=None, pending=None,
+                 pos_base=0, stream=None):
+        """Enqueues the K/V catch-up of a target batch of ``seq`` rows."""
+        from .api import mtp_kv_catch_up
+        need = L.load().mtp_kv_catch_up_workspace_bytes(C.byref(self.desc), int(seq))
+        if getattr(self, "catch_ws", None) is None or self.catch_ws.numel() < need:
+            self.catch_ws = workspace(need)
+        mtp_kv_catch_up(self.desc, tokens, embed_rows, target, pending, seq, cache_len, pos_base,
+                        self.catch_ws, stream)
 
 
 class DraftChain:
