@@ -359,6 +359,22 @@ mtp_status mtp_draft_chain(const mtp_layer_desc *layers, int32_t n_layers,
                            int32_t m, float *d_values, float *d_hidden_out, float *d_u2,
                            float *d_logits, void *d_ws, size_t ws_bytes, void *stream);
 
+/* k_steps chained one-row draft steps of one layer ("hf2q 0.1.13 ... mtp.rs",
+ * forward_draft_with_hidden: a chained step reads the normed row the shared
+ * head returns, the only valid hidden for a second MTP step).  Step i
+ * embeds d_tokens[i], reads hidden h_i (h_0 = d_hidden [hidden], h_{i+1} =
+ * d_hidden_out[i]), appends its K/V row at cache row cache_len + i (rotary
+ * position pos_base + cache_len + i), and writes its draft to
+ * d_tokens[i + 1], its logit to d_values[i] and its normed row to
+ * d_hidden_out[i] ([k_steps][hidden]).  d_tokens holds k_steps + 1 int32,
+ * the first given.  The layer needs an embedding table; the steps follow
+ * each other on the device with no host synchronisation.  d_ws: at least
+ * mtp_draft_workspace_bytes(L, 1). */
+mtp_status mtp_draft_steps(const mtp_layer_desc *L, int32_t k_steps, const float *d_hidden,
+                           int32_t *d_tokens, int32_t cache_len, int32_t pos_base,
+                           float *d_values, float *d_hidden_out, void *d_ws, size_t ws_bytes,
+                           void *stream);
+
 /* ------------------------------------------------------------------------
  * mtp_kv_catch_up: the K/V rows of a target batch of seq tokens, written to
  * the layer's cache ("hf2q 0.1.13 ... mtp.rs", process_target_batch and
@@ -429,6 +445,60 @@ double mtp_spec_tokens_per_round(const mtp_spec_stats *s);
  * lengths at or below it are unchanged.  MTP_ERR_INVALID_ARG on a NULL
  * array with n_layers > 0, n_layers < 0 or keep < 0. */
 mtp_status mtp_spec_rewind(int32_t *cache_len, int32_t n_layers, int32_t keep);
+
+/* One draft layer's round state ("cortiq-engine 0.8.49 src/mimo_mtp.rs",
+ * MimoMtp): cache rows at positions below `committed` are final, `base` is
+ * the position of the cache's first row, `kv_len` the rows the cache holds.
+ * Zero-initialise before the first round. */
+typedef struct {
+    int32_t committed;
+    int32_t base;
+    int32_t kv_len;
+} mtp_mimo_layer_state;
+
+/* Plans layer `layer`'s part of a round that starts after the backbone
+ * processed position t (mimo_mtp_draft): the target-hidden history holds
+ * positions [hist_lo, hist_end) and ids_len token ids are known (x_{t+1}
+ * among them).  Returns the number of rows to run, n = t + 1 - *start (rows
+ * at positions *start .. t; row j embeds token j + layer + 1, a round's
+ * earlier draft past the known ids), 0 when nothing is drafted this round
+ * (the history lacks t, or ids_len < t + 2), -1 on a NULL pointer.  Updates
+ * *st: a committed position below the history (a gap) or beyond t + 1 (a
+ * stale state) restarts the cache at hist_lo (kv_len = 0, base = committed
+ * = hist_lo); the previous round's provisional rows are dropped (kv_len =
+ * committed - base).  The rows go to cache rows *start - base onwards, at
+ * rotary positions *start onwards (pos_base = base). */
+int32_t mtp_mimo_plan_layer(mtp_mimo_layer_state *st, int32_t layer, int32_t t, int32_t hist_lo,
+                            int32_t hist_end, int32_t ids_len, int32_t *start);
+
+/* After the layer ran its rows: kv_len = t + 1 - base, and committed rises to
+ * min(t + 1, ids_len - layer - 1) (the rows whose token is known). */
+mtp_status mtp_mimo_commit_layer(mtp_mimo_layer_state *st, int32_t layer, int32_t t,
+                                 int32_t ids_len);
+
+/* The draft half of one MiMo round on the device (mimo_mtp_draft): for each
+ * layer l < n_layers in order, mtp_mimo_plan_layer, then its rows: positions
+ * start .. t - 1 only add K/V rows (mtp_kv_catch_up: row j embeds
+ * d_ids[j + l + 1] and reads target hidden row j), and position t runs a
+ * one-row draft step whose argmax goes to d_ids[t + l + 2] and its logit to
+ * d_values[l]; then mtp_mimo_commit_layer.  Only the last row of a layer
+ * reaches the head and its output depends on the earlier rows only through
+ * their K/V rows, so this equals running all n rows through the layer.
+ *   d_hist: target hidden rows [hist_end - hist_lo][hidden] for positions
+ *     hist_lo .. hist_end - 1;  d_ids: token ids by position, at least
+ *     t + n_layers + 2 entries (the first ids_len known);
+ *   states[n_layers] are updated on the host as the launches are enqueued;
+ *   d_ws: mtp_draft_workspace_bytes(layer, 1) for every layer;
+ *   d_catch_ws: mtp_kv_catch_up_workspace_bytes(layer, rows) for the most
+ *     rows a layer catches up (t - hist_lo after a restart).
+ * *n_drafts receives the number of layers run (0: no draft this round).
+ * The layers need an embedding table.  No host synchronisation. */
+mtp_status mtp_mimo_draft_round(const mtp_layer_desc *layers, int32_t n_layers,
+                                mtp_mimo_layer_state *states, const float *d_hist,
+                                int32_t hist_lo, int32_t hist_end, int32_t t, int32_t *d_ids,
+                                int32_t ids_len, float *d_values, void *d_ws, size_t ws_bytes,
+                                void *d_catch_ws, size_t catch_ws_bytes, void *stream,
+                                int32_t *n_drafts);
 
 #ifdef __cplusplus
 }

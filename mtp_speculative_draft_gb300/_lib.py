@@ -58,6 +58,10 @@ class StepIn(C.Structure):
                 ("m", i32), ("pos_base", i32)]
 
 
+class MimoLayerState(C.Structure):
+    _fields_ = [("committed", i32), ("base", i32), ("kv_len", i32)]
+
+
 SPEC_MAX_DEPTH = 16
 
 
@@ -108,6 +112,11 @@ EXPORTS = {
                                     vp, sz, vp]),
     "mtp_draft_chain": (C.c_int, [C.POINTER(LayerDesc), i32, vp, vp, C.POINTER(i32), i32, vp, vp,
                                   vp, vp, vp, sz, vp]),
+    "mtp_draft_steps": (C.c_int, [C.POINTER(LayerDesc), i32, vp, vp, i32, i32, vp, vp, vp, sz, vp]),
+    "mtp_mimo_plan_layer": (i32, [C.POINTER(MimoLayerState), i32, i32, i32, i32, i32, C.POINTER(i32)]),
+    "mtp_mimo_commit_layer": (C.c_int, [C.POINTER(MimoLayerState), i32, i32, i32]),
+    "mtp_mimo_draft_round": (C.c_int, [C.POINTER(LayerDesc), i32, C.POINTER(MimoLayerState), vp, i32,
+                                       i32, i32, vp, i32, vp, vp, sz, vp, sz, vp, C.POINTER(i32)]),
     "mtp_kv_catch_up_workspace_bytes": (sz, [C.POINTER(LayerDesc), i32]),
     "mtp_kv_catch_up": (C.c_int, [C.POINTER(LayerDesc), vp, vp, vp, vp, i32, i32, i32, vp, sz, vp]),
 }

@@ -7,7 +7,7 @@ import ctypes as C
 import torch
 
 from . import _lib as L
-from ._lib import Affine4, AttnGeom, MoeWeights, SpecStats, check
+from ._lib import Affine4, AttnGeom, MimoLayerState, MoeWeights, SpecStats, check
 
 
 def _p(t):
@@ -196,6 +196,27 @@ def mtp_kv_catch_up(desc, tokens, embed_rows, target, pending, seq, cache_len, p
     return ws
 
 
+def mtp_draft_steps(desc, k_steps, hidden, tokens, cache_len, values, hidden_out, ws, pos_base=0,
+                    stream=None):
+    check(L.load().mtp_draft_steps(C.byref(desc), int(k_steps), _p(hidden), _p(tokens),
+                                   int(cache_len), int(pos_base), _p(values), _p(hidden_out),
+                                   _p(ws), ws.numel(), _stream(stream)), "mtp_draft_steps")
+
+
+def mtp_mimo_draft_round(descs, states, hist, hist_lo, hist_end, t, ids, ids_len, values, ws,
+                         catch_ws, stream=None) -> int:
+    """The device half of a MiMo round; ``states`` is a ctypes array of
+    MimoLayerState updated in place; returns the number of drafts."""
+    arr = (L.LayerDesc * len(descs))(*descs)
+    n = C.c_int32(0)
+    check(L.load().mtp_mimo_draft_round(arr, len(descs), states, _p(hist), int(hist_lo),
+                                        int(hist_end), int(t), _p(ids), int(ids_len), _p(values),
+                                        _p(ws), ws.numel(), _p(catch_ws),
+                                        0 if catch_ws is None else catch_ws.numel(),
+                                        _stream(stream), C.byref(n)), "mtp_mimo_draft_round")
+    return n.value
+
+
 # ------------------------------------------------------------- speculation bookkeeping (host)
 def _i32_array(values):
     vals = [int(v) for v in values]
@@ -229,3 +250,18 @@ def mtp_spec_rewind(cache_len, keep: int) -> list:
     check(L.load().mtp_spec_rewind(arr, n, keep), "mtp_spec_rewind")
     return list(arr[:n])
 
+
+
+def mtp_mimo_plan_layer(state: MimoLayerState, layer: int, t: int, hist_lo: int, hist_end: int,
+                        ids_len: int):
+    """(rows to run, first position) of one layer's part of a MiMo round; updates ``state``."""
+    start = C.c_int32(0)
+    n = L.load().mtp_mimo_plan_layer(C.byref(state), layer, t, hist_lo, hist_end, ids_len,
+                                     C.byref(start))
+    if n < 0:
+        raise ValueError("mtp_mimo_plan_layer: bad arguments")
+    return n, start.value
+
+
+def mtp_mimo_commit_layer(state: MimoLayerState, layer: int, t: int, ids_len: int):
+    check(L.load().mtp_mimo_commit_layer(C.byref(state), layer, t, ids_len), "mtp_mimo_commit_layer")

@@ -1123,6 +1123,102 @@ mtp_status mtp_draft_chain(const mtp_layer_desc* layers, int32_t n_layers, const
   return MTP_OK;
 }
 
+mtp_status mtp_draft_steps(const mtp_layer_desc* L, int32_t k_steps, const float* d_hidden,
+                           int32_t* d_tokens, int32_t cache_len, int32_t pos_base,
+                           float* d_values, float* d_hidden_out, void* d_ws, size_t ws_bytes,
+                           void* stream) {
+  mtp_status s = check_layer(L, 1);
+  if (s != MTP_OK) return s;
+  if (k_steps < 1 || k_steps > 64) return fail(MTP_ERR_UNSUPPORTED, "mtp_draft_steps: k_steps must be in 1..64");
+  if (!L->embed) return fail(MTP_ERR_INVALID_ARG, "mtp_draft_steps: the layer needs an embedding table");
+  if (!d_hidden || !d_tokens || !d_values || !d_hidden_out)
+    return fail(MTP_ERR_INVALID_ARG, "mtp_draft_steps: null argument");
+  if (!aligned16(d_hidden) || !aligned16(d_hidden_out))
+    return fail(MTP_ERR_INVALID_ARG, "mtp_draft_steps: hidden rows must be 16-byte aligned");
+  if (cache_len < 0 || pos_base < 0)
+    return fail(MTP_ERR_INVALID_ARG, "mtp_draft_steps: negative cache_len or pos_base");
+  if (cache_len + k_steps > L->cache_cap)
+    return fail(MTP_ERR_CAPACITY, "mtp_draft_steps: cache_len + k_steps exceeds the cache capacity");
+  if (!d_ws || ws_bytes < mtp_draft_workspace_bytes(L, 1))
+    return fail(MTP_ERR_WORKSPACE, "mtp_draft_steps: workspace too small");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int H = L->hidden;
+  for (int i = 0; i < k_steps; ++i) {
+    mtp_step_in in = {};
+    in.d_tokens = d_tokens + i;
+    in.d_hidden = i == 0 ? d_hidden : d_hidden_out + (size_t)(i - 1) * H;
+    in.cache_len = cache_len + i;
+    in.m = 1;
+    in.pos_base = pos_base;
+    mtp_step_out out = {};
+    out.d_token = d_tokens + i + 1;
+    out.d_value = d_values + i;
+    out.d_hidden_out = d_hidden_out + (size_t)i * H;
+    if ((s = enqueue_layer(L, &in, &out, d_ws, st)) != MTP_OK) return s;
+  }
+  return MTP_OK;
+}
+
+mtp_status mtp_mimo_draft_round(const mtp_layer_desc* layers, int32_t n_layers,
+                                mtp_mimo_layer_state* states, const float* d_hist,
+                                int32_t hist_lo, int32_t hist_end, int32_t t, int32_t* d_ids,
+                                int32_t ids_len, float* d_values, void* d_ws, size_t ws_bytes,
+                                void* d_catch_ws, size_t catch_ws_bytes, void* stream,
+                                int32_t* n_drafts) {
+  if (!layers || !states || !d_hist || !d_ids || !d_values || !n_drafts || n_layers < 1 ||
+      n_layers > MTP_SPEC_MAX_DEPTH)
+    return fail(MTP_ERR_INVALID_ARG, "mtp_mimo_draft_round: bad arguments");
+  *n_drafts = 0;
+  if (!aligned16(d_hist)) return fail(MTP_ERR_INVALID_ARG, "mtp_mimo_draft_round: d_hist must be 16-byte aligned");
+  // every check before any state changes or launches
+  for (int l = 0; l < n_layers; ++l) {
+    mtp_status s = check_layer(&layers[l], 1);
+    if (s != MTP_OK) return s;
+    if (!layers[l].embed) return fail(MTP_ERR_INVALID_ARG, "mtp_mimo_draft_round: layers need an embedding table");
+    if (layers[l].hidden != layers[0].hidden)
+      return fail(MTP_ERR_INVALID_ARG, "mtp_mimo_draft_round: layers must share the hidden size");
+    if (!d_ws || ws_bytes < mtp_draft_workspace_bytes(&layers[l], 1))
+      return fail(MTP_ERR_WORKSPACE, "mtp_mimo_draft_round: workspace too small");
+    mtp_mimo_layer_state probe = states[l];
+    int32_t start = 0;
+    const int32_t n = mtp_mimo_plan_layer(&probe, l, t, hist_lo, hist_end, ids_len, &start);
+    if (n <= 0) return MTP_OK;  // no draft this round (the history lacks t)
+    if (t + 1 - probe.base > layers[l].cache_cap)
+      return fail(MTP_ERR_CAPACITY, "mtp_mimo_draft_round: the rows exceed a layer's cache");
+    if (n > 1 && (!d_catch_ws || catch_ws_bytes < mtp_kv_catch_up_workspace_bytes(&layers[l], n - 1)))
+      return fail(MTP_ERR_WORKSPACE, "mtp_mimo_draft_round: catch-up workspace too small");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int H = layers[0].hidden;
+  auto hist_row = [&](int pos) { return d_hist + (size_t)(pos - hist_lo) * H; };
+  for (int l = 0; l < n_layers; ++l) {
+    const mtp_layer_desc* L = &layers[l];
+    mtp_mimo_layer_state& ls = states[l];
+    int32_t start = 0;
+    const int32_t n = mtp_mimo_plan_layer(&ls, l, t, hist_lo, hist_end, ids_len, &start);
+    mtp_status s;
+    if (n > 1) {  // positions start .. t - 1 add K/V rows only
+      s = mtp_kv_catch_up(L, d_ids + start + l + 1, nullptr, n > 2 ? hist_row(start + 1) : nullptr,
+                          hist_row(start), n - 1, start - ls.base, ls.base, d_catch_ws,
+                          catch_ws_bytes, stream);
+      if (s != MTP_OK) return s;
+    }
+    mtp_step_in in = {};  // position t: the layer's draft
+    in.d_tokens = d_ids + t + l + 1;
+    in.d_hidden = hist_row(t);
+    in.cache_len = t - ls.base;
+    in.m = 1;
+    in.pos_base = ls.base;
+    mtp_step_out out = {};
+    out.d_token = d_ids + t + l + 2;
+    out.d_value = d_values + l;
+    if ((s = enqueue_layer(L, &in, &out, d_ws, st)) != MTP_OK) return s;
+    if ((s = mtp_mimo_commit_layer(&ls, l, t, ids_len)) != MTP_OK) return s;
+    *n_drafts = l + 1;
+  }
+  return MTP_OK;
+}
+
 }  // extern "C"
 
 // ------------------------------------------------ attention without a workspace

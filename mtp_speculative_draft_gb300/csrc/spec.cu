@@ -2,7 +2,8 @@
 //
 // "cortiq-engine 0.8.49 src/mimo_mtp.rs": the counters of MtpStats and its
 // tokens_per_round, the accepted prefix and the counter updates at the end
-// of mimo_spec_round, and the absolute rewind of mimo_verify_rewind.
+// of mimo_spec_round, the absolute rewind of mimo_verify_rewind, and the
+// per-layer committed/base state of mimo_mtp_draft.
 #include "host.h"
 
 extern "C" {
@@ -43,6 +44,35 @@ mtp_status mtp_spec_rewind(int32_t* cache_len, int32_t n_layers, int32_t keep) {
     return mtp::fail(MTP_ERR_INVALID_ARG, "mtp_spec_rewind: bad arguments");
   for (int32_t l = 0; l < n_layers; ++l)
     if (cache_len[l] > keep) cache_len[l] = keep;
+  return MTP_OK;
+}
+
+int32_t mtp_mimo_plan_layer(mtp_mimo_layer_state* st, int32_t layer, int32_t t, int32_t hist_lo,
+                            int32_t hist_end, int32_t ids_len, int32_t* start) {
+  if (!st || !start || layer < 0) return -1;
+  // no draft this round: the history lacks position t, or x_{t+1} is unknown
+  if (hist_end <= hist_lo || t < hist_lo || t >= hist_end || ids_len < t + 2) return 0;
+  if (st->committed < hist_lo || st->committed > t + 1) {
+    // a history gap (first round after a long prompt) or a stale state
+    st->kv_len = 0;
+    st->base = hist_lo;
+    st->committed = hist_lo;
+  }
+  const int32_t keep = st->committed - st->base;  // drop last round's provisional rows
+  if (st->kv_len > keep) st->kv_len = keep;
+  *start = st->committed;
+  return t + 1 - st->committed;
+}
+
+mtp_status mtp_mimo_commit_layer(mtp_mimo_layer_state* st, int32_t layer, int32_t t,
+                                 int32_t ids_len) {
+  if (!st || layer < 0 || t + 1 < st->base)
+    return mtp::fail(MTP_ERR_INVALID_ARG, "mtp_mimo_commit_layer: bad arguments");
+  st->kv_len = t + 1 - st->base;
+  int32_t real_end = ids_len - (layer + 1);  // row j embeds token j + layer + 1
+  if (real_end < 0) real_end = 0;
+  if (real_end > t + 1) real_end = t + 1;
+  if (real_end > st->committed) st->committed = real_end;
   return MTP_OK;
 }
 

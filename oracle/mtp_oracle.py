@@ -311,7 +311,7 @@ def verify_head(hidden_rows, norm_w, eps, lm_head, logit_multiplier=None, final_
 # ---------------------------------------------------------------------------
 
 def draft_layer(cfg, w, lm_head, k_cache, v_cache, hidden, embed_rows, pos0=None,
-                want_logits=True):
+                want_logits=True, pos_base=0):
     """One MTP draft-layer step over ``m`` rows.
 
     Follows [mimo_mtp.rs] module doc (the four-line layer statement) with
@@ -337,7 +337,11 @@ def draft_layer(cfg, w, lm_head, k_cache, v_cache, hidden, embed_rows, pos0=None
        ``forward_draft_with_hidden``).
 
     ``k_cache``/``v_cache`` are ``[nkv, cap, d]`` with rows ``< pos0``
-    filled; they are not modified (the appended rows are returned).
+    filled; they are not modified (the appended rows are returned).  Cache
+    row ``i`` holds position ``pos_base + i`` (a cache restarted part-way,
+    [mimo_mtp.rs] ``base``): new row ``r`` rotates at ``pos_base + pos0 +
+    r``; the causal mask and the window compare row indices, which differ
+    from positions by the same ``pos_base``.
     """
     eps = cfg.eps
     H, nh, nkv, dqk, dv = cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim_qk, cfg.head_dim_v
@@ -364,8 +368,8 @@ def draft_layer(cfg, w, lm_head, k_cache, v_cache, hidden, embed_rows, pos0=None
     if cfg.qk_norm:
         q = rmsnorm(q, w["q_norm"], eps)
         k = rmsnorm(k, w["k_norm"], eps)
-    q = np.stack([rope(q[r], L + r, cfg.rope_theta, cfg.rot_dim) for r in range(m)])
-    k = np.stack([rope(k[r], L + r, cfg.rope_theta, cfg.rot_dim) for r in range(m)])
+    q = np.stack([rope(q[r], pos_base + L + r, cfg.rope_theta, cfg.rot_dim) for r in range(m)])
+    k = np.stack([rope(k[r], pos_base + L + r, cfg.rope_theta, cfg.rot_dim) for r in range(m)])
     k_all = np.concatenate([np.asarray(k_cache, np.float64)[:, :L], k.transpose(1, 0, 2)], axis=1)
     v_all = np.concatenate([np.asarray(v_cache, np.float64)[:, :L], v.transpose(1, 0, 2)], axis=1)
     o = attention(q, k_all, v_all, [L + r for r in range(m)], cfg.window,
@@ -428,6 +432,35 @@ def kv_catch_up(cfg, w, embed_rows, target_hidden, pending_hidden=None, pos0=0):
     return k, v
 
 
+def draft_steps(cfg, w, lm_head, embed, k_cache, v_cache, hidden, token, cache_len, k_steps,
+                pos_base=0, forced=None):
+    """``k_steps`` chained one-row draft steps of one layer.
+
+    [mtp.rs] ``forward_draft_with_hidden``: a chained step reads the normed
+    row the shared head returns (after ``shared_head_norm``), "the only valid
+    input for a chained second MTP step", and the draft token of the step
+    before.  Step ``i`` appends its K/V row at cache row ``cache_len + i``
+    (position ``pos_base + cache_len + i``).  ``forced[i]``, when given,
+    replaces draft ``i`` as the next step's token (near-ties).  Returns the
+    steps' results; the caches are not modified.
+    """
+    kc = np.array(k_cache, dtype=np.float64, copy=True)
+    vc = np.array(v_cache, dtype=np.float64, copy=True)
+    h = np.asarray(hidden, dtype=np.float64).reshape(1, -1)
+    tok = int(token)
+    out = []
+    for i in range(k_steps):
+        L = cache_len + i
+        res = draft_layer(cfg, w, lm_head, kc, vc, h, embed(tok)[None], pos0=L, pos_base=pos_base)
+        kc[:, L] = res["k_new"][0]
+        vc[:, L] = res["v_new"][0]
+        res["token_in"] = tok
+        out.append(res)
+        tok = res["token"] if forced is None or forced[i] is None else int(forced[i])
+        h = res["hidden_out"][None]
+    return out
+
+
 def draft_chain(cfg, layers, lm_head, embed, caches, hidden, tokens, forced=None):
     """The three-layer chained draft of one speculative round.
 
@@ -456,6 +489,81 @@ def draft_chain(cfg, layers, lm_head, embed, caches, hidden, tokens, forced=None
 # ---------------------------------------------------------------------------
 # Speculation bookkeeping (host)
 # ---------------------------------------------------------------------------
+
+def mimo_layer_state_new():
+    """One draft layer's round state of [mimo_mtp.rs] ``MimoMtp``: rows at
+    positions below ``committed`` are final, ``base`` is the position of the
+    cache's first row, ``kv_len`` the rows the cache holds."""
+    return {"committed": 0, "base": 0, "kv_len": 0}
+
+
+def mimo_plan_layer(st, layer, t, hist_lo, hist_end, ids_len):
+    """First position the layer runs this round (rows ``start .. t``), or None.
+
+    [mimo_mtp.rs] ``mimo_mtp_draft`` for a round that starts after the
+    backbone processed position ``t``: nothing is drafted when the hidden
+    history ``[hist_lo, hist_end)`` lacks ``t`` or fewer than ``t + 2`` ids
+    are known.  A layer whose committed position lies below the history
+    (a gap) or beyond ``t + 1`` (stale) restarts its cache at ``hist_lo``;
+    then the rows of the previous round that were provisional (past
+    ``committed``) are dropped, and the layer runs positions
+    ``committed .. t``.
+    """
+    if hist_end <= hist_lo or t < hist_lo or t >= hist_end or ids_len < t + 2:
+        return None
+    if st["committed"] < hist_lo or st["committed"] > t + 1:
+        st["kv_len"] = 0
+        st["base"] = hist_lo
+        st["committed"] = hist_lo
+    keep = st["committed"] - st["base"]
+    if st["kv_len"] > keep:
+        st["kv_len"] = keep
+    return st["committed"]
+
+
+def mimo_commit_layer(st, layer, t, ids_len):
+    """After the layer ran positions ``start .. t`` ([mimo_mtp.rs]
+    ``mimo_mtp_draft``): the cache holds rows up to ``t``, and rows whose
+    token is known (row ``j`` embeds ``ids[j + layer + 1]``) are final."""
+    st["kv_len"] = t + 1 - st["base"]
+    real_end = min(t + 1, max(0, ids_len - (layer + 1)))
+    st["committed"] = max(st["committed"], real_end)
+    return st
+
+
+def mimo_draft_round(cfg, layers, lm_head, embed, caches, states, hist, hist_lo, hist_end, t, ids,
+                     k, forced=None):
+    """The draft half of one MiMo round ([mimo_mtp.rs] ``mimo_mtp_draft``).
+
+    Layer ``l`` runs positions ``start .. t`` (``mimo_plan_layer``): row ``j``
+    embeds ``ids[j + l + 1]`` (this round's earlier drafts past the known
+    ids) and reads the target hidden ``hist(j)``; only the last row reaches
+    the head and its argmax is draft ``l``.  ``caches[l]`` is ``[kc, vc]``
+    (arrays ``[nkv, cap, d]``, updated in place).  ``forced[l]`` replaces
+    draft ``l`` for the later layers (near-ties).  Returns the drafts and the
+    layers' results.
+    """
+    drafts, results = [], []
+    for layer in range(min(k, len(layers))):
+        st = states[layer]
+        start = mimo_plan_layer(st, layer, t, hist_lo, hist_end, len(ids))
+        if start is None:
+            return [], []
+        rows = list(range(start, t + 1))
+        toks = [ids[j + layer + 1] if j + layer + 1 < len(ids) else drafts[j + layer + 1 - len(ids)]
+                for j in rows]
+        e = np.stack([embed(tk) for tk in toks])
+        h = np.stack([hist(j) for j in rows])
+        kc, vc = caches[layer]
+        L = st["kv_len"]
+        res = draft_layer(cfg, layers[layer], lm_head, kc, vc, h, e, pos0=L, pos_base=st["base"])
+        kc[:, L:L + len(rows)] = res["k_new"].transpose(1, 0, 2)
+        vc[:, L:L + len(rows)] = res["v_new"].transpose(1, 0, 2)
+        mimo_commit_layer(st, layer, t, len(ids))
+        res["start"] = start
+        results.append(res)
+        drafts.append(res["token"] if forced is None or forced[layer] is None else int(forced[layer]))
+    return drafts, results
 
 def spec_accept(drafts, verify_tokens):
     """Accepted drafts of one round.

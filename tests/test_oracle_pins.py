@@ -558,6 +558,93 @@ def test_layer_head_norm_comes_before_rope():
         assert np.max(np.abs(np.subtract(norm_then_rope, rope_then_norm))) > 1e-3
 
 
+def test_draft_steps_feed_the_normed_hidden():
+    """[mtp.rs] forward_draft_with_hidden: the second step reads the first
+    step's row after the final norm (written out here), not its pre-norm
+    output, and embeds the first step's draft."""
+    cfg = _tiny_cfg(cache_len=4)
+    w = make_layer_weights(cfg)
+    assert np.ptp(np.asarray(w["final_norm"])) > 0.05          # a non-uniform final norm
+    sh = make_shared(cfg)
+    st = make_state(cfg.with_(m=3))
+    step = make_step(cfg)
+    embed = lambda t: sh["embed"][t]  # noqa: E731
+    res = O.draft_steps(cfg, w, sh["lm_head"], embed, st["k_cache"], st["v_cache"], step["hidden"][0],
+                        int(step["tokens"][0]), cfg.cache_len, 2)
+    u2 = res[0]["u2"][0]
+    ms = sum(float(v) * float(v) for v in u2) / len(u2)
+    y1 = [float(v) / math.sqrt(ms + cfg.eps) * float(g) for v, g in zip(u2, w["final_norm"])]
+    assert np.allclose(res[0]["hidden_out"], y1, rtol=1e-12, atol=1e-12)
+    assert res[1]["token_in"] == res[0]["token"]
+    tok1 = res[0]["token"]
+    cat = np.concatenate([O.rmsnorm(embed(tok1), w["enorm"], 1e-6), O.rmsnorm(np.array(y1), w["hnorm"], 1e-6)])
+    assert np.allclose(res[1]["u"][0], O.dequant(w["eh_proj"]) @ cat, rtol=1e-12, atol=1e-12)
+    cat_pre = np.concatenate([O.rmsnorm(embed(tok1), w["enorm"], 1e-6), O.rmsnorm(u2, w["hnorm"], 1e-6)])
+    assert np.max(np.abs(O.dequant(w["eh_proj"]) @ cat_pre - res[1]["u"][0])) > 1e-3
+    # the second step attends to the first step's appended row at cache row cache_len
+    k2 = O.draft_layer(cfg, w, sh["lm_head"], st["k_cache"], st["v_cache"], np.array(y1)[None],
+                       embed(tok1)[None], pos0=cfg.cache_len + 1, want_logits=False)
+    assert not np.allclose(k2["u1"], res[1]["u1"])             # without that row the output differs
+
+
+def test_mimo_plan_by_hand():
+    """[mimo_mtp.rs] mimo_mtp_draft: the rows each layer runs over two rounds,
+    a history gap, a stale state and rounds with nothing to draft."""
+    sts = [O.mimo_layer_state_new() for _ in range(3)]
+    # first round after a 6-token prompt: t = 5, ids x_0 .. x_6 known
+    for l, st in enumerate(sts):
+        assert O.mimo_plan_layer(st, l, 5, 0, 6, 7) == 0            # every layer runs 0 .. 5
+        O.mimo_commit_layer(st, l, 5, 7)
+    assert [st["committed"] for st in sts] == [6, 5, 4] and all(st["kv_len"] == 6 for st in sts)
+    # one draft accepted: t = 7, ids up to x_8
+    starts = []
+    for l, st in enumerate(sts):
+        starts.append(O.mimo_plan_layer(st, l, 7, 0, 8, 9))
+        assert st["kv_len"] == starts[-1]                            # provisional rows dropped
+        O.mimo_commit_layer(st, l, 7, 9)
+    assert starts == [6, 5, 4]                                        # 2, 3 and 4 rows
+    assert [st["committed"] for st in sts] == [8, 7, 6] and all(st["kv_len"] == 8 for st in sts)
+    # a history gap: the history restarts at 20
+    st = sts[0]
+    assert O.mimo_plan_layer(st, 0, 24, 20, 25, 26) == 20
+    assert (st["base"], st["kv_len"], st["committed"]) == (20, 0, 20)
+    O.mimo_commit_layer(st, 0, 24, 26)
+    assert (st["kv_len"], st["committed"]) == (5, 25)
+    # a stale state (committed past t + 1) restarts too
+    st2 = {"committed": 40, "base": 20, "kv_len": 21}
+    assert O.mimo_plan_layer(st2, 1, 30, 22, 31, 32) == 22 and st2 == {"committed": 22, "base": 22, "kv_len": 0}
+    # nothing to draft: t outside the history, or x_{t+1} unknown
+    st3 = O.mimo_layer_state_new()
+    assert O.mimo_plan_layer(st3, 0, 9, 0, 9, 11) is None
+    assert O.mimo_plan_layer(st3, 0, 5, 0, 9, 6) is None and st3 == O.mimo_layer_state_new()
+
+
+def test_mimo_first_round_equals_the_chain():
+    """The first round after a prompt runs every prompt row of every layer;
+    its drafts and rows equal the three-layer chain statement ("How the three
+    layers chain") with the prompt's rows as the chain's rows."""
+    cfg = _tiny_cfg(m=4, n_layers=3, window=3, sinks=True, qk_norm=False, head_dim_qk=48,
+                    head_dim_v=32, cache_len=0, rope_theta=1e4)
+    layers = [make_layer_weights(cfg, k) for k in range(3)]
+    sh = make_shared(cfg)
+    embed = lambda t: sh["embed"][t]  # noqa: E731
+    rng = np.random.default_rng(31)
+    P = cfg.m
+    ids = rng.integers(0, cfg.vocab, P + 1).tolist()               # x_0 .. x_P (x_P pending)
+    hid = rng.standard_normal((P, cfg.hidden))
+    ref = O.draft_chain(cfg, layers, sh["lm_head"], embed,
+                        [(np.zeros((cfg.n_kv_heads, P, 48)), np.zeros((cfg.n_kv_heads, P, 32)))] * 3,
+                        hid, ids[1:])
+    caches = [[np.zeros((cfg.n_kv_heads, P, 48)), np.zeros((cfg.n_kv_heads, P, 32))] for _ in range(3)]
+    states = [O.mimo_layer_state_new() for _ in range(3)]
+    drafts, res = O.mimo_draft_round(cfg, layers, sh["lm_head"], embed, caches, states,
+                                     lambda j: hid[j], 0, P, P - 1, ids, 3)
+    assert drafts == [r["token"] for r in ref]
+    for l in range(3):
+        assert np.allclose(res[l]["u2"], ref[l]["u2"], rtol=1e-12, atol=1e-12)
+        assert np.allclose(caches[l][0].transpose(1, 0, 2), ref[l]["k_new"], rtol=1e-12, atol=1e-12)
+
+
 def test_chain_rows_take_earlier_drafts():
     cfg = _tiny_cfg(m=4, n_layers=3, window=3, sinks=True, qk_norm=False, head_dim_qk=48,
                     cache_len=6, name="tiny_chain")

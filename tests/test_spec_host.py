@@ -77,3 +77,29 @@ def test_bad_rounds_are_rejected_unchanged(M):
     assert load().mtp_spec_accept(None, None, 17) == -1
     with pytest.raises(MtpError):
         M.mtp_spec_rewind([1, 2], -1)
+
+
+def test_mimo_plan_commit_match_oracle(M):
+    """Per-layer round state over random rounds, gaps and stale states."""
+    rng = np.random.default_rng(14)
+    for trial in range(40):
+        layers = int(rng.integers(1, 5))
+        c = [M.MimoLayerState() for _ in range(layers)]
+        r = [O.mimo_layer_state_new() for _ in range(layers)]
+        t, lo = int(rng.integers(0, 30)), 0
+        for _ in range(30):
+            if rng.random() < 0.1:                     # the history restarts part-way
+                lo = int(rng.integers(max(0, t - 5), t + 1))
+            hist_end = t + 1 if rng.random() < 0.9 else t  # sometimes lacks t
+            ids_len = t + 2 if rng.random() < 0.95 else t + 1
+            for l in range(layers):
+                n, start = M.mtp_mimo_plan_layer(c[l], l, t, lo, hist_end, ids_len)
+                ref = O.mimo_plan_layer(r[l], l, t, lo, hist_end, ids_len)
+                assert (n > 0) == (ref is not None)
+                if ref is not None:
+                    assert start == ref and n == t + 1 - ref
+                    M.mtp_mimo_commit_layer(c[l], l, t, ids_len)
+                    O.mimo_commit_layer(r[l], l, t, ids_len)
+                assert (c[l].committed, c[l].base, c[l].kv_len) == (r[l]["committed"], r[l]["base"],
+                                                                    r[l]["kv_len"])
+            t += int(rng.integers(1, 5))
