@@ -5,7 +5,8 @@
   src/inference/models/qwen35/mtp.rs", forward_draft_with_hidden).
 * mtp_mimo_draft_round in a speculative loop driven by a CPU fake verifier
   (a fixed accept pattern): per-layer committed/base state, provisional rows
-  dropped each round, a history gap that restarts every layer's cache, the
+  dropped each round, a history gap that restarts the caches of the layers
+  whose committed rows fell out of the history, the
   accepted prefix and the generation's counters ("cortiq-engine 0.8.49
   src/mimo_mtp.rs", mimo_mtp_draft and mimo_spec_round).
 """
@@ -59,10 +60,23 @@ def test_draft_steps_match_oracle_self_chain(dev, name, k):
     assert mtp_workspace_status(lyr.ws) == 0
     drafts = tokens.cpu().numpy()[1:].tolist()
     embed = lambda t: shared["embed"][t]  # noqa: E731
-    ref = O.draft_steps(cfg, w, shared["lm_head"], embed, st["k_cache"], st["v_cache"],
-                        step["hidden"][0], int(step["tokens"][0]), cfg.cache_len, k, forced=drafts)
     kc, vc = lyr.k_cache.cpu().numpy(), lyr.v_cache.cpu().numpy()
     vals, hs = values.cpu().numpy(), hout.cpu().numpy()
+    # each step against the oracle on the inputs the device step had: the
+    # previous step's normed row and draft, and the cache rows the earlier
+    # steps appended (so rounding does not compound along the chain); a
+    # wrongly wired hidden or token shows up as a mismatch of that step
+    toks = [int(step["tokens"][0])] + drafts
+    ref = []
+    for i in range(k):
+        h_in = step["hidden"][0] if i == 0 else hs[i - 1]
+        ref.append(O.draft_layer(cfg, w, shared["lm_head"], kc, vc, h_in[None], embed(toks[i])[None],
+                                 pos0=cfg.cache_len + i))
+    # the chain wiring itself: the oracle's free-running chain drafts the same tokens
+    free = O.draft_steps(cfg, w, shared["lm_head"], embed, st["k_cache"], st["v_cache"],
+                         step["hidden"][0], toks[0], cfg.cache_len, k, forced=drafts)
+    for i, r in enumerate(free):
+        assert_token(drafts[i], r["token"], r["margin"], f"{name} free chain step {i}")
     for i, r in enumerate(ref):
         assert_token(drafts[i], r["token"], r["margin"], f"{name} step {i}")
         assert_close(hs[i], r["hidden_out"], f"{name} step {i} hidden_out")
@@ -120,9 +134,12 @@ def test_mimo_rounds_with_a_fake_verifier(dev):
     ostats = O.spec_stats_new()
     accept = [0, 3, 1, 2, 3, 0, 1, 2]
     t, lo, hist_end = P - 1, 0, P
+    restarted = []
     for rnd, a_want in enumerate(accept):
         if rnd == 4:
             lo = t - 2                      # a history gap: only positions t-2 .. t remain
+            restarted = [l for l in range(K) if ostates[l]["committed"] < lo]
+            assert restarted                # (layers whose committed rows fell out restart)
         hist_ptr = d_hist[lo:]
         n = mtp_mimo_draft_round([lyr.desc for lyr in layers], states, hist_ptr, lo, hist_end, t,
                                  d_ids, len(ids), values, ws, catch_ws)
@@ -141,7 +158,8 @@ def test_mimo_rounds_with_a_fake_verifier(dev):
             assert (states[l].committed, states[l].base, states[l].kv_len) == (
                 ostates[l]["committed"], ostates[l]["base"], ostates[l]["kv_len"]), f"round {rnd} layer {l}"
         if rnd == 4:
-            assert all(states[l].base == lo for l in range(K))          # every cache restarted
+            assert all(states[l].base == lo for l in restarted)
+            assert all(states[l].base == 0 for l in range(K) if l not in restarted)
         # the fake verifier agrees with the first a_want drafts, then differs
         a_want = min(a_want, n)
         bonus = (drafts[a_want] + 7919) % V if a_want < n else int(rng.integers(0, V))
