@@ -53,6 +53,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default=WORKLOAD, choices=CONFIG_CHOICES)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--bf16-stacks", action="store_true",
+                    help="MoE workload: expert stacks with bfloat16 scales and biases")
     ap.add_argument("--seq", type=int, default=512, help="rows of the catch-up batch (--profile-kernel catch_up)")
     ap.add_argument("--profile-kernel", default=None,
                     choices=["lm_head", "ffn_down", "attention", "verify_head", "step", "catch_up"],
@@ -71,7 +73,12 @@ def attn_keys(cfg):
     return cached + cfg.m
 
 
-def launch_plan(cfg):
+def aff_bf16(n, k):
+    """An expert stack with bfloat16 scales and biases: 0.625 B per element."""
+    return n * k // 2 + 2 * 2 * n * (k // 32)
+
+
+def launch_plan(cfg, bf16_stacks=False):
     """(name, algorithmic HBM bytes) of each launch of one draft step, in the
     order the library enqueues them (weights at 0.75 B per element, the KV
     rows the attention reads, the activation rows read from memory)."""
@@ -84,10 +91,11 @@ def launch_plan(cfg):
     lm = aff(cfg.vocab, H) + 4 * H
     if cfg.moe:
         E, Ie, k = cfg.n_experts, cfg.expert_intermediate, cfg.top_k
+        ea = aff_bf16 if bf16_stacks else aff   # routed stacks; the shared expert is float32
         return [("launch A: embedding pack + eh_proj + q/k/v", eh + qkv), ("attention", attn),
                 ("o_proj", o), ("router", 4 * E * H),
-                ("expert gate/up", (k + 1) * 2 * aff(Ie, H)),
-                ("expert down", (k + 1) * aff(H, Ie)), ("final norm", 4 * H),
+                ("expert gate/up", k * 2 * ea(Ie, H) + 2 * aff(Ie, H)),
+                ("expert down", k * ea(H, Ie) + aff(H, Ie)), ("final norm", 4 * H),
                 ("lm_head + argmax", lm)]
     I = cfg.intermediate
     gu, dn = 2 * aff(I, H), aff(H, I)
@@ -102,8 +110,8 @@ def launch_plan(cfg):
             ("lm_head + argmax", lm)]
 
 
-def step_bytes(cfg):
-    return sum(b for _, b in launch_plan(cfg)) * max(1, cfg.n_layers)
+def step_bytes(cfg, bf16_stacks=False):
+    return sum(b for _, b in launch_plan(cfg, bf16_stacks)) * max(1, cfg.n_layers)
 
 
 # --------------------------------------------------------------- clocks
@@ -469,7 +477,8 @@ def run_layer_bench(args, cfg):
     sh = SharedHead(shared, dev)
     ws_l = [make_layer_weights(cfg, k) for k in range(nl)]
     sts = [make_state(cfg, k) for k in range(nl)]
-    layers = [DraftLayer(cfg, ws_l[k], sh, sts[k], device=dev) for k in range(nl)]
+    bfs = bool(args.bf16_stacks and cfg.moe)
+    layers = [DraftLayer(cfg, ws_l[k], sh, sts[k], device=dev, bf16_stacks=bfs) for k in range(nl)]
     hidden = torch.from_numpy(step["hidden"]).to(dev)
     tokens = torch.from_numpy(step["tokens"]).to(dev)
     tok = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -497,7 +506,7 @@ def run_layer_bench(args, cfg):
     value = nl * job_value(world, args.steps, ms_total)   # draft tokens (one per layer step)
 
     # each launch alone (eager, same inputs)
-    plan = launch_plan(cfg) * nl
+    plan = launch_plan(cfg, bfs) * nl
     with torch.cuda.stream(stream):
         launch_ms, n_launch = timed_launches(fwd, len(plan) + 1, max(5, min(args.steps, 50)), flush)
     stream.synchronize()
@@ -509,7 +518,7 @@ def run_layer_bench(args, cfg):
         launch_ms = [sum(launch_ms[i + k * per] for k in range(nl)) / nl for i in range(per)]
         plan = plan[:per]
     roof, rows = roofline_of(plan, launch_ms, peak, peak_kind, traffic_key=f"{cfg.name}.dominant")
-    total_bytes = step_bytes(cfg)
+    total_bytes = step_bytes(cfg, bfs)
 
     # end to end through the C ABI with pinned host buffers
     h_hidden = torch.from_numpy(step["hidden"]).pin_memory()
@@ -550,6 +559,7 @@ def run_layer_bench(args, cfg):
                    "head_dim_v": cfg.head_dim_v, "intermediate": cfg.intermediate,
                    "vocab": cfg.vocab, "cache_len": cfg.cache_len, "window": cfg.window,
                    "gated_q": cfg.gated_q, "experts": cfg.n_experts, "top_k": cfg.top_k,
+                   "expert_scales": ("bfloat16" if bfs else "float32") if cfg.moe else None,
                    "weights": "affine 4-bit g32", "l2": l2,
                    "timing": ("CUDA graph of one step, replayed; CUDA events on the launch "
                               "stream" + ("; each step between its own events" if flush else "")),

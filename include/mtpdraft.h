@@ -266,7 +266,8 @@ mtp_status verify_head_argmax(const float *d_h, int32_t rows, const float *d_nor
  * sigmoid-gated shared expert).  "hf2q 0.1.13 ... mtp.rs" MtpFfnWeightsGpu::Moe
  * (router, stacked expert gate/up/down, four shared-expert tensors) and
  * "hf2q 0.1.1 ... forward_mlx_shared.rs" MlxAffineMoeStack (expert e of a
- * stack is slab e of [E][N][K/8]; here with float32 scales and biases).
+ * stack is slab e of [E][N][K/8]; scales and biases float32, or bfloat16 as
+ * the page's stacks store them).
  * ------------------------------------------------------------------------ */
 typedef struct {
     int32_t n_experts;        /* <= 1024 */
@@ -279,6 +280,12 @@ typedef struct {
     mtp_affine4 exp_down;     /* stacked: n = n_experts*hidden, k = expert_inter */
     mtp_affine4 sh_gate, sh_up, sh_down;
     const float *sh_gate_inp; /* [hidden]: shared expert gate = sigmoid(sh_gate_inp . f) */
+    int32_t scales_bf16;      /* 1: the stacks exp_gate/exp_up/exp_down hold their scales and
+                                 biases as bfloat16 [n][k/32] ("hf2q 0.1.1 ...
+                                 forward_mlx_shared.rs", MlxAffineMoeStack; their s and b
+                                 pointers then point at bfloat16 data); needs hidden and
+                                 expert_inter multiples of 256.  0: float32.  The shared
+                                 expert's are float32 either way. */
 } mtp_moe_weights;
 
 /* u2 = u1 + MoE(RMSNorm(u1)*post_norm) for one row (m = 1).

@@ -38,7 +38,7 @@ class MoeWeights(C.Structure):
     _fields_ = [("n_experts", i32), ("top_k", i32), ("expert_inter", i32), ("shared_inter", i32),
                 ("router", vp), ("exp_gate", Affine4), ("exp_up", Affine4), ("exp_down", Affine4),
                 ("sh_gate", Affine4), ("sh_up", Affine4), ("sh_down", Affine4),
-                ("sh_gate_inp", vp)]
+                ("sh_gate_inp", vp), ("scales_bf16", i32)]
 
 
 class LayerDesc(C.Structure):

@@ -43,9 +43,17 @@ def attn_geom(n_heads, n_kv_heads, head_dim_qk, head_dim_v, rot_dim=None, window
 
 
 def moe_weights(n_experts, top_k, expert_inter, shared_inter, router, exp_gate, exp_up, exp_down,
-                sh_gate, sh_up, sh_down, sh_gate_inp) -> MoeWeights:
+                sh_gate, sh_up, sh_down, sh_gate_inp, scales_bf16=False) -> MoeWeights:
     return MoeWeights(n_experts, top_k, expert_inter, shared_inter, _p(router), exp_gate, exp_up,
-                      exp_down, sh_gate, sh_up, sh_down, _p(sh_gate_inp))
+                      exp_down, sh_gate, sh_up, sh_down, _p(sh_gate_inp), int(bool(scales_bf16)))
+
+
+def affine4_bf16_scales(q: torch.Tensor, s: torch.Tensor, b: torch.Tensor) -> Affine4:
+    """Descriptor of an expert stack with bfloat16 scales and biases (``s``/``b``
+    bfloat16 device tensors ``[n, k/32]``); only MoE stacks take it."""
+    if q.dtype not in (torch.int32, torch.uint32) or s.dtype != torch.bfloat16 or b.dtype != torch.bfloat16:
+        raise TypeError("codes must be int32/uint32, scales and biases bfloat16")
+    return Affine4(_p(q), _p(s), _p(b), int(q.shape[0]), int(q.shape[-1] * 8))
 
 
 def workspace(nbytes: int, device="cuda", stream=None) -> torch.Tensor:

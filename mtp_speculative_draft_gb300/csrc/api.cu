@@ -61,12 +61,14 @@ mtp_status check_affine(const mtp_affine4* w, int n, int k, const char* name, bo
 
 // Tensor maps are pure functions of (pointer, shape); cache them so a warm
 // call encodes nothing.
-static mtp_status qmat_cached(QMat* out, const mtp_affine4& w, const char* name) {
+static mtp_status qmat_cached(QMat* out, const mtp_affine4& w, const char* name,
+                              bool sb_bf16 = false) {
   static std::mutex mu;
-  static std::map<std::tuple<const void*, const void*, const void*, int, int, int>, QMat> cache;
+  static std::map<std::tuple<const void*, const void*, const void*, int, int, int, bool>, QMat> cache;
   int dev = 0;
   cudaGetDevice(&dev);
-  auto key = std::make_tuple((const void*)w.q, (const void*)w.s, (const void*)w.b, w.n, w.k, dev);
+  auto key = std::make_tuple((const void*)w.q, (const void*)w.s, (const void*)w.b, w.n, w.k, dev,
+                             sb_bf16);
   {
     std::lock_guard<std::mutex> lk(mu);
     auto it = cache.find(key);
@@ -75,7 +77,7 @@ static mtp_status qmat_cached(QMat* out, const mtp_affine4& w, const char* name)
       return MTP_OK;
     }
   }
-  mtp_status st = encode_qmat(out, w, name);
+  mtp_status st = encode_qmat(out, w, name, sb_bf16);
   if (st != MTP_OK) return st;
   std::lock_guard<std::mutex> lk(mu);
   if (cache.size() > 4096) cache.clear();
@@ -562,6 +564,10 @@ static mtp_status check_moe(const mtp_moe_weights* w, int H) {
   if ((s = check_affine(&w->sh_up, I, H, "sh_up", true)) != MTP_OK) return s;
   if ((s = check_affine(&w->sh_down, H, I, "sh_down", true)) != MTP_OK) return s;
   if (!w->sh_gate_inp) return fail(MTP_ERR_INVALID_ARG, "moe: null sh_gate_inp");
+  if (w->scales_bf16 != 0 && w->scales_bf16 != 1)
+    return fail(MTP_ERR_INVALID_ARG, "moe: scales_bf16 must be 0 or 1");
+  if (w->scales_bf16 && (H % 256 || I % 256))
+    return fail(MTP_ERR_UNSUPPORTED, "moe: bfloat16 stacks need hidden and expert_inter multiples of 256");
   if (!aligned16(w->router)) return fail(MTP_ERR_INVALID_ARG, "moe: router must be 16-byte aligned");
   return MTP_OK;
 }
@@ -616,8 +622,10 @@ static mtp_status enqueue_moe(const mtp_moe_weights* w, const float* u1, const f
   // routed + shared expert gate/up with SwiGLU, scaled by the routing weights
   GemvParams p = {};
   mtp_status s;
-  if ((s = qmat_cached(&p.mat[0], w->exp_gate, "exp_gate")) != MTP_OK) return s;
-  if ((s = qmat_cached(&p.mat[1], w->exp_up, "exp_up")) != MTP_OK) return s;
+  const bool bf = w->scales_bf16 != 0;
+  if ((s = qmat_cached(&p.mat[0], w->exp_gate, "exp_gate", bf)) != MTP_OK) return s;
+  if ((s = qmat_cached(&p.mat[1], w->exp_up, "exp_up", bf)) != MTP_OK) return s;
+  p.sbf_mask = bf ? 0x3 : 0;  // routed stacks in slots 0 and 1, the shared expert f32
   if ((s = qmat_cached(&p.mat[2], w->sh_gate, "sh_gate")) != MTP_OK) return s;
   if ((s = qmat_cached(&p.mat[3], w->sh_up, "sh_up")) != MTP_OK) return s;
   p.xp = sc.xp_f;
@@ -646,7 +654,8 @@ static mtp_status enqueue_moe(const mtp_moe_weights* w, const float* u1, const f
 
   // down projections over the concatenated expert activations, + residual
   GemvParams d = {};
-  if ((s = qmat_cached(&d.mat[0], w->exp_down, "exp_down")) != MTP_OK) return s;
+  if ((s = qmat_cached(&d.mat[0], w->exp_down, "exp_down", bf)) != MTP_OK) return s;
+  d.sbf_mask = bf ? 0x1 : 0;
   if ((s = qmat_cached(&d.mat[1], w->sh_down, "sh_down")) != MTP_OK) return s;
   d.xp = sc.xp_h;
   d.xs = sc.xs_h;

@@ -168,11 +168,12 @@ static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
   return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
-                             const GemvScratch& sc, int* err, cudaStream_t st,
-                             const PreParams* pre) {
+template <bool SBF>
+static cudaError_t launch_gemv_rows_t(GemvParams* ph, const int* tiles, int nphase,
+                                      const GemvScratch& sc, int* err, cudaStream_t st,
+                                      const PreParams* pre) {
   constexpr int S = MTP_GEMV_STAGES;
-  auto kern = gemv_row_kernel<S>;
+  auto kern = gemv_row_kernel<S, SBF>;
   const int smem = kGemvWarps * S * (kRowCode + kRowRest) + 2048;  // + barriers, alignment
   static_assert(sizeof(StreamParams) <= 32764, "kernel parameters fit the 32 KB limit");
   if (nphase < 1 || nphase > kMaxPhases) return cudaErrorInvalidValue;
@@ -236,6 +237,15 @@ cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
   cfg.numAttrs = 1;
   launch_mark(cfg.stream);
   return cudaLaunchKernelEx(&cfg, kern, sp);
+}
+
+cudaError_t launch_gemv_rows(GemvParams* ph, const int* tiles, int nphase,
+                             const GemvScratch& sc, int* err, cudaStream_t st,
+                             const PreParams* pre) {
+  bool sbf = false;
+  for (int q = 0; q < nphase && q < kMaxPhases; ++q) sbf = sbf || ph[q].sbf_mask != 0;
+  return sbf ? launch_gemv_rows_t<true>(ph, tiles, nphase, sc, err, st, pre)
+             : launch_gemv_rows_t<false>(ph, tiles, nphase, sc, err, st, pre);
 }
 
 cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
@@ -402,16 +412,16 @@ cudaError_t encode_bf16_rows_map(CUtensorMap* out, const void* base, uint64_t ro
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-mtp_status encode_qmat(QMat* out, const mtp_affine4& w, const char* name) {
+mtp_status encode_qmat(QMat* out, const mtp_affine4& w, const char* name, bool sb_bf16) {
   const uint64_t kw = (uint64_t)w.k / 8, kg = (uint64_t)w.k / kGroup;
   CUresult r = encode2d(&out->q, CU_TENSOR_MAP_DATA_TYPE_UINT32, w.q, kw, (uint64_t)w.n, kw * 4,
                         32, 32, CU_TENSOR_MAP_SWIZZLE_128B);
+  const CUtensorMapDataType sdt = sb_bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32;
+  const uint64_t esz = sb_bf16 ? 2 : 4;
   if (r == CUDA_SUCCESS)
-    r = encode2d(&out->s, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w.s, kg, (uint64_t)w.n, kg * 4, 8, 32,
-                 CU_TENSOR_MAP_SWIZZLE_NONE);
+    r = encode2d(&out->s, sdt, w.s, kg, (uint64_t)w.n, kg * esz, 8, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (r == CUDA_SUCCESS)
-    r = encode2d(&out->b, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, w.b, kg, (uint64_t)w.n, kg * 4, 8, 32,
-                 CU_TENSOR_MAP_SWIZZLE_NONE);
+    r = encode2d(&out->b, sdt, w.b, kg, (uint64_t)w.n, kg * esz, 8, 32, CU_TENSOR_MAP_SWIZZLE_NONE);
   if (r != CUDA_SUCCESS)
     return fail(MTP_ERR_CUDA, std::string("tensor map encoding failed for ") + name +
                                   " (CUresult " + std::to_string((int)r) + ")");

@@ -128,6 +128,7 @@ struct GemvParams {
   const float* segw;     // routed weights (device), or null
   int rowsel_after_wait; // 1: rowsel is produced by the previous kernel
   int epi;               // one-row kernel: kEpiStore / kEpiSwiglu / kEpiArgmax
+  int sbf_mask;          // one-row kernel: bit i set when slot i's scales/biases are bfloat16
   int um;                // one-row kernel: 2 when gate (mat) and up (mat + 1) are separate units
   int wq;                // one-row kernel: warps gw < wq take units gw, gw + wq, ... (same count each)
   // K-segment mode (MoE down projection): K = nkseg * kseg_len
@@ -981,6 +982,17 @@ constexpr unsigned kPhaseSpinLimit = 4u << 20;  // polls of >= 256 ns each befor
 constexpr int kRowCode = 4096;
 constexpr int kRowRest = 2048 + 1152;  // scales, biases, activations (128-byte multiple)
 constexpr int kRowStageTx = kStageMatBytes + 8 * (128 + 8);
+// with bfloat16 scales and biases: 512-byte tiles in the same places
+constexpr int kRowStageTxBf16 = kStageMatBytes - 1024 + 8 * (128 + 8);
+
+// Matrix slot a stage of the cursor reads (its scale type lives per slot).
+__device__ __forceinline__ int stage_slot(const GemvParams& p, const Cursor& c) {
+  if (p.kseg_len > 0 && p.kseg_last_mat >= 0) {
+    const int spk = p.kseg_len / (8 * kGroup);
+    if (c.ks / spk >= p.nkseg - 1) return p.kseg_last_mat;
+  }
+  return c.mat;
+}
 
 // Waits until *cnt >= target (acquire); false when the wait gives up.
 // Every warp of a launch polls the same counter: sleeps of 512 ns keep the
@@ -1055,7 +1067,9 @@ __device__ __forceinline__ float sum_rows(const float* src, int n) {
   return t;
 }
 
-template <int S>
+// SBF: some slot of the launch has bfloat16 scales and biases (the
+// MlxAffineMoeStack layout); the all-f32 instantiation has no per-stage test.
+template <int S, bool SBF>
 __global__ void __launch_bounds__(kGemvWarps * 32, 3)
     gemv_row_kernel(const __grid_constant__ StreamParams sp) {
   extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -1090,7 +1104,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
     c.c.coords(p, mat, row, kx, sx);
     uint8_t* cd = code_base + slot * kRowCode;
     uint8_t* rs = rest_base + slot * kRowRest;
-    mbar_arrive_expect_tx(&bars[slot], (uint32_t)kRowStageTx);
+    const bool bf = SBF && ((p.sbf_mask >> mat) & 1);
+    mbar_arrive_expect_tx(&bars[slot], (uint32_t)(bf ? kRowStageTxBf16 : kRowStageTx));
     const QMat& mt = p.mat[mat];
     tma_load_2d(cd, &mt.q, &bars[slot], kx, row, pol_w);
     tma_load_2d(rs, &mt.s, &bars[slot], sx, row, pol_w);
@@ -1243,6 +1258,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       break;
     }
     {
+      const bool stage_bf = SBF && ((sp.ph[cc.ph].sbf_mask >> stage_slot(sp.ph[cc.ph], cc.c)) & 1);
       const uint8_t* ct = code_base + slot * kRowCode;
       const uint8_t* rs = rest_base + slot * kRowRest;
       const uint4* xps = reinterpret_cast<const uint4*>(rs + 2048);
@@ -1263,11 +1279,21 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
           Wc[0][st] = *reinterpret_cast<const uint4*>(rp + a_chunk[st]);
           Wc[1][st] = *reinterpret_cast<const uint4*>(rp + 1024 + a_chunk[st]);
         }
-        const float* sr = reinterpret_cast<const float*>(rs) + (rt * 16 + gid) * 8 + 2 * tq;
-        const float2 s0 = *reinterpret_cast<const float2*>(sr);
-        const float2 s1 = *reinterpret_cast<const float2*>(sr + 64);
-        const float2 b0 = *reinterpret_cast<const float2*>(sr + 256);
-        const float2 b1 = *reinterpret_cast<const float2*>(sr + 256 + 64);
+        float2 s0, s1, b0, b1;
+        if (SBF && stage_bf) {  // [32 rows][8 groups] bfloat16, biases 1 KB further
+          const __nv_bfloat16* sh = reinterpret_cast<const __nv_bfloat16*>(rs) +
+                                    (rt * 16 + gid) * 8 + 2 * tq;
+          s0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sh));
+          s1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sh + 64));
+          b0 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sh + 512));
+          b1 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(sh + 512 + 64));
+        } else {
+          const float* sr = reinterpret_cast<const float*>(rs) + (rt * 16 + gid) * 8 + 2 * tq;
+          s0 = *reinterpret_cast<const float2*>(sr);
+          s1 = *reinterpret_cast<const float2*>(sr + 64);
+          b0 = *reinterpret_cast<const float2*>(sr + 256);
+          b1 = *reinterpret_cast<const float2*>(sr + 256 + 64);
+        }
         float d[2][4];
 #pragma unroll
         for (int st = 0; st < 2; ++st) {

@@ -25,7 +25,9 @@ void launch_mark(cudaStream_t st);
 int sm_count();
 
 // Encodes the three tensor maps of an affine weight viewed as [rows][k].
-mtp_status encode_qmat(QMat* out, const mtp_affine4& w, const char* name);
+// With sb_bf16 the scales and biases are bfloat16 [rows][k/32] (rows of 2k/32
+// bytes, a multiple of 16 when k % 256 == 0).
+mtp_status encode_qmat(QMat* out, const mtp_affine4& w, const char* name, bool sb_bf16 = false);
 
 // Checks an affine weight descriptor: non-null, aligned, positive sizes,
 // k % 32 == 0, and (when `need_tma`) k % 128 == 0 so the scale rows are

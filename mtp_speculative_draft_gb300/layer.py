@@ -43,7 +43,7 @@ class SharedHead:
 
 class DraftLayer:
     def __init__(self, cfg, weights: dict, shared: SharedHead, state: dict, m_max: int | None = None,
-                 device="cuda"):
+                 device="cuda", bf16_stacks: bool = False):
         self.cfg = cfg
         self.device = device
         self.m_max = cfg.m if m_max is None else m_max
@@ -70,15 +70,26 @@ class DraftLayer:
             E, Ie = cfg.n_experts, cfg.expert_intermediate
             for name in ("exp_gate", "exp_up", "exp_down"):
                 q, s, b = weights[name]
-                self.aff[name] = DeviceAffine((q.reshape(-1, q.shape[-1]), s.reshape(-1, s.shape[-1]),
-                                               b.reshape(-1, b.shape[-1])), device)
+                flat = (q.reshape(-1, q.shape[-1]), s.reshape(-1, s.shape[-1]), b.reshape(-1, b.shape[-1]))
+                if bf16_stacks:
+                    # the stacks as MlxAffineMoeStack holds them: float32 scales and
+                    # biases cast to bfloat16 (round to nearest even) at upload
+                    from .api import affine4_bf16_scales
+                    d = DeviceAffine.__new__(DeviceAffine)
+                    d.q = _dev(flat[0], device)
+                    d.s = torch.from_numpy(np.ascontiguousarray(flat[1])).to(torch.bfloat16).to(device)
+                    d.b = torch.from_numpy(np.ascontiguousarray(flat[2])).to(torch.bfloat16).to(device)
+                    d.desc = affine4_bf16_scales(d.q, d.s, d.b)
+                    self.aff[name] = d
+                else:
+                    self.aff[name] = DeviceAffine(flat, device)
             self.t["router"] = _dev(weights["router"], device)
             self.t["sh_gate_inp"] = _dev(weights["sh_gate_inp"], device)
             self.moe = moe_weights(E, cfg.top_k, Ie, cfg.shared_intermediate, self.t["router"],
                                    self.aff["exp_gate"].desc, self.aff["exp_up"].desc,
                                    self.aff["exp_down"].desc, self.aff["sh_gate"].desc,
                                    self.aff["sh_up"].desc, self.aff["sh_down"].desc,
-                                   self.t["sh_gate_inp"])
+                                   self.t["sh_gate_inp"], scales_bf16=bf16_stacks)
         g = attn_geom(cfg.n_heads, cfg.n_kv_heads, cfg.head_dim_qk, cfg.head_dim_v, cfg.rot_dim,
                       cfg.window, cfg.gated_q, cfg.eps)
         d = L.LayerDesc()
