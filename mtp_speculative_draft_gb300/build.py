@@ -30,6 +30,8 @@ def _flags():
     flags = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC"]
     if os.environ.get("MTP_PTXAS_VERBOSE"):
         flags += ["-Xptxas", "-v"]
+    # extra nvcc flags, e.g. -D overrides of the kernels' compile-time tuning knobs
+    flags += os.environ.get("MTP_NVCC_EXTRA", "").split()
     return flags
 
 

@@ -181,7 +181,11 @@ __device__ __forceinline__ float warp_col_sum(const float* part, int n, int m, i
 }
 
 constexpr int kStageMatBytes = 6144;  // 4 KB codes + 1 KB scales + 1 KB biases
-constexpr int kGemvWarps = 4;
+// Warps per GEMV CTA (compile-time tuning knob).
+#ifndef MTP_GEMV_WARPS
+#define MTP_GEMV_WARPS 4
+#endif
+constexpr int kGemvWarps = MTP_GEMV_WARPS;
 constexpr int kXChunk = 1088;         // staged activations per column: 8 groups x (128 + 8) bytes
 
 // Bytes of staged activations per stage, padded so every tensor-map
