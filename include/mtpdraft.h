@@ -125,6 +125,13 @@ mtp_status mtp_timing_end(int32_t *n_recorded);
  *   W->k must equal K and be a multiple of 32.
  *   d_ws: workspace of qmatmul_affine4_workspace_bytes(m, K) bytes; it holds
  *         the activations in the tensor-core operand layout.
+ * Activation range (this call and every projection of the draft step): the
+ * tensor-core path splits each activation into f16 high and low parts.  A
+ * 32-value group whose largest |x| reaches 2^15 is stored times a power of
+ * two 2^-e (its largest value then lies in [2^14, 2^15)) and its weight
+ * scales are multiplied back by 2^e, so every finite activation is accepted;
+ * within such a group, values more than about 2^-100 times its largest may
+ * flush to zero.  Inf and NaN propagate to the outputs.
  * ------------------------------------------------------------------------ */
 size_t qmatmul_affine4_workspace_bytes(int32_t m, int32_t k);
 mtp_status qmatmul_affine4(const float *d_x, const mtp_affine4 *W, float *d_y, int32_t m,

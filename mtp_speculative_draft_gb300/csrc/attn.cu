@@ -508,36 +508,34 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   const int noct = nit / 2;
   for (int o0 = 0; o0 < noct; o0 += nthreads) {
     const int oi = o0 + tid;
-    float2 sum = make_float2(0.f, 0.f);
+    const bool valid = oi < noct;
     int r = 0, k = 0;
-    if (oi < noct) {
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (valid) {
       const int gg = g0 + oi / 4;
       const int qi = gg / gpq;
       r = qi / G;
       const int h = kvh * G + qi % G;
       k = h * dv + (gg - qi * gpq) * kGroup + (oi & 3) * 8;
       const float4 v0 = fsm[2 * oi], v1 = fsm[2 * oi + 1];
-      float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+      v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+      v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
       if (a.out) {
         float4* dst = reinterpret_cast<float4*>(a.out + (size_t)r * a.nh * dv + k);
         dst[0] = v0;
         dst[1] = v1;
       }
-      if (a.out_xp) {
-        uint4 hi, lo;
-        sum = pack8(v, hi, lo);
-        const int g = k / kGroup, t = (k % kGroup) / 8;
-        a.out_xp[xp_index(g, r, t, 0, a.m)] = hi;
-        a.out_xp[xp_index(g, r, t, 1, a.m)] = lo;
-      }
     }
     if (a.out_xp) {
       // the four octets of a group are adjacent lanes (groups start at multiples of 4)
-      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 1);
-      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
-      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
-      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 2);
-      if (oi < noct && (oi & 3) == 0) a.out_xs[(k / kGroup) * a.m + r] = sum;
+      uint4 hi, lo;
+      const float2 gx = pack8_group(v, valid, hi, lo);
+      if (valid) {
+        const int g = k / kGroup, t = (k % kGroup) / 8;
+        a.out_xp[xp_index(g, r, t, 0, a.m)] = hi;
+        a.out_xp[xp_index(g, r, t, 1, a.m)] = lo;
+        if ((oi & 3) == 0) a.out_xs[g * a.m + r] = gx;
+      }
     }
   }
   // leave the counters cleared once every split has read the arrivals

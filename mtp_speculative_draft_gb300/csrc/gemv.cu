@@ -53,27 +53,24 @@ __global__ void pack_x_kernel(const float* __restrict__ x, int m, int K, uint4* 
   const int G = K / kGroup;
   const int total = G * m * 4;
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  float2 sum = make_float2(0.f, 0.f);
-  if (i < total) {
-    const int t = i & 3;
-    const int gc = i >> 2;
-    const int c = gc % m;
-    const int g = gc / m;
+  const bool valid = i < total;
+  const int t = i & 3;
+  const int gc = i >> 2;
+  const int c = gc % m;
+  const int g = gc / m;
+  float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  if (valid) {
     const float4* src = reinterpret_cast<const float4*>(x + (size_t)c * K + g * kGroup + t * 8);
     const float4 v0 = src[0], v1 = src[1];
-    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint4 hi, lo;
-    sum = pack8(v, hi, lo);
+    v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
+    v[4] = v1.x; v[5] = v1.y; v[6] = v1.z; v[7] = v1.w;
+  }
+  uint4 hi, lo;
+  const float2 gx = pack8_group(v, valid, hi, lo);
+  if (valid) {
     xp[xp_index(g, c, t, 0, m)] = hi;
     xp[xp_index(g, c, t, 1, m)] = lo;
-  }
-  sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 1);
-  sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
-  sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
-  sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 2);
-  if (i < total && (i & 3) == 0) {
-    const int gc = i >> 2;
-    xs[(gc / m) * m + gc % m] = sum;
+    if (t == 0) xs[g * m + c] = gx;
   }
 }
 
@@ -92,8 +89,12 @@ struct Plan {
   int ksplit, spu, units;
 };
 // kalign > 0: units must not straddle a multiple of kalign stages.
+// split_rounds > 1: a split may take up to that many rounds of the warps (a
+// tile's k chunks then run on different warps in different rounds); such a
+// plan must beat the others by a margin (its partials and combines cost
+// more than the model counts).
 static Plan plan_split(int tiles, int KS, int warps_cap, int nacc, int um,
-                       const GemvScratch& sc, int kalign = 0) {
+                       const GemvScratch& sc, int kalign = 0, int split_rounds = 1) {
   Plan best = {0, 0, 0};
   double best_cost = 1e30;
   for (int spu = KS; spu >= 1; --spu) {
@@ -102,12 +103,13 @@ static Plan plan_split(int tiles, int KS, int warps_cap, int nacc, int um,
     if (ksplit > 1 && spu * (ksplit - 1) >= KS) continue;  // same split as a larger spu
     const long long units = (long long)tiles * um * ksplit;
     if (ksplit > 1 || um > 1) {
-      if (ksplit > 1 && units > warps_cap) continue;
+      if (ksplit > 1 && units > (long long)warps_cap * split_rounds) continue;
       if (tiles > sc.cnt_len) continue;
       if ((size_t)units * 32 * nacc * sizeof(float) > sc.part_bytes) continue;
     }
     const long long rounds = (units + warps_cap - 1) / warps_cap;
-    const double cost = (double)rounds * spu + (ksplit > 1 ? 1.0 + 0.15 * ksplit : 0.0);
+    double cost = (double)rounds * spu + (ksplit > 1 ? 1.0 + 0.15 * ksplit : 0.0);
+    if (ksplit > 1 && rounds > 1) cost += 0.1 * rounds * spu;
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = {ksplit, spu, (int)units};
@@ -115,6 +117,14 @@ static Plan plan_split(int tiles, int KS, int warps_cap, int nacc, int um,
   }
   return best;
 }
+
+// Rounds of warps a split-K plan of the one-row kernel may take (tuning
+// knob; 2 lets the Qwen-style gate/up phase, 1088 tiles x 20 stages, run as
+// 3 k chunks over two rounds of every warp instead of one chunk on 1088).
+#ifndef MTP_ROW_SPLIT_ROUNDS
+#define MTP_ROW_SPLIT_ROUNDS 2
+#endif
+constexpr int kRowSplitRounds = MTP_ROW_SPLIT_ROUNDS;
 
 size_t gemv_scratch_part_bytes() {
   // one round of resident warps (at most 16 per SM) x 32 lanes x 32 floats
@@ -202,7 +212,8 @@ static cudaError_t launch_gemv_rows_t(GemvParams* ph, const int* tiles, int npha
     const int KS = (p.K / kGroup + 7) / 8;
     // with packed halves (kPreEmbedPack) the first phase's units stay in one half
     const int kalign = (q == 0 && pre && pre->kind == kPreEmbedPack) ? pre->dim / 256 : 0;
-    const Plan pl = plan_split(tiles[q], KS, warps_cap, 1, um, sc, kalign);  // 32 floats per unit
+    const Plan pl = plan_split(tiles[q], KS, warps_cap, 1, um, sc, kalign,
+                               kRowSplitRounds);  // 32 floats per unit
     if (pl.ksplit == 0) return cudaErrorInvalidValue;  // scratch too small for the split
     p.um = um;
     p.ksplit = pl.ksplit;

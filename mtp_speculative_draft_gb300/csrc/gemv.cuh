@@ -35,9 +35,13 @@ namespace mtp {
 // hl = 0 holds the f16 "hi" parts, 1 the "lo" parts, of the eight values
 // x[c][32g + 8t + p] as f16x2 words (first element in the low half):
 //   word 0: (p0, p4)   word 1: (p1/16, p5/16)   word 2: (p2, p6)   word 3: (p3/16, p7/16)
-// xs[g][c] = (2^-24 * sum of the represented x over the group, 0): the sum
-// meets the bias b at the scale of the tensor-core sums (see above).
-// Activations must lie within the f16 range (|x| < 65504).
+// xs[g][c] = (2^-24 * sum of the represented x over the group, 2^e): the
+// sum meets the bias b at the scale of the tensor-core sums (see above), and
+// the parts hold x * 2^-e, with e = 0 while the group's largest |x| is below
+// 2^15, else the e that brings it into [2^14, 2^15).  The consumer multiplies
+// the group's weight scale by 2^e, so any finite activation is represented
+// (to the split's 22 bits; elements more than 2^-100 below their group's
+// largest may flush to zero).
 __host__ __device__ inline int xpack_groups(int K) { return (K / kGroup + 7) / 8 * 8; }
 __host__ __device__ inline size_t xpack_xs_offset(int m, int K) {
   return (size_t)xpack_groups(K) * m * 128;
@@ -59,14 +63,28 @@ __device__ __forceinline__ float split_f16(float x, __half& hi, __half& lo) {
   return h + __half2float(lo);
 }
 
-// Packs the eight values of (g, c, t); returns their (sum, correction) pair.
-__device__ __forceinline__ float2 pack8(const float v[8], uint4& hi, uint4& lo) {
+// Power-of-two scale 2^e of a group whose largest |x| is amax: 1 below 2^15
+// (and for inf or NaN, which then propagate), else amax * 2^-e in [2^14, 2^15).
+__device__ __forceinline__ float xpack_group_scale(float amax) {
+  if (!(amax >= 32768.f) || isinf(amax)) return 1.f;
+  const unsigned ex = (__float_as_uint(amax) >> 23) & 0xffu;  // biased exponent, >= 142
+  return __uint_as_float((ex - 14u) << 23);
+}
+// 1 / s for a power of two s in [1, 2^113] (exact).
+__device__ __forceinline__ float pow2_inverse(float s) {
+  return __uint_as_float((254u << 23) - __float_as_uint(s));
+}
+
+// Packs the eight values of (g, c, t) times inv (the group's 2^-e); returns
+// their contribution to the group's sum (2^-24 * represented x).
+__device__ __forceinline__ float pack8(const float v[8], float inv, float scale, uint4& hi,
+                                       uint4& lo) {
   __half h[8], l[8];
   float sa = 0.f, sb = 0.f;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const bool bslot = (i & 1) != 0;  // elements 1, 3, 5, 7 meet a 16*code
-    const float r = split_f16(bslot ? v[i] * 0.0625f : v[i], h[i], l[i]);
+    const float r = split_f16((bslot ? v[i] * 0.0625f : v[i]) * inv, h[i], l[i]);
     if (bslot) sb += r; else sa += r;
   }
   auto pk = [](__half a, __half b) -> uint32_t {
@@ -74,22 +92,54 @@ __device__ __forceinline__ float2 pack8(const float v[8], uint4& hi, uint4& lo) 
   };
   hi = make_uint4(pk(h[0], h[4]), pk(h[1], h[5]), pk(h[2], h[6]), pk(h[3], h[7]));
   lo = make_uint4(pk(l[0], l[4]), pk(l[1], l[5]), pk(l[2], l[6]), pk(l[3], l[7]));
-  return make_float2((sa + 16.f * sb) * kCodeUnscale, 0.f);
+  return (sa + 16.f * sb) * scale * kCodeUnscale;
 }
 
-// Stores element p (0..7) of an (g, c, t) octet: word p % 4, half p / 4.
-// Returns its contribution to the group's (sum, correction) pair.
-__device__ __forceinline__ float2 xp_store_elem(uint4* xp, int m, int g, int c, int t, int p,
-                                               float v) {
+// One octet of a group held by four adjacent lanes (octet t in lane t of the
+// four); every lane of the warp calls it (valid = false: no octet, v unused).
+// Packs the octet with the group's scale and returns the group's xs entry.
+__device__ __forceinline__ float2 pack8_group(const float v[8], bool valid, uint4& hi, uint4& lo) {
+  float amax = 0.f;
+  if (valid)
+#pragma unroll
+    for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+  amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+  const float sc = xpack_group_scale(amax);
+  float sum = valid ? pack8(v, pow2_inverse(sc), sc, hi, lo) : 0.f;
+  sum += __shfl_xor_sync(0xffffffffu, sum, 1);
+  sum += __shfl_xor_sync(0xffffffffu, sum, 2);
+  return make_float2(sum, sc);
+}
+
+// Stores element p (0..7) of an (g, c, t) octet times inv (the group's
+// 2^-e): word p % 4, half p / 4.  Returns its contribution to the group's
+// sum (2^-24 * represented x).
+__device__ __forceinline__ float xp_store_elem(uint4* xp, int m, int g, int c, int t, int p,
+                                               float v, float inv, float scale) {
   const bool bslot = (p & 1) != 0;
   __half h, l;
-  const float r = split_f16(bslot ? v * 0.0625f : v, h, l);
+  const float r = split_f16((bslot ? v * 0.0625f : v) * inv, h, l);
   unsigned short* base = reinterpret_cast<unsigned short*>(xp);
   const size_t w_hi = (size_t)xp_index(g, c, t, 0, m) * 8 + (p & 3) * 2 + (p >> 2);
   const size_t w_lo = (size_t)xp_index(g, c, t, 1, m) * 8 + (p & 3) * 2 + (p >> 2);
   base[w_hi] = __half_as_ushort(h);
   base[w_lo] = __half_as_ushort(l);
-  return make_float2((bslot ? 16.f * r : r) * kCodeUnscale, 0.f);
+  return (bslot ? 16.f * r : r) * scale * kCodeUnscale;
+}
+
+// A group held one element per lane (element `lane`, v = 0 where store is
+// false); every lane of the warp calls it.  Returns the group's xs entry.
+__device__ __forceinline__ float2 xp_store_group(uint4* xp, int m, int g, int c, int lane,
+                                                 float v, bool store = true) {
+  float amax = store ? fabsf(v) : 0.f;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  const float sc = xpack_group_scale(amax);
+  float sum = store ? xp_store_elem(xp, m, g, c, lane >> 3, lane & 7, v, pow2_inverse(sc), sc) : 0.f;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+  return make_float2(sum, sc);
 }
 
 // ------------------------------------------------------------------ params
@@ -384,8 +434,10 @@ __device__ __forceinline__ void epi_store(const GemvParams& p, const GemvSeg& sg
   const int g_out = (sg.out_col0 + rbase) / kGroup;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    float ssq[2] = {0.f, 0.f};
+    // a group (32 rows of column c) is the 8 lanes of one tq, 4 values each
+    float pv[2][4];
+    bool pk[2][4];
+    float amax[2] = {0.f, 0.f}, ssq[2] = {0.f, 0.f};
 #pragma unroll
     for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
@@ -393,34 +445,52 @@ __device__ __forceinline__ void epi_store(const GemvParams& p, const GemvSeg& sg
         const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
         const int row = rbase + rloc;
         const int c = nt * 8 + 2 * tq + (e & 1);
+        pk[rt][e] = false;
+        pv[rt][e] = 0.f;
         if (row < sg.n && c < m) {
           const size_t o = (size_t)c * sg.ld + sg.out_col0 + row;
           float v = f[rt][nt][e];
           if (sg.res) v += __ldcg(sg.res + o);
           sg.out[o] = v;
           if (packing && c >= p.pack_c0) {
-            const float2 hs = xp_store_elem(p.out_xp, p.out_m, g_out, c - p.pack_c0, rloc >> 3,
-                                            rloc & 7, v * p.pack_w[sg.out_col0 + row]);
-            part[e & 1].x += hs.x;
-            part[e & 1].y += hs.y;
+            pk[rt][e] = true;
+            pv[rt][e] = v * p.pack_w[sg.out_col0 + row];
+            amax[e & 1] = fmaxf(amax[e & 1], fabsf(pv[rt][e]));
             ssq[e & 1] = fmaf(v, v, ssq[e & 1]);
           }
         }
       }
     if (packing) {
+      float sc[2], sum[2] = {0.f, 0.f};
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float2 v = part[e];
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1)
+          amax[e] = fmaxf(amax[e], __shfl_xor_sync(0xffffffffu, amax[e], o));
+        sc[e] = xpack_group_scale(amax[e]);
+      }
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (pk[rt][e]) {
+            const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
+            const int c = nt * 8 + 2 * tq + (e & 1);
+            sum[e & 1] += xp_store_elem(p.out_xp, p.out_m, g_out, c - p.pack_c0, rloc >> 3,
+                                        rloc & 7, pv[rt][e], pow2_inverse(sc[e & 1]), sc[e & 1]);
+          }
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = sum[e];
         float q2 = ssq[e];
 #pragma unroll
         for (int o = 4; o < 32; o <<= 1) {
-          v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-          v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+          v += __shfl_xor_sync(0xffffffffu, v, o);
           q2 += __shfl_xor_sync(0xffffffffu, q2, o);
         }
         const int c = nt * 8 + 2 * tq + e;
         if (gid == 0 && c < m && c >= p.pack_c0) {
-          p.out_xs[g_out * p.out_m + (c - p.pack_c0)] = v;
+          p.out_xs[g_out * p.out_m + (c - p.pack_c0)] = make_float2(v, sc[e]);
           p.ss_out[lt * p.out_m + (c - p.pack_c0)] = q2;
         }
       }
@@ -439,7 +509,8 @@ __device__ __forceinline__ void epi_swiglu(const GemvParams& p, const GemvSeg& s
   const int g_out = (sg.out_col0 + rbase) / kGroup;
 #pragma unroll
   for (int nt = 0; nt < NT; ++nt) {
-    float2 part[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    float hv[2][4];
+    float amax[2] = {0.f, 0.f};
 #pragma unroll
     for (int rt = 0; rt < 2; ++rt)
 #pragma unroll
@@ -447,24 +518,37 @@ __device__ __forceinline__ void epi_swiglu(const GemvParams& p, const GemvSeg& s
         const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
         const int c = nt * 8 + 2 * tq + (e & 1);
         const float gv = g[rt][nt][e], uv = u[rt][nt][e];
-        const float hv = gv / (1.f + __expf(-gv)) * uv * scale;
+        hv[rt][e] = gv / (1.f + __expf(-gv)) * uv * scale;
         if (c < p.out_m) {
-          const float2 hs = xp_store_elem(p.out_xp, p.out_m, g_out, c, rloc >> 3, rloc & 7, hv);
-          part[e & 1].x += hs.x;
-          part[e & 1].y += hs.y;
-          if (sg.out) sg.out[(size_t)c * sg.ld + sg.out_col0 + rbase + rloc] = hv;
+          amax[e & 1] = fmaxf(amax[e & 1], fabsf(hv[rt][e]));
+          if (sg.out) sg.out[(size_t)c * sg.ld + sg.out_col0 + rbase + rloc] = hv[rt][e];
         }
+      }
+    float sc[2], sum[2] = {0.f, 0.f};
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+#pragma unroll
+      for (int o = 4; o < 32; o <<= 1)
+        amax[e] = fmaxf(amax[e], __shfl_xor_sync(0xffffffffu, amax[e], o));
+      sc[e] = xpack_group_scale(amax[e]);
+    }
+#pragma unroll
+    for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int rloc = rt * 16 + gid + ((e & 2) ? 8 : 0);
+        const int c = nt * 8 + 2 * tq + (e & 1);
+        if (c < p.out_m)
+          sum[e & 1] += xp_store_elem(p.out_xp, p.out_m, g_out, c, rloc >> 3, rloc & 7, hv[rt][e],
+                                      pow2_inverse(sc[e & 1]), sc[e & 1]);
       }
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
-      float2 v = part[e];
+      float v = sum[e];
 #pragma unroll
-      for (int o = 4; o < 32; o <<= 1) {
-        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
-        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
-      }
+      for (int o = 4; o < 32; o <<= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
       const int c = nt * 8 + 2 * tq + e;
-      if (gid == 0 && c < p.out_m) p.out_xs[g_out * p.out_m + c] = v;
+      if (gid == 0 && c < p.out_m) p.out_xs[g_out * p.out_m + c] = make_float2(v, sc[e]);
     }
   }
 }
@@ -505,13 +589,12 @@ __device__ __forceinline__ void argmax_finish(const GemvParams& p, unsigned long
     unsigned long long b = red[0];
     for (int w2 = 1; w2 < kGemvWarps; ++w2) b = red[w2] > b ? red[w2] : b;
     p.am_partial[blockIdx.x] = b;
-    __threadfence();
-    const unsigned prev = atomicAdd(p.am_counter, 1u);
+    const unsigned prev = atom_add_acq_rel_gpu(p.am_counter, 1u);  // releases the partial
     last = (prev == gridDim.x - 1);
   }
   __syncthreads();
   if (last) {
-    __threadfence();
+    asm volatile("fence.acq_rel.gpu;" ::: "memory");  // every CTA's partial, for all threads
     unsigned long long b = 0ull;
     for (int i2 = threadIdx.x; i2 < (int)gridDim.x; i2 += blockDim.x) {
       const unsigned long long v = __ldcg(p.am_partial + i2);
@@ -720,13 +803,13 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     for (int jp = 0; jp < 4; ++jp) {
       const uint32_t coff = ((uint32_t)jp << 5) ^ ld_c;
       float d[NMAT][2][2][NT][4];
-      float sx0[2][NT], sx1[2][NT];
+      float2 sx0[2][NT], sx1[2][NT];  // (sum, scale) of the columns' groups
 #pragma unroll
       for (int h = 0; h < 2; ++h)
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          sx0[h][nt] = xs0[h][nt].x;
-          sx1[h][nt] = xs1[h][nt].x;
+          sx0[h][nt] = xs0[h][nt];
+          sx1[h][nt] = xs1[h][nt];
         }
 #pragma unroll
       for (int mi = 0; mi < NMAT; ++mi) {
@@ -783,10 +866,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
             for (int nt = 0; nt < NT; ++nt) {
               const float* dd = d[mi][rt][h][nt];
               float* a = acc[mi][rt][nt];
-              a[0] = fmaf(s0, dd[0], fmaf(b0, sx0[h][nt], a[0]));
-              a[2] = fmaf(s1, dd[2], fmaf(b1, sx0[h][nt], a[2]));
-              a[1] = fmaf(s0, dd[1], fmaf(b0, sx1[h][nt], a[1]));
-              a[3] = fmaf(s1, dd[3], fmaf(b1, sx1[h][nt], a[3]));
+              const float2 x0 = sx0[h][nt], x1 = sx1[h][nt];
+              a[0] = fmaf(s0 * x0.y, dd[0], fmaf(b0, x0.x, a[0]));
+              a[2] = fmaf(s1 * x0.y, dd[2], fmaf(b1, x0.x, a[2]));
+              a[1] = fmaf(s0 * x1.y, dd[1], fmaf(b0, x1.x, a[1]));
+              a[3] = fmaf(s1 * x1.y, dd[3], fmaf(b1, x1.x, a[3]));
             }
           }
         }
@@ -920,14 +1004,8 @@ __device__ __forceinline__ void pre_embed_pack(const PreParams& q, int u, int* e
   const float wv = first ? q.w0[k] : q.w1[k];
   const float x = __ldcg(row + k);
   const float v = x * wv;
-  float2 hs = xp_store_elem(q.xp, 1, u, 0, lane >> 3, lane & 7, v);
-  float ss = x * x;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    hs.x += __shfl_xor_sync(0xffffffffu, hs.x, o);
-    hs.y += __shfl_xor_sync(0xffffffffu, hs.y, o);
-    ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  }
+  const float2 hs = xp_store_group(q.xp, 1, u, 0, lane, v);
+  const float ss = warp_sum(x * x);
   if (lane == 0) {
     q.xs[u] = hs;
     q.ss[u] = ss;
@@ -969,12 +1047,7 @@ __device__ __forceinline__ void pre_attn_merge(const PreParams& q, int u, int la
   }
   acc = den > 0.f ? acc / den : 0.f;
   if (q.gated) acc = acc / (1.f + __expf(-g));
-  float2 hs = xp_store_elem(q.xp, 1, (h * q.dv + d0) / kGroup, 0, lane >> 3, lane & 7, acc);
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    hs.x += __shfl_xor_sync(0xffffffffu, hs.x, o);
-    hs.y += __shfl_xor_sync(0xffffffffu, hs.y, o);
-  }
+  const float2 hs = xp_store_group(q.xp, 1, (h * q.dv + d0) / kGroup, 0, lane, acc);
   if (lane == 0) q.xs[(h * q.dv + d0) / kGroup] = hs;
 }
 
@@ -1314,10 +1387,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
                           codes_hi_f16x2(y1), B[st][w].z, B[st][w].w);
           }
         }
-        acc[rt][0] = fmaf(s0.x, d[0][0] + d[0][1], fmaf(b0.x, sxv.x, acc[rt][0]));
-        acc[rt][0] = fmaf(s0.y, d[1][0] + d[1][1], fmaf(b0.y, sxv.z, acc[rt][0]));
-        acc[rt][1] = fmaf(s1.x, d[0][2] + d[0][3], fmaf(b1.x, sxv.x, acc[rt][1]));
-        acc[rt][1] = fmaf(s1.y, d[1][2] + d[1][3], fmaf(b1.y, sxv.z, acc[rt][1]));
+        // (sxv: the two groups' sums and power-of-two scales)
+        acc[rt][0] = fmaf(s0.x * sxv.y, d[0][0] + d[0][1], fmaf(b0.x, sxv.x, acc[rt][0]));
+        acc[rt][0] = fmaf(s0.y * sxv.w, d[1][0] + d[1][1], fmaf(b0.y, sxv.z, acc[rt][0]));
+        acc[rt][1] = fmaf(s1.x * sxv.y, d[0][2] + d[0][3], fmaf(b1.x, sxv.x, acc[rt][1]));
+        acc[rt][1] = fmaf(s1.y * sxv.w, d[1][2] + d[1][3], fmaf(b1.y, sxv.z, acc[rt][1]));
       }
     }
     __syncwarp();
@@ -1391,14 +1465,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
         const float v = g + resv;
         if (row_ok) sg.out[sg.out_col0 + row] = v;
         if (p.pack_w) {  // full tiles (checked by the host)
-          float2 hs = xp_store_elem(p.out_xp, 1, g_out, 0, rr >> 3, rr & 7, v * pw);
-          float q2 = v * v;
-#pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            hs.x += __shfl_xor_sync(0xffffffffu, hs.x, o);
-            hs.y += __shfl_xor_sync(0xffffffffu, hs.y, o);
-            q2 += __shfl_xor_sync(0xffffffffu, q2, o);
-          }
+          const float2 hs = xp_store_group(p.out_xp, 1, g_out, 0, rr, v * pw);
+          const float q2 = warp_sum(v * v);
           if (lane == 0) {
             p.out_xs[g_out] = hs;
             p.ss_out[lt] = q2;
@@ -1407,13 +1475,8 @@ __global__ void __launch_bounds__(kGemvWarps * 32, 3)
       } else if (p.epi == kEpiSwiglu) {
         const float scale = sg.w_idx >= 0 ? p.segw[sg.w_idx] : 1.f;
         const float hv = g / (1.f + __expf(-g)) * u * scale;
-        float2 hs = xp_store_elem(p.out_xp, 1, g_out, 0, rr >> 3, rr & 7, hv);
+        const float2 hs = xp_store_group(p.out_xp, 1, g_out, 0, rr, hv);
         if (sg.out) sg.out[sg.out_col0 + lt * 32 + rr] = hv;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          hs.x += __shfl_xor_sync(0xffffffffu, hs.x, o);
-          hs.y += __shfl_xor_sync(0xffffffffu, hs.y, o);
-        }
         if (lane == 0) p.out_xs[g_out] = hs;
       } else {
         if (row_ok) {

@@ -47,22 +47,19 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterPara
   if (blockIdx.x == 0 && r.xp) {
     for (int o0 = 0; o0 < H / 8; o0 += kRouterThreads) {
       const int o = o0 + tid;
-      float2 sum = make_float2(0.f, 0.f);
-      if (o < H / 8) {
-        float v[8];
+      const bool valid = o < H / 8;
+      float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (valid)
 #pragma unroll
         for (int i = 0; i < 8; ++i) v[i] = fsm[o * 8 + i];
-        uint4 hi, lo;
-        sum = pack8(v, hi, lo);
+      uint4 hi, lo;
+      const float2 gx = pack8_group(v, valid, hi, lo);
+      if (valid) {
         const int g = o / 4, t = o & 3;
         r.xp[xp_index(g, 0, t, 0, 1)] = hi;
         r.xp[xp_index(g, 0, t, 1, 1)] = lo;
+        if (t == 0) r.xs[g] = gx;
       }
-      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 1);
-      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
-      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
-      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 2);
-      if (o < H / 8 && (o & 3) == 0) r.xs[o / 4] = sum;
     }
   }
 

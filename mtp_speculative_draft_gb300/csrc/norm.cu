@@ -86,15 +86,15 @@ __global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackA
   const int o_end = min(octets, o_begin + per);
   for (int o0 = o_begin; o0 < o_end; o0 += kNormThreads) {
     const int o = o0 + threadIdx.x;
-    float2 sum = make_float2(0.f, 0.f);
-    if (o < o_end) {
-      const int k = o * 8;
+    const bool valid = o < o_end;
+    const int k = o * 8;
+    float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    if (valid) {
       const int si = (a.nseg > 1 && k >= a.seg[0].dim) ? 1 : 0;
       const NormSeg& s = a.seg[si];
       const int kk = k - (si ? a.seg[0].dim : 0);
       const float* row = seg_row(s, c, a.err);
       const float* dl = s.delta ? s.delta + (size_t)c * s.src_ld : nullptr;
-      float v[8];
       const float4 v0 = *reinterpret_cast<const float4*>(row + kk);
       const float4 v1 = *reinterpret_cast<const float4*>(row + kk + 4);
       v[0] = v0.x; v[1] = v0.y; v[2] = v0.z; v[3] = v0.w;
@@ -120,21 +120,17 @@ __global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackA
 #pragma unroll
         for (int i = 0; i < 8; ++i) s.out_norm[(size_t)c * s.dim + kk + i] = v[i];
       }
-      if (a.xp) {
-        uint4 hi, lo;
-        sum = pack8(v, hi, lo);
-        const int g = k / kGroup, t = (k % kGroup) / 8;
-        a.xp[xp_index(g, c, t, 0, a.m)] = hi;
-        a.xp[xp_index(g, c, t, 1, a.m)] = lo;
-      }
     }
     if (a.xp) {
       // octets o..o+3 of one group sit in adjacent lanes (kNormThreads % 4 == 0)
-      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 1);
-      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 1);
-      sum.x += __shfl_xor_sync(0xffffffffu, sum.x, 2);
-      sum.y += __shfl_xor_sync(0xffffffffu, sum.y, 2);
-      if (o < o_end && (o & 3) == 0) a.xs[(o / 4) * a.m + c] = sum;
+      uint4 hi, lo;
+      const float2 gx = pack8_group(v, valid, hi, lo);
+      if (valid) {
+        const int g = k / kGroup, t = (k % kGroup) / 8;
+        a.xp[xp_index(g, c, t, 0, a.m)] = hi;
+        a.xp[xp_index(g, c, t, 1, a.m)] = lo;
+        if ((o & 3) == 0) a.xs[(o / 4) * a.m + c] = gx;
+      }
     }
   }
 }
