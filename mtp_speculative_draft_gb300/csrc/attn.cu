@@ -49,6 +49,7 @@ constexpr int kAttnMaxWarps = MTP_ATTN_MAX_WARPS;  // warps per CTA (tuning knob
 constexpr int kAttnQMax = 8;                     // query rows per warp (template bound)
 constexpr size_t kAttnSmemLimit = 226 * 1024;     // dynamic shared memory of one CTA (227 KB less static)
 constexpr size_t kAttnSlack = 1024;               // alignment of the swizzled K boxes
+constexpr int kAttnWq = 18;                       // per query row: <= 16 buffer weights, M, l
 
 // Partials: (M, l) pairs [nkv][nsplit][QG][2], then outputs [nkv][nsplit][QG][dv]
 // starting on a 16-byte boundary.
@@ -409,22 +410,40 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   __syncthreads();
   const size_t pidx = (size_t)(kvh * a.nsplit + split) * QG;
   float* part_o = a.part + attn_part_o_offset(a.nkv, a.nsplit, QG);
+  // each query row's buffer weights exp2(M_b - M) once (a warp per row,
+  // lanes over the buffers), then the weighted sums of the outputs
+  float* wq = wout + (size_t)nw * QM * dv;  // [QG][kAttnWq]: weights, then M and l
+  for (int q = warp; q < QG; q += nw) {
+    const int g = q / qpw, ql = q - g * qpw;
+    const float mb = lane < nbuf ? wstat[((lane * qgroups + g) * QM + ql) * 2] : kNegBig;
+    const float lb = lane < nbuf ? wstat[((lane * qgroups + g) * QM + ql) * 2 + 1] : 0.f;
+    const float M = warp_max(mb);
+    const float f = lane < nbuf ? exp2f(mb - M) : 0.f;
+    const float l = warp_sum(f * lb);
+    if (lane < nbuf) wq[q * kAttnWq + lane] = f;
+    if (lane == 0) {
+      wq[q * kAttnWq + kAttnWq - 2] = M;
+      wq[q * kAttnWq + kAttnWq - 1] = l;
+    }
+  }
+  __syncthreads();
   for (int it = tid; it < QG * dv; it += nthreads) {
     const int q = it / dv, d = it - q * dv;
     const int g = q / qpw, ql = q - g * qpw;
-    float M = kNegBig;
-    for (int bb = 0; bb < nbuf; ++bb) M = fmaxf(M, wstat[((bb * qgroups + g) * QM + ql) * 2]);
-    float l = 0.f, o = 0.f;
-    for (int bb = 0; bb < nbuf; ++bb) {
-      const int w = bb * qgroups + g;
-      const float f = exp2f(wstat[(w * QM + ql) * 2] - M);
-      l += f * wstat[(w * QM + ql) * 2 + 1];
-      o += f * wout[((size_t)w * QM + ql) * dv + d];
+    const float* fq = wq + q * kAttnWq;
+    const float* src = wout + (size_t)(g * QM + ql) * dv + d;  // buffer bb at + bb * qgroups * QM * dv
+    const size_t bstride = (size_t)qgroups * QM * dv;
+    float o0 = 0.f, o1 = 0.f;
+    int bb = 0;
+    for (; bb + 2 <= nbuf; bb += 2) {  // two independent chains
+      o0 = fmaf(fq[bb], src[bb * bstride], o0);
+      o1 = fmaf(fq[bb + 1], src[(bb + 1) * bstride], o1);
     }
-    part_o[(pidx + q) * dv + d] = o;
+    if (bb < nbuf) o0 = fmaf(fq[bb], src[bb * bstride], o0);
+    part_o[(pidx + q) * dv + d] = o0 + o1;
     if (d == 0) {
-      a.part[(pidx + q) * 2 + 0] = M;
-      a.part[(pidx + q) * 2 + 1] = l;
+      a.part[(pidx + q) * 2 + 0] = fq[kAttnWq - 2];
+      a.part[(pidx + q) * 2 + 1] = fq[kAttnWq - 1];
     }
   }
   // ---- all splits of this KV head publish their partials, then each merges
@@ -682,7 +701,8 @@ cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
   const int nw = nbuf * a.qgroups;
   const AttnLayout Ly = attn_layout(a.dqk, a.dv, qslots, a.m, nbuf, nw);
   // the tile buffers are reused for the buffers' states, then the merge
-  const size_t combine = ((size_t)kAttnMaxWarps * kAttnQMax * 2 + (size_t)nw * qm * a.dv) * 4;
+  const size_t combine =
+      ((size_t)kAttnMaxWarps * kAttnQMax * 2 + (size_t)nw * qm * a.dv + (size_t)QG * kAttnWq) * 4;
   // the merge of one split: weights and denominators [ns][QG], its slice's
   // partials [ns][items] and merged items (float4 items, 8 per 32-dim group)
   const int ngroups = QG * a.dv / kGroup;

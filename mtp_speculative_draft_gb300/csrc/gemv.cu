@@ -137,9 +137,12 @@ size_t gemv_scratch_part_bytes() {
 #endif
 
 template <int NMAT, int NT, int EPI, int XM, bool PAIRED = false>
+#ifndef MTP_TC_STAGES
+#define MTP_TC_STAGES MTP_GEMV_STAGES
+#endif
 static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
                                  cudaStream_t st) {
-  constexpr int S = MTP_GEMV_STAGES;
+  constexpr int S = MTP_TC_STAGES;
   auto kern = gemv_tc_kernel<NMAT, NT, EPI, S, XM, PAIRED>;
   const int smem = gemv_smem_bytes<NMAT, S, XM>();
   static thread_local int configured_dev = -1;
@@ -268,17 +271,20 @@ cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
     return launch_gemv_rows(&p, &tiles, 1, sc, p.err, st);
   }
   if (epi == kEpiArgmax) return cudaErrorInvalidValue;
-  // activations staged per stage by bulk copy for up to 4 columns
+  // activations staged per stage by bulk copy for up to MTP_TC_XM_ROWS columns
+#ifndef MTP_TC_XM_ROWS
+#define MTP_TC_XM_ROWS 4
+#endif
   if (nmat == 1) {
     if (epi != kEpiStore) return cudaErrorInvalidValue;
     if (nt == 2) return launch_gemv_t<1, 2, kEpiStore, 0>(p, tiles, sc, st);
-    if (m <= 4) return launch_gemv_t<1, 1, kEpiStore, 4>(p, tiles, sc, st);
+    if (m <= MTP_TC_XM_ROWS) return launch_gemv_t<1, 1, kEpiStore, 4>(p, tiles, sc, st);
     return launch_gemv_t<1, 1, kEpiStore, 0>(p, tiles, sc, st);
   }
   // SwiGLU: gate (slot mat) and up (slot mat + 1) tiles are separate units
   if (epi != kEpiSwiglu) return cudaErrorInvalidValue;
   if (nt == 2) return launch_gemv_t<1, 2, kEpiSwiglu, 0, true>(p, tiles, sc, st);
-  if (m <= 4) return launch_gemv_t<1, 1, kEpiSwiglu, 4, true>(p, tiles, sc, st);
+  if (m <= MTP_TC_XM_ROWS) return launch_gemv_t<1, 1, kEpiSwiglu, 4, true>(p, tiles, sc, st);
   return launch_gemv_t<1, 1, kEpiSwiglu, 0, true>(p, tiles, sc, st);
 }
 
