@@ -616,6 +616,7 @@ static mtp_status enqueue_moe(const mtp_moe_weights* w, const float* u1, const f
   r.weight = sc.weight;
   r.xp = sc.xp_f;
   r.xs = sc.xs_f;
+  r.err = &header(ws)->err;
   cudaError_t e = launch_router(r, st);
   if (e != cudaSuccess) return cuda_fail(e, "moe router launch");
 

@@ -690,6 +690,15 @@ cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
   const int ntiles = ceil_div(a.L - kbeg, kTileKeys);
   const int tps = ntiles > 0 ? ceil_div(ntiles, a.nsplit) : 1;
   int nbuf = tps;
+  // at least one warp per query slot and new row for the prologue (its norm
+  // and rotation are a dependent round trip per row), within the warp limit
+#ifndef MTP_ATTN_PROLOGUE_WARPS
+#define MTP_ATTN_PROLOGUE_WARPS 1
+#endif
+  if (MTP_ATTN_PROLOGUE_WARPS) {
+    const int want = std::min(kAttnMaxWarps, qslots + a.m);
+    if (nbuf * a.qgroups < want) nbuf = std::max(nbuf, want / a.qgroups);
+  }
   if (nbuf > kAttnMaxWarps / a.qgroups) nbuf = kAttnMaxWarps / a.qgroups;
   if (nbuf > 15) nbuf = 15;  // named barriers 1..15 (0 is the CTA barrier)
   while (nbuf > 1 &&

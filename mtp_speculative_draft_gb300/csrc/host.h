@@ -142,6 +142,8 @@ struct RouterParams {
   float* weight;         // [top_k + 1]
   uint4* xp;             // packed normalised row for the expert projections
   float2* xs;
+  int* err;
+  int rows_per_cta;      // set by launch_router
 };
 cudaError_t launch_router(const RouterParams& r, cudaStream_t st);
 
