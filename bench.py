@@ -92,11 +92,13 @@ def launch_plan(cfg, bf16_stacks=False):
     if cfg.moe:
         E, Ie, k = cfg.n_experts, cfg.expert_intermediate, cfg.top_k
         ea = aff_bf16 if bf16_stacks else aff   # routed stacks; the shared expert is float32
-        return [("launch A: embedding pack + eh_proj + q/k/v", eh + qkv), ("attention", attn),
-                ("o_proj", o), ("router", 4 * E * H),
-                ("expert gate/up", k * 2 * ea(Ie, H) + 2 * aff(Ie, H)),
-                ("expert down", k * ea(H, Ie) + aff(H, Ie)), ("final norm", 4 * H),
-                ("lm_head + argmax", lm)]
+        plan = [("launch A: embedding pack + eh_proj + q/k/v", eh + qkv), ("attention", attn),
+                ("split merge + o_proj", o), ("router", 4 * E * H),
+                ("expert gate/up + expert down + lm_head", k * 2 * ea(Ie, H) + 2 * aff(Ie, H)
+                 + k * ea(H, Ie) + aff(H, Ie) + lm)]
+        if H % 256:
+            plan.insert(0, ("embedding/hidden norm pack", 4 * 2 * H))
+        return plan
     I = cfg.intermediate
     gu, dn = 2 * aff(I, H), aff(H, I)
     if m == 1:

@@ -597,9 +597,14 @@ static void carve_moe(Carve& cv, const mtp_moe_weights* w, int H, MoeScratch* m)
   m->gemv = carve_scratch(cv);
 }
 
-static mtp_status enqueue_moe(const mtp_moe_weights* w, const float* u1, const float* post_norm,
-                              float eps, int H, float* u2, const MoeScratch& sc, void* ws,
-                              cudaStream_t st) {
+// Launches the router and fills the one-row phases of the experts: gate/up
+// with SwiGLU over the routed and shared experts (rows chosen by the router),
+// then down + residual into u2.
+static mtp_status moe_router_and_phases(const mtp_moe_weights* w, const float* u1,
+                                        const float* post_norm, float eps, int H, float* u2,
+                                        const MoeScratch& sc, void* ws, cudaStream_t st,
+                                        GemvParams* gu_out, GemvParams* dn_out, int* gu_tiles,
+                                        int* dn_tiles) {
   const int E = w->n_experts, I = w->expert_inter, K = w->top_k;
   RouterParams r = {};
   r.u1 = u1;
@@ -650,8 +655,7 @@ static mtp_status enqueue_moe(const mtp_moe_weights* w, const float* u1, const f
   p.out_xs = sc.xs_h;
   p.out_m = 1;
   p.err = &header(ws)->err;
-  e = launch_gemv(2, 1, kEpiSwiglu, p, (K + 1) * tpe, sc.gemv, st);
-  if (e != cudaSuccess) return cuda_fail(e, "moe expert gate/up launch");
+  p.epi = kEpiSwiglu;
 
   // down projections over the concatenated expert activations, + residual
   GemvParams d = {};
@@ -671,7 +675,25 @@ static mtp_status enqueue_moe(const mtp_moe_weights* w, const float* u1, const f
   d.kseg_row_mult = H;
   d.kseg_last_mat = 1;
   d.err = &header(ws)->err;
-  e = launch_gemv(1, 1, kEpiStore, d, tiles_of(H), sc.gemv, st);
+  d.epi = kEpiStore;
+  *gu_out = p;
+  *dn_out = d;
+  *gu_tiles = (K + 1) * tpe;
+  *dn_tiles = tiles_of(H);
+  return MTP_OK;
+}
+
+// The MoE FFN alone: router, gate/up launch, down launch.
+static mtp_status enqueue_moe(const mtp_moe_weights* w, const float* u1, const float* post_norm,
+                              float eps, int H, float* u2, const MoeScratch& sc, void* ws,
+                              cudaStream_t st) {
+  GemvParams gu = {}, dn = {};
+  int tg = 0, td = 0;
+  mtp_status s = moe_router_and_phases(w, u1, post_norm, eps, H, u2, sc, ws, st, &gu, &dn, &tg, &td);
+  if (s != MTP_OK) return s;
+  cudaError_t e = launch_gemv(2, 1, kEpiSwiglu, gu, tg, sc.gemv, st);
+  if (e != cudaSuccess) return cuda_fail(e, "moe expert gate/up launch");
+  e = launch_gemv(1, 1, kEpiStore, dn, td, sc.gemv, st);
   if (e != cudaSuccess) return cuda_fail(e, "moe expert down launch");
   return MTP_OK;
 }
@@ -935,11 +957,26 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
   a.prefetch_before_wait = 1;  // the q/k/v projection signals only after its own wait
   // one row, dense FFN: the next launch merges the splits before o_proj
   const bool fused_tail = rows && !L->moe;  // o, gate/up, down and lm_head in one launch
-  a.merge_in_kernel = fused_tail ? 0 : 1;
+  a.merge_in_kernel = rows ? 0 : 1;  // one row: the o_proj launch merges the splits
   a.out = nullptr;
   a.out_xp = w.xa;
   a.out_xs = w.xsa;
   if ((e = launch_attn(a, st)) != cudaSuccess) return cuda_fail(e, "attention launch");
+  PreParams pre_b = {};  // the split merge, as pre-units of the o_proj launch (m = 1)
+  pre_b.kind = kPreAttnMerge;
+  pre_b.units = g.n_heads * g.head_dim_v / kGroup;
+  pre_b.xp = w.xa;
+  pre_b.xs = w.xsa;
+  pre_b.part = w.part;
+  pre_b.part_o = attn_part_outputs(w.part, g.n_kv_heads, a.nsplit, g.n_heads / g.n_kv_heads);
+  pre_b.nkv = g.n_kv_heads;
+  pre_b.ns = a.nsplit;
+  pre_b.G = g.n_heads / g.n_kv_heads;
+  pre_b.dv = g.head_dim_v;
+  pre_b.dqk = g.head_dim_qk;
+  pre_b.gated = g.gated_q ? 1 : 0;
+  pre_b.sinks = L->sinks;
+  pre_b.qp = w.qp;
 
   // 6. u1 = u + W_o o
   const int ko = g.n_heads * g.head_dim_v;
@@ -961,10 +998,58 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     o.ss_out = w.ss1;
   }
   o.epi = kEpiStore;
-  if (!fused_tail && (e = launch_gemv(1, nt, kEpiStore, o, tiles_of(H), w.gemv, st)) != cudaSuccess)
+  if (rows && !fused_tail) {
+    const int to = tiles_of(H);
+    if ((e = launch_gemv_rows(&o, &to, 1, w.gemv, err, st, &pre_b)) != cudaSuccess)
+      return cuda_fail(e, "split merge + o_proj launch");
+  } else if (!fused_tail &&
+             (e = launch_gemv(1, nt, kEpiStore, o, tiles_of(H), w.gemv, st)) != cudaSuccess) {
     return cuda_fail(e, "o_proj launch");
+  }
 
   float* u2 = out->d_u2 ? out->d_u2 : w.u2;
+  if (L->moe && rows) {
+    // one row: the experts' gate/up, down (+ residual, final norm folded)
+    // and lm_head + argmax in one launch after the router
+    GemvParams gu = {}, dn = {};
+    int tg = 0, td = 0;
+    s = moe_router_and_phases(L->moe, w.u1, L->post_norm, L->eps, H, u2, w.moe, ws, st, &gu, &dn,
+                              &tg, &td);
+    if (s != MTP_OK) return s;
+    dn.pack_w = L->final_norm;
+    dn.pack_c0 = 0;
+    dn.out_xp = w.xb;
+    dn.out_xs = w.xsb;
+    dn.out_m = 1;
+    dn.ss_out = w.ss2;
+    GemvParams hd = {};
+    if ((s = qmat_cached(&hd.mat[0], L->lm_head, "lm_head")) != MTP_OK) return s;
+    hd.xp = w.xb;
+    hd.xs = w.xsb;
+    hd.m = 1;
+    hd.K = H;
+    hd.nseg = 1;
+    hd.seg[0] = plain_seg(tiles_of(L->vocab), L->vocab, 0, nullptr, L->vocab, nullptr);
+    hd.in_ss = w.ss2;
+    hd.in_ss_n = ht;
+    hd.in_ss_dim = H;
+    hd.in_ss_eps = L->eps;
+    hd.normed_src = u2;
+    hd.normed_w = L->final_norm;
+    hd.normed_out = out->d_hidden_out;
+    hd.am_partial = w.am_partial;
+    hd.am_counter = header(ws)->counters + kCntArgmax;
+    hd.am_token = out->d_token;
+    hd.am_value = out->d_value;
+    hd.logits = out->d_logits;
+    hd.err = err;
+    hd.epi = kEpiArgmax;
+    GemvParams ph[3] = {gu, dn, hd};
+    const int tl[3] = {tg, td, tiles_of(L->vocab)};
+    if ((e = launch_gemv_rows(ph, tl, 3, w.gemv, err, st)) != cudaSuccess)
+      return cuda_fail(e, "experts + lm head launch");
+    return MTP_OK;
+  }
   if (L->moe) {
     s = enqueue_moe(L->moe, w.u1, L->post_norm, L->eps, H, u2, w.moe, ws, st);
     if (s != MTP_OK) return s;
@@ -1038,21 +1123,6 @@ static mtp_status enqueue_layer(const mtp_layer_desc* L, const mtp_step_in* in,
     if (fused_tail) {
       GemvParams ph[4] = {o, gu, dn, hd};
       const int tl[4] = {tiles_of(H), tiles_of(I), tiles_of(H), tiles_of(L->vocab)};
-      PreParams pre_b = {};
-      pre_b.kind = kPreAttnMerge;
-      pre_b.units = g.n_heads * g.head_dim_v / kGroup;
-      pre_b.xp = w.xa;
-      pre_b.xs = w.xsa;
-      pre_b.part = w.part;
-      pre_b.part_o = attn_part_outputs(w.part, g.n_kv_heads, a.nsplit, g.n_heads / g.n_kv_heads);
-      pre_b.nkv = g.n_kv_heads;
-      pre_b.ns = a.nsplit;
-      pre_b.G = g.n_heads / g.n_kv_heads;
-      pre_b.dv = g.head_dim_v;
-      pre_b.dqk = g.head_dim_qk;
-      pre_b.gated = g.gated_q ? 1 : 0;
-      pre_b.sinks = L->sinks;
-      pre_b.qp = w.qp;
       if ((e = launch_gemv_rows(ph, tl, 4, w.gemv, err, st, &pre_b)) != cudaSuccess)
         return cuda_fail(e, "o_proj + gate/up + down + lm head launch");
     } else if ((e = launch_gemv(1, 1, kEpiArgmax, hd, tiles_of(L->vocab), w.gemv, st)) != cudaSuccess) {
