@@ -247,7 +247,182 @@ __device__ __forceinline__ void warp_tile(const AttnParams& a, WarpState<QM, DV>
   __syncwarp();
 }
 
-template <int QM, int DV>
+// ------------------------------------------------ tensor-core tile path
+// For 128-dim heads and at most 8 query rows per KV head: logits and P.V as
+// mma.sync m16n8k8 TF32 products, each operand split into a TF32 "big" part
+// and the remainder (three products, the small x small one dropped: about
+// 2^-21 relative error per product, float32 accumulation).  One warp owns a
+// 16-key tile and all 8 query slots:
+//   S^T[key][q] = K . Q^T: M = keys, N = query slots, K = dims, with the dims
+//     of k-step (block b, step s) permuted so lane (gid, tq) reads dims
+//     32b + 8tq + [0, 8) of key rows gid and gid + 8 (two conflict-free
+//     16-byte loads per row from the swizzled K box) and holds the same dims
+//     of query slot gid in registers;
+//   O^T[dim][q] += V^T . P^T: M = dims with row r of m-tile mt standing for
+//     dim 16 (r mod 8) + 2 mt + r / 8, so lane gid's A elements of all eight
+//     m-tiles are dims 16 gid + [0, 16) of its two key rows; P goes through
+//     the warp's row of shared memory from the logits' layout to the B layout.
+// The accumulator layouts of both products put query slots 2tq, 2tq + 1 in
+// lane (gid, tq), so the online-softmax rescale needs no data movement.
+constexpr int kTcNB = 4;   // 32-dim blocks of the 128-dim q/k heads
+constexpr int kTcNMT = 8;  // 16-dim m-tiles of the 128-dim v heads
+// unrolling of the tile's dim-block and key-step loops (tuning knob: the
+// code size of one tile against the loop overhead)
+#ifndef MTP_ATTN_TC_UNROLL
+#define MTP_ATTN_TC_UNROLL 1
+#endif
+constexpr int kTcUnrollB = MTP_ATTN_TC_UNROLL;
+constexpr int kTcUnrollK = MTP_ATTN_TC_UNROLL > 2 ? 2 : MTP_ATTN_TC_UNROLL;
+
+__device__ __forceinline__ void tf32_split(float x, uint32_t& big, uint32_t& small) {
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(big) : "f"(x));
+  small = __float_as_uint(x - __uint_as_float(big));  // truncated to TF32 by the tensor core
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                         uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};\n"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// d += A B with A = a (four f32 values, split here) and B given split
+__device__ __forceinline__ void mma_tf32x3(float (&d)[4], const float (&a)[4], uint32_t bb0,
+                                           uint32_t bs0, uint32_t bb1, uint32_t bs1) {
+  uint32_t ab[4], as[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) tf32_split(a[i], ab[i], as[i]);
+  mma_tf32(d, as, bb0, bb1);
+  mma_tf32(d, ab, bs0, bs1);
+  mma_tf32(d, ab, bb0, bb1);
+}
+
+struct TcState {
+  float M[2], l[2];         // query slots 2tq, 2tq + 1
+  float o[kTcNMT][4];       // O^T fragments
+};
+
+__device__ __forceinline__ void load8(float (&v)[8], const float* p0, const float* p1) {
+  const float4 x = *reinterpret_cast<const float4*>(p0);
+  const float4 y = *reinterpret_cast<const float4*>(p1);
+  v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+  v[4] = y.x; v[5] = y.y; v[6] = y.z; v[7] = y.w;
+}
+
+// One tile of nk <= 16 keys from key0 on.  swz: K in swizzled boxes (cached
+// tiles), else plain rows of 128 floats (the new keys); V plain rows of 128
+// floats.  Rows at or past nk are not read.
+__device__ __forceinline__ void warp_tile_tc(const AttnParams& a, TcState& st, const float* Ks,
+                                             bool swz, const float* Vs, int nk, int key0,
+                                             const float* qrow, int G, int QG, float* ps,
+                                             int lane) {
+  const int gid = lane >> 2, tq = lane & 3;
+  // two accumulators (even and odd dim blocks) halve the dependent MMA chain
+  float d[4] = {0.f, 0.f, 0.f, 0.f}, d2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll kTcUnrollB
+  for (int b = 0; b < kTcNB; ++b) {
+    float k0[8], k1[8];  // key rows gid and gid + 8, dims 32b + 8tq + [0, 8)
+    if (swz) {
+      const float* kb = Ks + b * (kTileKeys * 32);
+      const int c0 = ((2 * tq) ^ (gid & 7)) << 2, c1 = ((2 * tq + 1) ^ (gid & 7)) << 2;
+      load8(k0, kb + gid * 32 + c0, kb + gid * 32 + c1);
+      load8(k1, kb + (gid + 8) * 32 + c0, kb + (gid + 8) * 32 + c1);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) k0[i] = k1[i] = 0.f;
+      const int off = 32 * b + 8 * tq;
+      if (gid < nk) load8(k0, Ks + gid * 128 + off, Ks + gid * 128 + off + 4);
+      if (gid + 8 < nk) load8(k1, Ks + (gid + 8) * 128 + off, Ks + (gid + 8) * 128 + off + 4);
+    }
+    float q[8];  // query slot gid, the same dims
+    load8(q, qrow + gid * 128 + 32 * b + 8 * tq, qrow + gid * 128 + 32 * b + 8 * tq + 4);
+#pragma unroll
+    for (int s2 = 0; s2 < 4; ++s2) {
+      uint32_t bb0, bs0, bb1, bs1;
+      tf32_split(q[2 * s2], bb0, bs0);
+      tf32_split(q[2 * s2 + 1], bb1, bs1);
+      const float av[4] = {k0[2 * s2], k1[2 * s2], k0[2 * s2 + 1], k1[2 * s2 + 1]};
+      mma_tf32x3((b & 1) ? d2 : d, av, bb0, bs0, bb1, bs1);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] += d2[i];
+  // online softmax per query slot column (d[2 hh + c]: key gid + 8 hh, slot 2tq + c)
+  float p[4], alpha[2];
+#pragma unroll
+  for (int c = 0; c < 2; ++c) {
+    const int qi = 2 * tq + c;
+    const int pos = a.L + qi / G;
+    bool ok[2];
+    float mx = kNegBig;
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      const int key = gid + 8 * hh, j = key0 + key;
+      ok[hh] = qi < QG && key < nk && j <= pos && (a.window <= 0 || j > pos - a.window);
+      if (ok[hh]) mx = fmaxf(mx, d[2 * hh + c]);
+    }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mnew = fmaxf(st.M[c], mx);
+    const float p0 = ok[0] ? exp2f(d[c] - mnew) : 0.f;
+    const float p1 = ok[1] ? exp2f(d[2 + c] - mnew) : 0.f;
+    float sm = p0 + p1;
+    sm += __shfl_xor_sync(0xffffffffu, sm, 4);
+    sm += __shfl_xor_sync(0xffffffffu, sm, 8);
+    sm += __shfl_xor_sync(0xffffffffu, sm, 16);
+    alpha[c] = exp2f(st.M[c] - mnew);
+    st.l[c] = st.l[c] * alpha[c] + sm;
+    st.M[c] = mnew;
+    p[c] = p0;
+    p[2 + c] = p1;
+  }
+#pragma unroll
+  for (int mt = 0; mt < kTcNMT; ++mt) {
+    st.o[mt][0] *= alpha[0];
+    st.o[mt][2] *= alpha[0];
+    st.o[mt][1] *= alpha[1];
+    st.o[mt][3] *= alpha[1];
+  }
+  // probabilities as [slot][key] in the warp's row of shared memory
+  ps[(2 * tq) * kTileKeys + gid] = p[0];
+  ps[(2 * tq + 1) * kTileKeys + gid] = p[1];
+  ps[(2 * tq) * kTileKeys + gid + 8] = p[2];
+  ps[(2 * tq + 1) * kTileKeys + gid + 8] = p[3];
+  __syncwarp();
+#pragma unroll kTcUnrollK
+  for (int ks = 0; ks < 2; ++ks) {
+    const int ka = 8 * ks + tq, kb2 = ka + 4;
+    uint32_t bb0, bs0, bb1, bs1;
+    tf32_split(ps[gid * kTileKeys + ka], bb0, bs0);
+    tf32_split(ps[gid * kTileKeys + kb2], bb1, bs1);
+    float va[16], vb[16];  // key rows ka, kb2, dims 16 gid + [0, 16) (zero past nk)
+#pragma unroll
+    for (int i = 0; i < 16; ++i) va[i] = vb[i] = 0.f;
+    // swz: dims 16 gid + [0, 16) of key row k sit in box gid / 2, 16-byte
+    // chunks 4 (gid & 1) + c4 at position chunk ^ (k & 7) (conflict-free)
+    auto vrow = [&](int k, float (&v)[16]) {
+#pragma unroll
+      for (int c4 = 0; c4 < 4; ++c4) {
+        const float* src = swz ? Vs + (gid >> 1) * (kTileKeys * 32) + k * 32 +
+                                     (((4 * (gid & 1) + c4) ^ (k & 7)) << 2)
+                               : Vs + k * 128 + 16 * gid + 4 * c4;
+        const float4 x = *reinterpret_cast<const float4*>(src);
+        v[4 * c4] = x.x; v[4 * c4 + 1] = x.y; v[4 * c4 + 2] = x.z; v[4 * c4 + 3] = x.w;
+      }
+    };
+    if (ka < nk) vrow(ka, va);
+    if (kb2 < nk) vrow(kb2, vb);
+#pragma unroll
+    for (int mt = 0; mt < kTcNMT; ++mt) {
+      const float av[4] = {va[2 * mt], va[2 * mt + 1], vb[2 * mt], vb[2 * mt + 1]};
+      mma_tf32x3(st.o[mt], av, bb0, bs0, bb1, bs1);
+    }
+  }
+  __syncwarp();  // the probability row is rewritten by the next tile
+}
+
+template <int QM, int DV, bool TC>
 __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
     attn_decode_kernel(const __grid_constant__ AttnParams a) {
   extern __shared__ __align__(1024) uint8_t smraw_unaligned[];
@@ -303,10 +478,16 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   auto issue = [&](int t) {
     const int key0 = kbeg + t * kTileKeys;
     const int nk = min(kTileKeys, L - key0);
-    mbar_arrive_expect_tx(&bars[b], (uint32_t)kTileKeys * dqk * 4 + (uint32_t)nk * dv * 4);
+    if constexpr (TC) {  // V in swizzled boxes as well (whole boxes; rows past nk unused)
+      mbar_arrive_expect_tx(&bars[b], (uint32_t)kTileKeys * (dqk + dv) * 4);
+      for (int bx = 0; bx < dv / 32; ++bx)
+        tma_load_2d(Vb + bx * (kTileKeys * 32), &a.vmap, &bars[b], bx * 32, kvh * a.cap + key0, pol);
+    } else {
+      mbar_arrive_expect_tx(&bars[b], (uint32_t)kTileKeys * dqk * 4 + (uint32_t)nk * dv * 4);
+      bulk_load(Vb, vbase + (size_t)key0 * dv, (uint32_t)nk * dv * 4, &bars[b], pol);
+    }
     for (int bx = 0; bx < dqk / 32; ++bx)
       tma_load_2d(Kb + bx * (kTileKeys * 32), &a.kmap, &bars[b], bx * 32, kvh * a.cap + key0, pol);
-    bulk_load(Vb, vbase + (size_t)key0 * dv, (uint32_t)nk * dv * 4, &bars[b], pol);
   };
   const int t_first = t_begin + b;
   if (a.prefetch_before_wait && leader && t_first < t_end) issue(t_first);
@@ -355,12 +536,20 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   __syncthreads();
 
   WarpState<QM, DV> st;
+  TcState tc;
+  if constexpr (TC) {
+    tc.M[0] = tc.M[1] = kNegBig;
+    tc.l[0] = tc.l[1] = 0.f;
 #pragma unroll
-  for (int q = 0; q < QM; ++q) {
-    st.M[q] = kNegBig;
-    st.l[q] = 0.f;
+    for (int mt = 0; mt < kTcNMT; ++mt) tc.o[mt][0] = tc.o[mt][1] = tc.o[mt][2] = tc.o[mt][3] = 0.f;
+  } else {
 #pragma unroll
-    for (int i = 0; i < DV; ++i) st.o[q][i] = 0.f;
+    for (int q = 0; q < QM; ++q) {
+      st.M[q] = kNegBig;
+      st.l[q] = 0.f;
+#pragma unroll
+      for (int i = 0; i < DV; ++i) st.o[q][i] = 0.f;
+    }
   }
   // ---- the buffer's tiles: t_first, t_first + nbuf, ...
   const int bar_id = 1 + b, bar_cnt = qgroups * 32;
@@ -376,7 +565,9 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
     }
     phase ^= 1u;
     const int key0 = kbeg + t * kTileKeys;
-    if (nq > 0)
+    if constexpr (TC)
+      warp_tile_tc(a, tc, Kb, true, Vb, min(kTileKeys, L - key0), key0, qrow, G, QG, ps, lane);
+    else if (nq > 0)
       warp_tile<QM, DV>(a, st, Kb, true, Vb, min(kTileKeys, L - key0), key0, qrow, q0, G, ps,
                         lane);
     if (t + nbuf < t_end) {
@@ -384,27 +575,56 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
       if (leader) issue(t + nbuf);
     }
   }
-  if (has_new && b == nbuf - 1 && nq > 0)
-    warp_tile<QM, DV>(a, st, newk, false, newv, a.m, L, qrow, q0, G, ps, lane);
+  if (has_new && b == nbuf - 1) {
+    if constexpr (TC)
+      warp_tile_tc(a, tc, newk, false, newv, a.m, L, qrow, G, QG, ps, lane);
+    else if (nq > 0)
+      warp_tile<QM, DV>(a, st, newk, false, newv, a.m, L, qrow, q0, G, ps, lane);
+  }
   if (__syncthreads_or(dead)) return;
   if (tid < nbuf) mbar_inval(&bars[tid]);
   __syncthreads();
 
   // ---- the buffers' states meet in shared memory (the tile buffers are free)
   float* wstat = reinterpret_cast<float*>(smraw);                 // [nw][QM][2]
-  float* wout = wstat + (size_t)kAttnMaxWarps * kAttnQMax * 2;    // [nw][QM][dv]
+  float* wout = wstat + (size_t)kAttnMaxWarps * kAttnQMax * 2;    // [nw][QM][ldw]
+  const int ldw = dv + 4;  // padded rows: the tensor-core fragments store with 2-way conflicts at most
+  if constexpr (TC) {
+    const int gid = lane >> 2, tq = lane & 3;
 #pragma unroll
-  for (int q = 0; q < QM; ++q) {
-    if (q < nq) {
-      if (lane == 0) {
-        wstat[(warp * QM + q) * 2] = st.M[q];
-        wstat[(warp * QM + q) * 2 + 1] = st.l[q];
+    for (int c = 0; c < 2; ++c) {
+      const int q = 2 * tq + c;
+      if (q < nq && gid == 0) {
+        wstat[(warp * QM + q) * 2] = tc.M[c];
+        wstat[(warp * QM + q) * 2 + 1] = tc.l[c];
       }
+    }
+    // slot 2tq + c holds dims 16 gid + [0, 16): fragments (mt, c) and (mt, c + 2)
+    // are dims 16 gid + 2 mt and + 1
 #pragma unroll
-      for (int c = 0; c < LD::NV; ++c)
+    for (int c = 0; c < 2; ++c) {
+      const int q = 2 * tq + c;
+      if (q < nq)
 #pragma unroll
-        for (int e = 0; e < LD::VW; ++e)
-          wout[((size_t)warp * QM + q) * dv + LD::dim(lane, c) + e] = st.o[q][c * LD::VW + e];
+        for (int j4 = 0; j4 < 4; ++j4)
+          *reinterpret_cast<float4*>(wout + ((size_t)warp * QM + q) * ldw + 16 * gid + 4 * j4) =
+              make_float4(tc.o[2 * j4][c], tc.o[2 * j4][c + 2], tc.o[2 * j4 + 1][c],
+                          tc.o[2 * j4 + 1][c + 2]);
+    }
+  } else {
+#pragma unroll
+    for (int q = 0; q < QM; ++q) {
+      if (q < nq) {
+        if (lane == 0) {
+          wstat[(warp * QM + q) * 2] = st.M[q];
+          wstat[(warp * QM + q) * 2 + 1] = st.l[q];
+        }
+#pragma unroll
+        for (int c = 0; c < LD::NV; ++c)
+#pragma unroll
+          for (int e = 0; e < LD::VW; ++e)
+            wout[((size_t)warp * QM + q) * ldw + LD::dim(lane, c) + e] = st.o[q][c * LD::VW + e];
+      }
     }
   }
   __syncthreads();
@@ -412,7 +632,7 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
   float* part_o = a.part + attn_part_o_offset(a.nkv, a.nsplit, QG);
   // each query row's buffer weights exp2(M_b - M) once (a warp per row,
   // lanes over the buffers), then the weighted sums of the outputs
-  float* wq = wout + (size_t)nw * QM * dv;  // [QG][kAttnWq]: weights, then M and l
+  float* wq = wout + (size_t)nw * QM * ldw;  // [QG][kAttnWq]: weights, then M and l
   for (int q = warp; q < QG; q += nw) {
     const int g = q / qpw, ql = q - g * qpw;
     const float mb = lane < nbuf ? wstat[((lane * qgroups + g) * QM + ql) * 2] : kNegBig;
@@ -431,8 +651,8 @@ __global__ void __launch_bounds__(kAttnMaxWarps * 32, 1)
     const int q = it / dv, d = it - q * dv;
     const int g = q / qpw, ql = q - g * qpw;
     const float* fq = wq + q * kAttnWq;
-    const float* src = wout + (size_t)(g * QM + ql) * dv + d;  // buffer bb at + bb * qgroups * QM * dv
-    const size_t bstride = (size_t)qgroups * QM * dv;
+    const float* src = wout + (size_t)(g * QM + ql) * ldw + d;  // buffer bb at + bb * bstride
+    const size_t bstride = (size_t)qgroups * QM * ldw;
     float o0 = 0.f, o1 = 0.f;
     int bb = 0;
     for (; bb + 2 <= nbuf; bb += 2) {  // two independent chains
@@ -604,6 +824,15 @@ static int attn_qmax(int dv) { return dv <= 128 ? kAttnQMax : 4; }
 
 // Query groups per buffer and the slots per group (the kernel's QM: the
 // smallest instantiated size that holds a group's rows).
+// The tensor-core tile path: 128-dim q/k and v heads, at most 8 query rows
+// per KV head (one warp holds all of them as the MMA's 8 columns).
+#ifndef MTP_ATTN_TC
+#define MTP_ATTN_TC 1
+#endif
+static bool attn_use_tc(int QG, int dqk, int dv) {
+  return MTP_ATTN_TC && dqk == 128 && dv == 128 && QG <= 8;
+}
+
 static void attn_groups(int QG, int dv, int* qgroups, int* qm) {
   *qgroups = ceil_div(QG, attn_qmax(dv));
   // more warps per buffer (fewer rows each) shorten the per-tile chains
@@ -611,23 +840,31 @@ static void attn_groups(int QG, int dv, int* qgroups, int* qm) {
   const int qpw = ceil_div(QG, *qgroups);
   *qm = qpw <= 2 ? 2 : qpw <= 4 ? 4 : qpw <= 6 ? 6 : 8;
 }
+static void attn_groups(int QG, int dqk, int dv, int* qgroups, int* qm) {
+  if (attn_use_tc(QG, dqk, dv)) {
+    *qgroups = 1;
+    *qm = 8;
+    return;
+  }
+  attn_groups(QG, dv, qgroups, qm);
+}
 
 bool attn_supported(int QG, int dqk, int dv, int m) {
   int qg, qm;
-  attn_groups(QG, dv, &qg, &qm);
+  attn_groups(QG, dqk, dv, &qg, &qm);
   if (qg > kAttnMaxWarps) return false;
   const AttnLayout Ly = attn_layout(dqk, dv, qg * qm, m, 1, qg);
   return Ly.total + kAttnSlack <= kAttnSmemLimit;
 }
 
-template <int QM, int DV>
+template <int QM, int DV, bool TC = false>
 static cudaError_t launch_attn_t(const AttnParams& a, size_t smem, cudaStream_t st) {
   static_assert(sizeof(AttnParams) <= 4096, "kernel parameters fit the classic limit");
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
   if (configured_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<QM, DV>,
+    cudaError_t e = cudaFuncSetAttribute(attn_decode_kernel<QM, DV, TC>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)kAttnSmemLimit);
     if (e != cudaSuccess) return e;
@@ -644,7 +881,7 @@ static cudaError_t launch_attn_t(const AttnParams& a, size_t smem, cudaStream_t 
   cfg.attrs = &attr;
   cfg.numAttrs = 1;
   launch_mark(cfg.stream);
-  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<QM, DV>, a);
+  return cudaLaunchKernelEx(&cfg, attn_decode_kernel<QM, DV, TC>, a);
 }
 
 template <int DV>
@@ -679,11 +916,13 @@ cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
   AttnParams a = a_in;
   cudaError_t ke =
       encode_f32_tile_map(&a.kmap, a.kc, (uint64_t)a.nkv * a.cap, (uint64_t)a.dqk, kTileKeys);
+  if (ke == cudaSuccess && attn_use_tc((a.nh / a.nkv) * a.m, a.dqk, a.dv))
+    ke = encode_f32_tile_map(&a.vmap, a.vc, (uint64_t)a.nkv * a.cap, (uint64_t)a.dv, kTileKeys);
   if (ke != cudaSuccess) return ke;
   const int QG = (a.nh / a.nkv) * a.m;
   // warps per buffer: the fewest that keep each warp within attn_qmax rows
   int qm = 0;
-  attn_groups(QG, a.dv, &a.qgroups, &qm);
+  attn_groups(QG, a.dqk, a.dv, &a.qgroups, &qm);
   const int qslots = a.qgroups * qm;
   // buffers: as many as the split has tiles, within the warp and smem limits
   const int kbeg = a.window > 0 ? (a.L + 1 - a.window > 0 ? a.L + 1 - a.window : 0) : 0;
@@ -711,7 +950,7 @@ cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
   const AttnLayout Ly = attn_layout(a.dqk, a.dv, qslots, a.m, nbuf, nw);
   // the tile buffers are reused for the buffers' states, then the merge
   const size_t combine =
-      ((size_t)kAttnMaxWarps * kAttnQMax * 2 + (size_t)nw * qm * a.dv + (size_t)QG * kAttnWq) * 4;
+      ((size_t)kAttnMaxWarps * kAttnQMax * 2 + (size_t)nw * qm * (a.dv + 4) + (size_t)QG * kAttnWq) * 4;
   // the merge of one split: weights and denominators [ns][QG], its slice's
   // partials [ns][items] and merged items (float4 items, 8 per 32-dim group)
   const int ngroups = QG * a.dv / kGroup;
@@ -722,6 +961,7 @@ cudaError_t launch_attn(const AttnParams& a_in, cudaStream_t st) {
   if (merge > smem) smem = merge;
   smem += kAttnSlack;
   if (smem > kAttnSmemLimit) return cudaErrorInvalidValue;
+  if (attn_use_tc(QG, a.dqk, a.dv)) return launch_attn_t<8, 4, true>(a, smem, st);
   return launch_attn_dv(a, qm, smem, st);
 }
 

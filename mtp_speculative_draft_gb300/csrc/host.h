@@ -94,6 +94,7 @@ cudaError_t encode_f32_tile_map(CUtensorMap* out, const float* base, uint64_t ro
 
 struct alignas(64) AttnParams {
   CUtensorMap kmap;     // K cache viewed as [n_kv * cap][dqk]
+  CUtensorMap vmap;     // V cache viewed as [n_kv * cap][dv] (tensor-core tile path)
   int nh, nkv, dqk, dv, rot, window, gated;
   float eps, scale;
   const float *qp, *kp, *vp, *qn, *kn, *rope, *sinks;
