@@ -707,6 +707,7 @@ def run_profile_kernel(args):
             n, k, name = H, cfg.intermediate, f"{cfg.name}.L0.ffn_down"
         w = DeviceAffine(mtp_synth.affine4_weight(cfg.seed, name, n, k), dev)
         x = torch.from_numpy(mtp_synth.normal_f32(cfg.seed, "profile.x", (1, k))).to(dev)
+        extra["algorithmic_bytes_per_call"] = aff(n, k) + 4 * k
         if args.profile_kernel == "lm_head":
             tok = torch.zeros(1, dtype=torch.int32, device=dev)
             val = torch.zeros(1, dtype=torch.float32, device=dev)
