@@ -22,7 +22,7 @@ constexpr int kMaxTopK = 16;
 constexpr size_t kRouterSmemLimit = 200 * 1024;
 
 __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterParams r) {
-  extern __shared__ __align__(16) float smem[];  // [rows][H] router rows, then [H] normalised row
+  extern __shared__ __align__(16) float smem[];  // [rows][H] router rows, [H] normalised row, [H] gate
   __shared__ float red[kRouterThreads / 32];
   __shared__ bool last;
   __shared__ float lg[kMaxExperts];
@@ -33,16 +33,20 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterPara
   const int nrows = min(r.rows_per_cta, r.E - e0);
   float* wsm = smem;
   float* fsm = smem + (size_t)r.rows_per_cta * H;
+  float* gsm = fsm + H;  // CTA 0: the shared-expert gate vector
+  const bool gate_copy = blockIdx.x == 0 && r.sh_gate_inp &&
+                         (reinterpret_cast<uintptr_t>(r.sh_gate_inp) & 15) == 0;
   if (tid == 0) {
     mbar_init(&bar, 1);
     mbar_fence_init();
   }
   __syncthreads();
   if (tid == 0) {
-    mbar_arrive_expect_tx(&bar, (uint32_t)(nrows * H * 4));
+    mbar_arrive_expect_tx(&bar, (uint32_t)((nrows + (gate_copy ? 1 : 0)) * H * 4));
     for (int i = 0; i < nrows; ++i)
       bulk_load(wsm + (size_t)i * H, r.router + (size_t)(e0 + i) * H, (uint32_t)(H * 4), &bar,
                 l2_policy_evict_first());
+    if (gate_copy) bulk_load(gsm, r.sh_gate_inp, (uint32_t)(H * 4), &bar, l2_policy_evict_first());
   }
   pdl_wait();
   pdl_launch_dependents();
@@ -81,10 +85,16 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterPara
         }
       }
     }
-    // shared expert gate
+    // shared expert gate (from the copy when it was aligned for one)
     float gsum = 0.f;
-    if (r.sh_gate_inp)
+    if (gate_copy) {
+      if (mbar_wait_bounded(&bar, 0))
+        for (int k = tid; k < H; k += kRouterThreads) gsum = fmaf(gsm[k], fsm[k], gsum);
+      else if (tid == 0)
+        set_dev_error(r.err, kErrMbarTimeout);
+    } else if (r.sh_gate_inp) {
       for (int k = tid; k < H; k += kRouterThreads) gsum = fmaf(r.sh_gate_inp[k], fsm[k], gsum);
+    }
     gsum = warp_sum(gsum);
     __syncthreads();
     if (lane == 0) red[warp] = gsum;
@@ -98,7 +108,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterPara
 
   // router logits of this CTA's rows (from shared memory)
   bool ok = true;
-  if (nrows > 0) ok = mbar_wait_bounded(&bar, 0);
+  if (nrows > 0 || gate_copy) ok = mbar_wait_bounded(&bar, 0);
   if (!ok) {
     if (tid == 0) set_dev_error(r.err, kErrMbarTimeout);
   } else if (warp < nrows) {
@@ -165,11 +175,11 @@ cudaError_t launch_router(const RouterParams& r_in, cudaStream_t st) {
   RouterParams r = r_in;
   // as many rows per CTA (one warp each) as fit beside the normalised row
   int rows = kRouterMaxRows;
-  while (rows > 1 && (size_t)(rows + 1) * r.H * sizeof(float) > kRouterSmemLimit) --rows;
-  if ((size_t)(rows + 1) * r.H * sizeof(float) > kRouterSmemLimit) return cudaErrorInvalidValue;
+  while (rows > 1 && (size_t)(rows + 2) * r.H * sizeof(float) > kRouterSmemLimit) --rows;
+  if ((size_t)(rows + 2) * r.H * sizeof(float) > kRouterSmemLimit) return cudaErrorInvalidValue;
   r.rows_per_cta = rows;
   const int grid = (r.E + rows - 1) / rows;
-  const size_t smem = (size_t)(rows + 1) * r.H * sizeof(float);
+  const size_t smem = (size_t)(rows + 2) * r.H * sizeof(float);  // + the normalised row, the gate
   static thread_local int configured_dev = -1;
   int dev = 0;
   cudaGetDevice(&dev);
