@@ -40,6 +40,17 @@ SCALED = {
     "moe_small": CONFIGS["moe"].with_(name="moe_small", hidden=512, n_heads=4, n_kv_heads=2,
                                       n_experts=64, top_k=8, expert_intermediate=256,
                                       shared_intermediate=256, vocab=3000, cache_len=100),
+    # degenerate caches: the first draft after an empty cache (the new keys alone)
+    "qwen_small_empty": CONFIGS["qwen_dense"].with_(name="qwen_small_empty", hidden=512, n_heads=8,
+                                                    n_kv_heads=2, intermediate=1024 + 128,
+                                                    vocab=6000, cache_len=0),
+    "qwen_small_m3_empty": CONFIGS["qwen_dense"].with_(name="qwen_small_m3_empty", hidden=512,
+                                                       n_heads=4, n_kv_heads=2, intermediate=768,
+                                                       vocab=3000, cache_len=0, m=3),
+    "moe_small_empty": CONFIGS["moe"].with_(name="moe_small_empty", hidden=512, n_heads=4,
+                                            n_kv_heads=2, n_experts=64, top_k=8,
+                                            expert_intermediate=256, shared_intermediate=256,
+                                            vocab=3000, cache_len=0),
 }
 
 
