@@ -364,7 +364,8 @@ static AttnParams make_attn(const mtp_attn_geom* g, const float* qp, const float
   a.L = L;
   a.cap = cap;
   a.m = m;
-  a.nsplit = attn_splits(a.nkv, g->window > 0 ? std::min(L, g->window - 1) : L);
+  a.nsplit = attn_splits(a.nkv, g->window > 0 ? std::min(L, g->window - 1) : L,
+                         (a.nh / a.nkv) * m, a.dqk, a.dv, m);
   a.merge_in_kernel = 1;
   return a;
 }

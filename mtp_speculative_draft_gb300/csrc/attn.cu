@@ -801,11 +801,25 @@ int attn_splits_bound(int nkv, int cached) {
   return ns < 1 ? 1 : ns;
 }
 
-int attn_splits(int nkv, int cached) {
+// Splits: as many as the SMs allow (one CTA per SM), but never fewer tiles
+// per split than a CTA has buffers while that still leaves a quarter of the
+// SMs a CTA: the MoE layer's 2048-key cache of 256-dim heads (6 buffers per
+// CTA) then takes 22 splits per KV head instead of 64, and the next launch
+// merges 22 partials (measured -1.9 us per step); short caches (a 128-key
+// window, a 64-key cache) keep one tile per split, which measured faster.
+static void attn_groups(int QG, int dqk, int dv, int* qgroups, int* qm);
+int attn_splits(int nkv, int cached, int QG, int dqk, int dv, int m) {
   const int ntiles = ceil_div(cached, kTileKeys);
   const int bound = attn_splits_bound(nkv, cached);
   if (ntiles == 0) return 1;
-  const int tps = ceil_div(ntiles, bound);
+  int tps = ceil_div(ntiles, bound);
+  int qg = 0, qm = 0;
+  attn_groups(QG, dqk, dv, &qg, &qm);
+  int nb = std::min(kAttnMaxWarps / qg, 15);
+  while (nb > 1 && attn_layout(dqk, dv, qg * qm, m, nb, nb * qg).total + kAttnSlack > kAttnSmemLimit)
+    --nb;
+  // one tile per buffer while that still gives a quarter of the SMs a CTA
+  if (tps < nb && ceil_div(ntiles, nb) * nkv >= sm_count() / 4) tps = nb;
   return ceil_div(ntiles, tps);  // no split without cached tiles
 }
 

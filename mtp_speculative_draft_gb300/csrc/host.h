@@ -122,7 +122,7 @@ struct alignas(64) AttnParams {
 const float* attn_part_outputs(const float* part, int nkv, int nsplit, int q_per_kv);
 // Split count for `cached` keys inside the window, and an upper bound of it
 // that grows with `cached` (sizes the partials).
-int attn_splits(int nkv, int cached);
+int attn_splits(int nkv, int cached, int q_rows_per_kv, int dqk, int dv, int m);
 int attn_splits_bound(int nkv, int cached);
 // Whether one CTA can serve QG query rows of the given head dims and m.
 bool attn_supported(int QG, int dqk, int dv, int m);
