@@ -136,14 +136,14 @@ size_t gemv_scratch_part_bytes() {
 #define MTP_GEMV_STAGES 2
 #endif
 
-template <int NMAT, int NT, int EPI, int XM, bool PAIRED = false>
+template <int NMAT, int NT, int EPI, int XM, bool PAIRED = false, bool PC = false>
 #ifndef MTP_TC_STAGES
 #define MTP_TC_STAGES MTP_GEMV_STAGES
 #endif
 static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
                                  cudaStream_t st) {
   constexpr int S = MTP_TC_STAGES;
-  auto kern = gemv_tc_kernel<NMAT, NT, EPI, S, XM, PAIRED>;
+  auto kern = gemv_tc_kernel<NMAT, NT, EPI, S, XM, PAIRED, PC>;
   const int smem = gemv_smem_bytes<NMAT, S, XM>();
   static thread_local int configured_dev = -1;
   static thread_local int ctas_per_sm = 1;
@@ -278,13 +278,13 @@ cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
   if (nmat == 1) {
     if (epi != kEpiStore) return cudaErrorInvalidValue;
     if (nt == 2) return launch_gemv_t<1, 2, kEpiStore, 0>(p, tiles, sc, st);
-    if (m <= MTP_TC_XM_ROWS) return launch_gemv_t<1, 1, kEpiStore, 4>(p, tiles, sc, st);
+    if (m <= MTP_TC_XM_ROWS) return launch_gemv_t<1, 1, kEpiStore, 4, false, true>(p, tiles, sc, st);
     return launch_gemv_t<1, 1, kEpiStore, 0>(p, tiles, sc, st);
   }
   // SwiGLU: gate (slot mat) and up (slot mat + 1) tiles are separate units
   if (epi != kEpiSwiglu) return cudaErrorInvalidValue;
   if (nt == 2) return launch_gemv_t<1, 2, kEpiSwiglu, 0, true>(p, tiles, sc, st);
-  if (m <= MTP_TC_XM_ROWS) return launch_gemv_t<1, 1, kEpiSwiglu, 4, true>(p, tiles, sc, st);
+  if (m <= MTP_TC_XM_ROWS) return launch_gemv_t<1, 1, kEpiSwiglu, 4, true, true>(p, tiles, sc, st);
   return launch_gemv_t<1, 1, kEpiSwiglu, 0, true>(p, tiles, sc, st);
 }
 

@@ -619,9 +619,16 @@ __device__ __forceinline__ void argmax_finish(const GemvParams& p, unsigned long
 
 // ------------------------------------------------------- several activation rows
 // m in 2..16: the m16n8 tiles' columns are activation rows (NT tiles of 8).
-template <int NMAT, int NT, int EPI, int S, int XM, bool PAIRED = false>
+// PC (m <= 4, one tile of columns): the eight columns are (activation row,
+// hi/lo part) pairs instead, so one product covers both parts of four rows:
+// half the MMAs and activation fragments per stage; lane (gid, tq) sums the
+// two parts of row tq and applies that row's group scale and sum.  At a
+// unit's end the per-lane results move (shuffles) to the column layout the
+// epilogues share.
+template <int NMAT, int NT, int EPI, int S, int XM, bool PAIRED = false, bool PC = false>
 __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 2)
     gemv_tc_kernel(const __grid_constant__ GemvParams p) {
+  static_assert(!PC || (NT == 1 && XM > 0), "paired columns: one column tile, staged rows");
   // PAIRED: the SwiGLU gate and up matrices of a tile are separate work
   // units (one matrix in flight per warp); their partial sums meet in the
   // split-K reduction.
@@ -720,6 +727,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
   row_scales<NT>(p, m, tq, false, rsc);
 
   float acc[NMAT][2][NT][4];
+  float accp[NMAT][2][2];  // PC: [mi][rt][row gid, gid + 8] for activation row tq
+#pragma unroll
+  for (int mi = 0; mi < NMAT; ++mi) accp[mi][0][0] = accp[mi][0][1] = accp[mi][1][0] = accp[mi][1][1] = 0.f;
 #pragma unroll
   for (int mi = 0; mi < NMAT; ++mi)
 #pragma unroll
@@ -797,6 +807,53 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     // last pair of a stage loads the first pair of the next stage when it
     // continues the same unit (global activations only).  Activations are
     // zero-padded to whole stages of 8 groups.
+    if constexpr (PC) {
+      // B column gid is part (gid & 1) of activation row gid >> 1; lane tq
+      // scales and sums row tq's product
+      const uint4* xps = reinterpret_cast<const uint4*>(rs + NMAT * 2048);
+      const float2* xss = reinterpret_cast<const float2*>(rs + NMAT * 2048 + XM * 1024);
+      const int cb = gid >> 1, hl = gid & 1;
+#pragma unroll 1
+      for (int jp = 0; jp < 4; ++jp) {
+        const uint32_t coff = ((uint32_t)jp << 5) ^ ld_c;
+        uint4 bp[2];
+        float2 xv[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = 2 * jp + h;
+          bp[h] = cb < m ? xps[xp_index(j, cb, tq, hl, m)] : make_uint4(0u, 0u, 0u, 0u);
+          xv[h] = tq < m ? xss[j * m + tq] : make_float2(0.f, 0.f);
+        }
+#pragma unroll
+        for (int mi = 0; mi < NMAT; ++mi) {
+          const float* ssm = reinterpret_cast<const float*>(rs + mi * 2048) + sb_lane + 2 * jp;
+          const float* bsm = ssm + 256;
+#pragma unroll
+          for (int rt = 0; rt < 2; ++rt) {
+            uint32_t w[4];
+            ldmatrix_x4(w[0], w[1], w[2], w[3], cd + mi * 4096 + rt * 2048 + coff);
+            const float2 sa = *reinterpret_cast<const float2*>(ssm + rt * 128);
+            const float2 sb = *reinterpret_cast<const float2*>(ssm + rt * 128 + 64);
+            const float2 ba = *reinterpret_cast<const float2*>(bsm + rt * 128);
+            const float2 bb = *reinterpret_cast<const float2*>(bsm + rt * 128 + 64);
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const uint32_t wa = w[2 * h], wb = w[2 * h + 1];
+              const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+              float dd[4] = {0.f, 0.f, 0.f, 0.f};
+              mma_f16_16816(dd, codes_lo_f16x2(wa), codes_lo_f16x2(wb), codes_hi_f16x2(wa),
+                            codes_hi_f16x2(wb), bp[h].x, bp[h].y);
+              mma_f16_16816(dd, codes_lo_f16x2(wa8), codes_lo_f16x2(wb8), codes_hi_f16x2(wa8),
+                            codes_hi_f16x2(wb8), bp[h].z, bp[h].w);
+              const float s0 = h ? sa.y : sa.x, s1 = h ? sb.y : sb.x;
+              const float b0 = h ? ba.y : ba.x, b1 = h ? bb.y : bb.x;
+              accp[mi][rt][0] = fmaf(s0 * xv[h].y, dd[0] + dd[1], fmaf(b0, xv[h].x, accp[mi][rt][0]));
+              accp[mi][rt][1] = fmaf(s1 * xv[h].y, dd[2] + dd[3], fmaf(b1, xv[h].x, accp[mi][rt][1]));
+            }
+          }
+        }
+      }
+    } else {
     if (!b_ready) load_b(0, bh, bl, xs0, xs1);
     const bool next_same_unit = XM == 0 && cc.ks + 1 < cc.ke;
 #pragma unroll 1
@@ -877,6 +934,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
       }
     }
     b_ready = next_same_unit;
+    }  // PC
     __syncwarp();
     if (lane == 0 && pc.u < units) {
       issue_w(pc, slot);
@@ -890,6 +948,22 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     if (!cc.advance(p, W, units, ksplit, spu, KS, UM)) continue;
 
     // ------------------------------------------------------------ unit done
+    if constexpr (PC) {
+      // to the column layout: element e of lane (gid, tq) is row gid + 8 (e >> 1),
+      // activation row 2tq + (e & 1), held by lane (gid, 2tq + (e & 1))
+#pragma unroll
+      for (int mi = 0; mi < NMAT; ++mi)
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int c = 2 * tq + (e & 1);
+            const float v = __shfl_sync(0xffffffffu, accp[mi][rt][e >> 1], gid * 4 + (c & 3));
+            acc[mi][rt][0][e] = c < 4 ? v : 0.f;
+          }
+          accp[mi][rt][0] = accp[mi][rt][1] = 0.f;
+        }
+    }
     // fin[um] is the tile's full sum for matrix um of the unit's tile
     constexpr int NACC = NMAT * 2 * NT * 4;
     float fin[UM][NACC];
