@@ -136,10 +136,14 @@ size_t gemv_scratch_part_bytes() {
 #define MTP_GEMV_STAGES 2
 #endif
 
-template <int NMAT, int NT, int EPI, int XM, bool PAIRED = false, bool PC = false>
+#ifndef MTP_TC_PC_XM
+#define MTP_TC_PC_XM 4
+#endif
+constexpr int kTcPcXm = MTP_TC_PC_XM;
 #ifndef MTP_TC_STAGES
 #define MTP_TC_STAGES MTP_GEMV_STAGES
 #endif
+template <int NMAT, int NT, int EPI, int XM, bool PAIRED = false, bool PC = false>
 static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
                                  cudaStream_t st) {
   constexpr int S = MTP_TC_STAGES;
@@ -271,20 +275,18 @@ cudaError_t launch_gemv(int nmat, int nt, int epi, GemvParams p, int tiles,
     return launch_gemv_rows(&p, &tiles, 1, sc, p.err, st);
   }
   if (epi == kEpiArgmax) return cudaErrorInvalidValue;
-  // activations staged per stage by bulk copy for up to MTP_TC_XM_ROWS columns
-#ifndef MTP_TC_XM_ROWS
-#define MTP_TC_XM_ROWS 4
-#endif
+  // 2-4 rows: paired columns, activations staged per stage by bulk copy
+  // (kTcPcXm = 4) or read through L1 (0); 5-16 rows: one column per row
   if (nmat == 1) {
     if (epi != kEpiStore) return cudaErrorInvalidValue;
     if (nt == 2) return launch_gemv_t<1, 2, kEpiStore, 0>(p, tiles, sc, st);
-    if (m <= MTP_TC_XM_ROWS) return launch_gemv_t<1, 1, kEpiStore, 4, false, true>(p, tiles, sc, st);
+    if (m <= 4) return launch_gemv_t<1, 1, kEpiStore, kTcPcXm, false, true>(p, tiles, sc, st);
     return launch_gemv_t<1, 1, kEpiStore, 0>(p, tiles, sc, st);
   }
   // SwiGLU: gate (slot mat) and up (slot mat + 1) tiles are separate units
   if (epi != kEpiSwiglu) return cudaErrorInvalidValue;
   if (nt == 2) return launch_gemv_t<1, 2, kEpiSwiglu, 0, true>(p, tiles, sc, st);
-  if (m <= MTP_TC_XM_ROWS) return launch_gemv_t<1, 1, kEpiSwiglu, 4, true, true>(p, tiles, sc, st);
+  if (m <= 4) return launch_gemv_t<1, 1, kEpiSwiglu, kTcPcXm, true, true>(p, tiles, sc, st);
   return launch_gemv_t<1, 1, kEpiSwiglu, 0, true>(p, tiles, sc, st);
 }
 

@@ -628,7 +628,7 @@ __device__ __forceinline__ void argmax_finish(const GemvParams& p, unsigned long
 template <int NMAT, int NT, int EPI, int S, int XM, bool PAIRED = false, bool PC = false>
 __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 2)
     gemv_tc_kernel(const __grid_constant__ GemvParams p) {
-  static_assert(!PC || (NT == 1 && XM > 0), "paired columns: one column tile, staged rows");
+  static_assert(!PC || NT == 1, "paired columns: one column tile");
   // PAIRED: the SwiGLU gate and up matrices of a tile are separate work
   // units (one matrix in flight per warp); their partial sums meet in the
   // split-K reduction.
@@ -810,8 +810,11 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     if constexpr (PC) {
       // B column gid is part (gid & 1) of activation row gid >> 1; lane tq
       // scales and sums row tq's product
-      const uint4* xps = reinterpret_cast<const uint4*>(rs + NMAT * 2048);
-      const float2* xss = reinterpret_cast<const float2*>(rs + NMAT * 2048 + XM * 1024);
+      // the stage's activations: staged with the weights, or read through L1
+      const uint4* xps = XM > 0 ? reinterpret_cast<const uint4*>(rs + NMAT * 2048)
+                                : p.xp + (size_t)gbase * m * 8;
+      const float2* xss = XM > 0 ? reinterpret_cast<const float2*>(rs + NMAT * 2048 + XM * 1024)
+                                 : p.xs + (size_t)gbase * m;
       const int cb = gid >> 1, hl = gid & 1;
 #pragma unroll 1
       for (int jp = 0; jp < 4; ++jp) {
@@ -821,8 +824,9 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
 #pragma unroll
         for (int h = 0; h < 2; ++h) {
           const int j = 2 * jp + h;
-          bp[h] = cb < m ? xps[xp_index(j, cb, tq, hl, m)] : make_uint4(0u, 0u, 0u, 0u);
-          xv[h] = tq < m ? xss[j * m + tq] : make_float2(0.f, 0.f);
+          bp[h] = cb < m ? (XM > 0 ? xps[xp_index(j, cb, tq, hl, m)] : __ldg(xps + xp_index(j, cb, tq, hl, m)))
+                         : make_uint4(0u, 0u, 0u, 0u);
+          xv[h] = tq < m ? (XM > 0 ? xss[j * m + tq] : __ldg(xss + j * m + tq)) : make_float2(0.f, 0.f);
         }
 #pragma unroll
         for (int mi = 0; mi < NMAT; ++mi) {
