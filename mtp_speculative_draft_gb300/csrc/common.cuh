@@ -159,6 +159,12 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+// Orders this thread's earlier generic-proxy accesses of shared memory (and,
+// after a warp barrier, its warp's) before its later bulk copies into it.
+__device__ __forceinline__ void fence_proxy_async_shared_cta() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
 // GPU-scope counters: a barrier (bar.sync / bar.warp.sync) makes the block's
 // or warp's earlier stores precede the releasing thread's operation, whose
 // release then publishes them (the barrier-then-release pattern).

@@ -143,6 +143,15 @@ constexpr int kTcPcXm = MTP_TC_PC_XM;
 #ifndef MTP_TC_STAGES
 #define MTP_TC_STAGES MTP_GEMV_STAGES
 #endif
+// Shared-memory carveout (percent of the maximum) of the tensor-core kernels
+// that read activations through L1, and a cap on their CTAs per SM (tuning
+// knobs; -1 / 0: the driver's choice).
+#ifndef MTP_TC_CARVEOUT
+#define MTP_TC_CARVEOUT -1
+#endif
+#ifndef MTP_TC_MAX_CTAS
+#define MTP_TC_MAX_CTAS 0
+#endif
 template <int NMAT, int NT, int EPI, int XM, bool PAIRED = false, bool PC = false>
 static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
                                  cudaStream_t st) {
@@ -156,9 +165,15 @@ static cudaError_t launch_gemv_t(GemvParams p, int tiles, const GemvScratch& sc,
   if (configured_dev != dev) {
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return e;
+    if (XM == 0 && MTP_TC_CARVEOUT >= 0) {
+      e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               MTP_TC_CARVEOUT);
+      if (e != cudaSuccess) return e;
+    }
     int nb = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&nb, kern, kGemvWarps * 32, smem);
     if (e != cudaSuccess) return e;
+    if (XM == 0 && MTP_TC_MAX_CTAS > 0 && nb > MTP_TC_MAX_CTAS) nb = MTP_TC_MAX_CTAS;
     ctas_per_sm = nb > 0 ? nb : 1;
     configured_dev = dev;
   }

@@ -625,8 +625,17 @@ __device__ __forceinline__ void argmax_finish(const GemvParams& p, unsigned long
 // two parts of row tq and applies that row's group scale and sum.  At a
 // unit's end the per-lane results move (shuffles) to the column layout the
 // epilogues share.
+// With staged activations the paired-column kernel fits two CTAs per SM, and
+// may first move a whole stage into registers, release its slot for the next
+// copy and then compute (tuning knob: 1 releases early, 0 after the stage).
+#ifndef MTP_TC_PC_EARLY
+#define MTP_TC_PC_EARLY 1
+#endif
+constexpr bool kTcPcEarly = MTP_TC_PC_EARLY != 0;
+
 template <int NMAT, int NT, int EPI, int S, int XM, bool PAIRED = false, bool PC = false>
-__global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 2)
+__global__ void __launch_bounds__(kGemvWarps * 32,
+                                  (NMAT == 1 && NT == 1 && !(PC && XM > 0)) ? 4 : 2)
     gemv_tc_kernel(const __grid_constant__ GemvParams p) {
   static_assert(!PC || NT == 1, "paired columns: one column tile");
   // PAIRED: the SwiGLU gate and up matrices of a tile are separate work
@@ -807,7 +816,75 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     // last pair of a stage loads the first pair of the next stage when it
     // continues the same unit (global activations only).  Activations are
     // zero-padded to whole stages of 8 groups.
-    if constexpr (PC) {
+    bool refilled = false;
+    if constexpr (PC && XM > 0 && kTcPcEarly) {
+      static_assert(NMAT == 1, "paired columns: one matrix per unit");
+      // the whole stage into registers: codes (ldmatrix), the rows'
+      // activation fragments and group sums, the lane's scales and biases
+      const uint4* xps = reinterpret_cast<const uint4*>(rs + 2048);
+      const float2* xss = reinterpret_cast<const float2*>(rs + 2048 + XM * 1024);
+      const int cb = gid >> 1, hl = gid & 1;
+      uint32_t wr[4][2][4];
+      uint4 bpr[4][2];
+      float2 xvr[4][2];
+#pragma unroll
+      for (int jp = 0; jp < 4; ++jp) {
+        const uint32_t coff = ((uint32_t)jp << 5) ^ ld_c;
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt)
+          ldmatrix_x4(wr[jp][rt][0], wr[jp][rt][1], wr[jp][rt][2], wr[jp][rt][3],
+                      cd + rt * 2048 + coff);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const int j = 2 * jp + h;
+          bpr[jp][h] = cb < m ? xps[xp_index(j, cb, tq, hl, m)] : make_uint4(0u, 0u, 0u, 0u);
+          xvr[jp][h] = tq < m ? xss[j * m + tq] : make_float2(0.f, 0.f);
+        }
+      }
+      // [rt][row gid / gid + 8][groups 0-3 / 4-7] of the [32][8] scale and bias tiles
+      float4 scr[2][2][2], bir[2][2][2];
+      const float* sbase = reinterpret_cast<const float*>(rs) + sb_lane;
+#pragma unroll
+      for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+        for (int r2 = 0; r2 < 2; ++r2)
+#pragma unroll
+          for (int q = 0; q < 2; ++q) {
+            scr[rt][r2][q] = *reinterpret_cast<const float4*>(sbase + rt * 128 + r2 * 64 + q * 4);
+            bir[rt][r2][q] = *reinterpret_cast<const float4*>(sbase + 256 + rt * 128 + r2 * 64 + q * 4);
+          }
+      // the slot is free: the warp's reads precede the next copy into it
+      __syncwarp();
+      if (lane == 0 && pc.u < units) {
+        fence_proxy_async_shared_cta();
+        issue_w(pc, slot);
+        issue_x(pc, slot);
+        pc.advance(p, W, units, ksplit, spu, KS, UM);
+      }
+      refilled = true;
+      auto comp = [](const float4& v, int i) {
+        return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+      };
+#pragma unroll
+      for (int jp = 0; jp < 4; ++jp)
+#pragma unroll
+        for (int rt = 0; rt < 2; ++rt)
+#pragma unroll
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t wa = wr[jp][rt][2 * h], wb = wr[jp][rt][2 * h + 1];
+            const uint32_t wa8 = wa >> 8, wb8 = wb >> 8;
+            float dd[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_f16_16816(dd, codes_lo_f16x2(wa), codes_lo_f16x2(wb), codes_hi_f16x2(wa),
+                          codes_hi_f16x2(wb), bpr[jp][h].x, bpr[jp][h].y);
+            mma_f16_16816(dd, codes_lo_f16x2(wa8), codes_lo_f16x2(wb8), codes_hi_f16x2(wa8),
+                          codes_hi_f16x2(wb8), bpr[jp][h].z, bpr[jp][h].w);
+            const int g = 2 * jp + h;
+            const float s0 = comp(scr[rt][0][g >> 2], g & 3), s1 = comp(scr[rt][1][g >> 2], g & 3);
+            const float b0 = comp(bir[rt][0][g >> 2], g & 3), b1 = comp(bir[rt][1][g >> 2], g & 3);
+            accp[0][rt][0] = fmaf(s0 * xvr[jp][h].y, dd[0] + dd[1], fmaf(b0, xvr[jp][h].x, accp[0][rt][0]));
+            accp[0][rt][1] = fmaf(s1 * xvr[jp][h].y, dd[2] + dd[3], fmaf(b1, xvr[jp][h].x, accp[0][rt][1]));
+          }
+    } else if constexpr (PC) {
       // B column gid is part (gid & 1) of activation row gid >> 1; lane tq
       // scales and sums row tq's product
       // the stage's activations: staged with the weights, or read through L1
@@ -940,7 +1017,7 @@ __global__ void __launch_bounds__(kGemvWarps * 32, (NMAT == 1 && NT == 1) ? 4 : 
     b_ready = next_same_unit;
     }  // PC
     __syncwarp();
-    if (lane == 0 && pc.u < units) {
+    if (lane == 0 && !refilled && pc.u < units) {
       issue_w(pc, slot);
       issue_x(pc, slot);
       pc.advance(p, W, units, ksplit, spu, KS, UM);
