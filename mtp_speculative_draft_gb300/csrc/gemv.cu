@@ -349,15 +349,40 @@ __global__ void __launch_bounds__(kRowArgmaxThreads)
   __shared__ unsigned long long red[kRowArgmaxThreads / 32];
   const int r = blockIdx.y;
   float* row = logits + (size_t)r * V;
-  const int per = (V + gridDim.x - 1) / gridDim.x;
+  // slices of whole octets; a thread's octet is read with two 16-byte loads
+  // when the row allows it (one round trip instead of one per logit)
+  const int per = ((V + gridDim.x - 1) / gridDim.x + 7) / 8 * 8;
   const int v0 = blockIdx.x * per, v1 = min(V, v0 + per);
+  const bool vec = (V & 3) == 0 && (reinterpret_cast<uintptr_t>(logits) & 15) == 0;
   unsigned long long best = 0ull;  // below any real key
-  for (int v = v0 + threadIdx.x; v < v1; v += blockDim.x) {
-    float l = row[v] * mult;
-    if (cap > 0.f) l = cap * tanhf(l / cap);
-    row[v] = l;
-    const unsigned long long k = argmax_key(l, v);
-    best = k > best ? k : best;
+  for (int v8 = v0 + threadIdx.x * 8; v8 < v1; v8 += blockDim.x * 8) {
+    float l[8];
+    const bool full = vec && v8 + 8 <= v1;
+    if (full) {
+      const float4 a = *reinterpret_cast<const float4*>(row + v8);
+      const float4 b = *reinterpret_cast<const float4*>(row + v8 + 4);
+      l[0] = a.x; l[1] = a.y; l[2] = a.z; l[3] = a.w;
+      l[4] = b.x; l[5] = b.y; l[6] = b.z; l[7] = b.w;
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) l[i] = v8 + i < v1 ? row[v8 + i] : 0.f;
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      l[i] *= mult;
+      if (cap > 0.f) l[i] = cap * tanhf(l[i] / cap);
+    }
+    if (full) {
+      *reinterpret_cast<float4*>(row + v8) = make_float4(l[0], l[1], l[2], l[3]);
+      *reinterpret_cast<float4*>(row + v8 + 4) = make_float4(l[4], l[5], l[6], l[7]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (v8 + i < v1) {
+        if (!full) row[v8 + i] = l[i];
+        const unsigned long long k = argmax_key(l[i], v8 + i);
+        best = k > best ? k : best;
+      }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
