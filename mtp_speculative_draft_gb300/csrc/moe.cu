@@ -52,7 +52,8 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterPara
   pdl_launch_dependents();
 
   float ss = 0.f;
-  for (int k = tid * 4; k < H; k += kRouterThreads * 4) {
+#pragma unroll 4
+  for (int k = tid * 4; k < H; k += kRouterThreads * 4) {  // loads issued together
     const float4 v = __ldcg(reinterpret_cast<const float4*>(r.u1 + k));
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
@@ -62,6 +63,7 @@ __global__ void __launch_bounds__(kRouterThreads) router_kernel(const RouterPara
   float tot = 0.f;
   for (int w = 0; w < kRouterThreads / 32; ++w) tot += red[w];
   const float inv = rsqrtf(tot / (float)H + r.eps);
+#pragma unroll 8
   for (int k = tid; k < H; k += kRouterThreads) fsm[k] = __ldcg(r.u1 + k) * inv * r.post_norm[k];
   __syncthreads();
 

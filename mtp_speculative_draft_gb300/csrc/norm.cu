@@ -66,7 +66,8 @@ __global__ void __launch_bounds__(kNormThreads) norm_pack_kernel(const NormPackA
     const float* row = seg_row(s, c, a.err);
     const float* dl = s.delta ? s.delta + (size_t)c * s.src_ld : nullptr;
     float ss = 0.f;
-    for (int k = threadIdx.x * 4; k < s.dim; k += kNormThreads * 4) {
+#pragma unroll 4
+    for (int k = threadIdx.x * 4; k < s.dim; k += kNormThreads * 4) {  // loads issued together
       float4 v = *reinterpret_cast<const float4*>(row + k);
       if (dl) {
         const float4 d = *reinterpret_cast<const float4*>(dl + k);
