@@ -464,18 +464,34 @@ static cudaLaunchAttribute pdl_attr_ct() {
 
 static int tc_bn_for_rows(int rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 : rows <= 64 ? 64 : 128; }
 
-// Split-K count that brings the grid near one CTA per SM, with at least 8
-// stages per split.
+// Split-K count (at least 8 stages per split).  One CTA runs per SM, so the
+// GEMM takes ceil(CTAs / SMs) waves of one split's K stages plus a fixed
+// cost per wave (TMEM allocation, pipeline fill, epilogue: about 4 stages);
+// each further split also writes (and the next kernel reads) one more f32
+// partial of rows x N, counted in waves of one K stage (about 4.8 MB of HBM
+// traffic each, as measured at 128 x 128 tiles).  The split count with the
+// lowest total wins (eh_proj at 512 rows: 4 splits in 5 waves of 40 stages
+// instead of 2 waves of 160).
 static int tc_splits(int tiles, int rows, int K) {
   const int bn = tc_bn_for_rows(rows);
   const int ctas = tiles * ((rows + bn - 1) / bn);
   const int KS = K / 64;
-  int ns = (sm_count() + ctas - 1) / ctas;
   const int cap = KS / 8 > 1 ? KS / 8 : 1;
-  if (ns > cap) ns = cap;
-  if (ns < 1) ns = 1;
-  const int per = (KS + ns - 1) / ns;
-  return (KS + per - 1) / per;
+  const int sms = sm_count();
+  const double split_cost = (double)rows * tiles * 128 * 8.0 / 4.8e6;
+  int best = 1;
+  double best_cost = 1e300;
+  for (int ns = 1; ns <= cap; ++ns) {
+    const int per = (KS + ns - 1) / ns;
+    const int n = (KS + per - 1) / per;  // no empty split
+    const long long waves = ((long long)ctas * n + sms - 1) / sms;
+    const double cost = (double)waves * (per + 4) + (n - 1) * split_cost;
+    if (cost < best_cost - 1e-9) {
+      best_cost = cost;
+      best = n;
+    }
+  }
+  return best;
 }
 
 template <int BN>
