@@ -472,6 +472,9 @@ static int tc_bn_for_rows(int rows) { return rows <= 16 ? 16 : rows <= 32 ? 32 :
 // traffic each, as measured at 128 x 128 tiles).  The split count with the
 // lowest total wins (eh_proj at 512 rows: 4 splits in 5 waves of 40 stages
 // instead of 2 waves of 160).
+#ifndef MTP_CATCH_WAVE_COST
+#define MTP_CATCH_WAVE_COST 4  // fixed cost of a wave, in K stages (tuning knob)
+#endif
 static int tc_splits(int tiles, int rows, int K) {
   const int bn = tc_bn_for_rows(rows);
   const int ctas = tiles * ((rows + bn - 1) / bn);
@@ -485,7 +488,7 @@ static int tc_splits(int tiles, int rows, int K) {
     const int per = (KS + ns - 1) / ns;
     const int n = (KS + per - 1) / per;  // no empty split
     const long long waves = ((long long)ctas * n + sms - 1) / sms;
-    const double cost = (double)waves * (per + 4) + (n - 1) * split_cost;
+    const double cost = (double)waves * (per + MTP_CATCH_WAVE_COST) + (n - 1) * split_cost;
     if (cost < best_cost - 1e-9) {
       best_cost = cost;
       best = n;
